@@ -1,0 +1,327 @@
+// The C ABI (include/csa.h): argument validation, workspace carving, TMA
+// tensor-map encoding and kernel launches.  No allocation, no host sync
+// except in csa_check_device_status.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "csa_device.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+size_t score_ws_bytes(int32_t R, int32_t Hi);
+int score_group_rows(int32_t Hi);
+}  // namespace csa
+
+using namespace csa;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) & ~(a - 1); }
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Indexer pool as TMA tensors: data [pages][64 entries][64 B] with the 64-byte
+// swizzle the MMA descriptor expects, and scales [pages][256 B].
+bool encode_idx_maps(const csa_cache_t* c, CUtensorMap* data, CUtensorMap* scale) {
+  if (!get_encode()) return false;
+  const cuuint64_t dims_d[3] = {64, 64, (cuuint64_t)c->num_pages};
+  const cuuint64_t strides_d[2] = {64, CSA_IDX_PAGE_BYTES};
+  const cuuint32_t box_d[3] = {64, 64, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c->idx_pool, dims_d, strides_d, box_d, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  const cuuint64_t dims_s[2] = {256, (cuuint64_t)c->num_pages};
+  const cuuint64_t strides_s[1] = {CSA_IDX_PAGE_BYTES};
+  const cuuint32_t box_s[2] = {256, 1};
+  r = g_encode(scale, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, static_cast<uint8_t*>(c->idx_pool) + 4096, dims_s,
+               strides_s, box_s, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+csa_status_t check_cache(const csa_cache_t* c) {
+  if (!c || !c->kv_pool || !c->idx_pool || !c->page_table) return CSA_ERR_INVALID_ARGUMENT;
+  if (!aligned(c->kv_pool, 128) || !aligned(c->idx_pool, 128) || !aligned(c->page_table, 4))
+    return CSA_ERR_INVALID_ARGUMENT;
+  if (c->num_pages <= 0 || c->num_requests <= 0 || c->max_pages_per_req <= 0) return CSA_ERR_INVALID_ARGUMENT;
+  if (c->pool_ratio != 1 && c->pool_ratio != 2) return CSA_ERR_INVALID_ARGUMENT;
+  return CSA_OK;
+}
+
+csa_status_t check_window(const csa_window_t* w, int32_t rows_per_req) {
+  if (!w) return CSA_OK;
+  if (!w->e4m3 || !w->scale || !aligned(w->e4m3, 16) || !aligned(w->scale, 4)) return CSA_ERR_INVALID_ARGUMENT;
+  if (w->capacity < CSA_WINDOW + (rows_per_req > 0 ? rows_per_req : 1) - 1) return CSA_ERR_INVALID_ARGUMENT;
+  return CSA_OK;
+}
+
+csa_status_t check_rows(const csa_rows_t* r, const csa_cache_t* c) {
+  if (!r || r->num_rows < 0) return CSA_ERR_INVALID_ARGUMENT;
+  if (r->num_rows > 0 && (!r->row_req || !r->row_pos)) return CSA_ERR_INVALID_ARGUMENT;
+  if (r->max_entries < 0 || r->max_rows_per_req < 1) return CSA_ERR_INVALID_ARGUMENT;
+  if ((int64_t)r->max_entries > (int64_t)c->max_pages_per_req * CSA_PAGE_ENTRIES) return CSA_ERR_INVALID_ARGUMENT;
+  return CSA_OK;
+}
+
+size_t scores_ld(int32_t max_entries) { return align_up((size_t)(max_entries > 0 ? max_entries : 1), 64); }
+
+struct DecodeLayout {
+  size_t scores, topk, attn, end;
+};
+DecodeLayout decode_layout(int32_t R, int32_t max_entries, int32_t H) {
+  DecodeLayout L;
+  L.scores = align_up(score_ws_bytes(R, CSA_MAX_IDX_HEADS));
+  L.topk = align_up(L.scores + sizeof(float) * (size_t)R * scores_ld(max_entries));
+  L.attn = align_up(L.topk + sizeof(int32_t) * (size_t)R * CSA_TOPK);
+  L.end = align_up(L.attn + attn_partial_bytes(R, H, attn_choose_splits(R, num_sms())));
+  return L;
+}
+
+csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t Hi, const void* q_idx,
+                       const float* w, float* scores, int64_t ld, void* ws, cudaStream_t stream) {
+  CUtensorMap tm_data, tm_scale;
+  if (!encode_idx_maps(cache, &tm_data, &tm_scale)) return CSA_ERR_CUDA;
+  ScoreArgs a;
+  a.page_table = cache->page_table;
+  a.num_pages = cache->num_pages;
+  a.num_requests = cache->num_requests;
+  a.max_pages = cache->max_pages_per_req;
+  a.P = cache->pool_ratio;
+  a.row_req = rows->row_req;
+  a.row_pos = rows->row_pos;
+  a.num_rows = rows->num_rows;
+  a.Hi = Hi;
+  a.group_rows = score_group_rows(Hi);
+  a.max_entries = rows->max_entries;
+  a.q_idx = static_cast<const uint16_t*>(q_idx);
+  a.w = w;
+  a.scores = scores;
+  a.ld = ld;
+  a.status = static_cast<uint32_t*>(ws);
+  return from_cuda(launch_index_score(a, &tm_data, &tm_scale, num_sms(), stream));
+}
+
+csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
+                      const int32_t* topk, int32_t H, const void* q, float softmax_scale, void* out, float* lse,
+                      void* ws, size_t part_off, cudaStream_t stream) {
+  AttnArgs a;
+  a.kv_pool = static_cast<const uint8_t*>(cache->kv_pool);
+  a.page_table = cache->page_table;
+  a.num_pages = cache->num_pages;
+  a.num_requests = cache->num_requests;
+  a.max_pages = cache->max_pages_per_req;
+  a.P = cache->pool_ratio;
+  a.win_codes = window ? window->e4m3 : nullptr;
+  a.win_scale = window ? window->scale : nullptr;
+  a.win_cap = window ? window->capacity : 0;
+  a.row_req = rows->row_req;
+  a.row_pos = rows->row_pos;
+  a.num_rows = rows->num_rows;
+  a.H = H;
+  a.topk = topk;
+  a.q = static_cast<const uint16_t*>(q);
+  a.softmax_scale = softmax_scale;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.splits = attn_choose_splits(rows->num_rows, num_sms());
+  a.part = a.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + part_off) : nullptr;
+  a.status = static_cast<uint32_t*>(ws);
+  return from_cuda(launch_sparse_attn(a, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int32_t n_heads) {
+  if (num_rows < 0 || max_entries < 0) return 0;
+  const int32_t H = n_heads > 0 ? n_heads : CSA_MAX_HEADS;
+  switch (op) {
+    case CSA_OP_APPEND:
+    case CSA_OP_TOPK:
+      return kStatusBytes;
+    case CSA_OP_INDEX_SCORE:
+      return align_up(score_ws_bytes(num_rows, CSA_MAX_IDX_HEADS));
+    case CSA_OP_SPARSE_ATTN:
+      return align_up(kStatusBytes + attn_partial_bytes(num_rows, H, attn_choose_splits(num_rows, num_sms())));
+    case CSA_OP_DECODE:
+      return decode_layout(num_rows, max_entries, H).end;
+    default:
+      return 0;
+  }
+}
+
+csa_status_t csa_append(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
+                        const int32_t* tok_off, int32_t total_tokens, const void* kv_in, const void* idx_in,
+                        void* pending, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status_t s = check_cache(cache);
+  if (s != CSA_OK) return s;
+  if ((s = check_window(window, 1)) != CSA_OK) return s;
+  if (total_tokens < 0 || !pos0 || !tok_off) return CSA_ERR_INVALID_ARGUMENT;
+  if (total_tokens > 0 && (!kv_in || !idx_in || !aligned(kv_in, 16) || !aligned(idx_in, 16)))
+    return CSA_ERR_INVALID_ARGUMENT;
+  if (cache->pool_ratio == 2 && (!pending || !aligned(pending, 16))) return CSA_ERR_INVALID_ARGUMENT;
+  if (ws && ws_bytes < kStatusBytes) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  AppendArgs a;
+  a.kv_pool = static_cast<uint8_t*>(cache->kv_pool);
+  a.idx_pool = static_cast<uint8_t*>(cache->idx_pool);
+  a.page_table = cache->page_table;
+  a.num_pages = cache->num_pages;
+  a.num_requests = cache->num_requests;
+  a.max_pages = cache->max_pages_per_req;
+  a.P = cache->pool_ratio;
+  a.win_codes = window ? window->e4m3 : nullptr;
+  a.win_scale = window ? window->scale : nullptr;
+  a.win_cap = window ? window->capacity : 1;
+  a.pos0 = pos0;
+  a.tok_off = tok_off;
+  a.total_tokens = total_tokens;
+  a.kv_in = static_cast<const uint16_t*>(kv_in);
+  a.idx_in = static_cast<const uint16_t*>(idx_in);
+  a.pending = static_cast<uint16_t*>(pending);
+  a.status = static_cast<uint32_t*>(ws);
+  return from_cuda(launch_append(a, stream));
+}
+
+csa_status_t csa_index_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t n_idx_heads,
+                             const void* q_idx, const float* w, float* scores, int32_t ld, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+  csa_status_t s = check_cache(cache);
+  if (s != CSA_OK) return s;
+  if ((s = check_rows(rows, cache)) != CSA_OK) return s;
+  if (n_idx_heads < 1 || n_idx_heads > CSA_MAX_IDX_HEADS) return CSA_ERR_UNSUPPORTED;
+  if (rows->num_rows == 0) return CSA_OK;
+  if (!q_idx || !w || !scores || !aligned(q_idx, 16) || !aligned(w, 4) || !aligned(scores, 4))
+    return CSA_ERR_INVALID_ARGUMENT;
+  if (ld < rows->max_entries || ld < 1) return CSA_ERR_INVALID_ARGUMENT;
+  if (!ws || ws_bytes < score_ws_bytes(rows->num_rows, CSA_MAX_IDX_HEADS) || !aligned(ws, 256))
+    return CSA_ERR_WORKSPACE_TOO_SMALL;
+  return run_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, stream);
+}
+
+csa_status_t csa_topk(int32_t num_rows, const float* scores, int32_t ld, const int32_t* n_valid, int32_t max_n,
+                      int32_t k, int32_t* out_idx, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (k != CSA_TOPK) return CSA_ERR_UNSUPPORTED;
+  if (num_rows < 0 || max_n < 0 || ld < max_n || ld < 1) return CSA_ERR_INVALID_ARGUMENT;
+  if (num_rows == 0) return CSA_OK;
+  if (!scores || !n_valid || !out_idx || !aligned(scores, 16) || (ld % 4) != 0) return CSA_ERR_INVALID_ARGUMENT;
+  if (ws && ws_bytes < kStatusBytes) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  TopkArgs a;
+  a.scores = scores;
+  a.ld = ld;
+  a.num_rows = num_rows;
+  a.n_valid = n_valid;
+  a.row_pos = nullptr;
+  a.P = 1;
+  a.max_n = max_n;
+  a.out = out_idx;
+  a.status = static_cast<uint32_t*>(ws);
+  return from_cuda(launch_topk(a, stream));
+}
+
+csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
+                             const int32_t* topk_idx, int32_t n_heads, const void* q, float softmax_scale,
+                             void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status_t s = check_cache(cache);
+  if (s != CSA_OK) return s;
+  if ((s = check_rows(rows, cache)) != CSA_OK) return s;
+  if ((s = check_window(window, rows->max_rows_per_req)) != CSA_OK) return s;
+  if (n_heads < 1 || n_heads > CSA_MAX_HEADS) return CSA_ERR_UNSUPPORTED;
+  if (rows->num_rows == 0) return CSA_OK;
+  if (!topk_idx || !q || !out || !aligned(q, 16) || !aligned(out, 16)) return CSA_ERR_INVALID_ARGUMENT;
+  const size_t need = kStatusBytes + attn_partial_bytes(rows->num_rows, n_heads,
+                                                        attn_choose_splits(rows->num_rows, num_sms()));
+  if (!ws || ws_bytes < need || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, ws, kStatusBytes, stream);
+}
+
+csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
+                        int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
+                        float softmax_scale, void* out, float* lse, int32_t* topk_out, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+  csa_status_t s = check_cache(cache);
+  if (s != CSA_OK) return s;
+  if ((s = check_rows(rows, cache)) != CSA_OK) return s;
+  if ((s = check_window(window, rows->max_rows_per_req)) != CSA_OK) return s;
+  if (n_idx_heads < 1 || n_idx_heads > CSA_MAX_IDX_HEADS || n_heads < 1 || n_heads > CSA_MAX_HEADS)
+    return CSA_ERR_UNSUPPORTED;
+  if (rows->num_rows == 0) return CSA_OK;
+  if (!q_idx || !w || !q || !out || !aligned(q_idx, 16) || !aligned(q, 16) || !aligned(out, 16))
+    return CSA_ERR_INVALID_ARGUMENT;
+  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries, n_heads);
+  if (!ws || ws_bytes < L.end || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* scores = reinterpret_cast<float*>(base + L.scores);
+  int32_t* topk = topk_out ? topk_out : reinterpret_cast<int32_t*>(base + L.topk);
+  const int64_t ld = (int64_t)scores_ld(rows->max_entries);
+  if ((s = run_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, stream)) != CSA_OK) return s;
+  TopkArgs t;
+  t.scores = scores;
+  t.ld = ld;
+  t.num_rows = rows->num_rows;
+  t.n_valid = nullptr;
+  t.row_pos = rows->row_pos;
+  t.P = cache->pool_ratio;
+  t.max_n = rows->max_entries;
+  t.out = topk;
+  t.status = static_cast<uint32_t*>(ws);
+  if ((s = from_cuda(launch_topk(t, stream))) != CSA_OK) return s;
+  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, ws, L.attn, stream);
+}
+
+csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out) {
+  if (!ws || !flags_out) return CSA_ERR_INVALID_ARGUMENT;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
+  uint32_t f = 0;
+  if (cudaMemcpy(&f, ws, sizeof(f), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(f), stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
+  *flags_out = f;
+  if (f & CSA_FLAG_TIMEOUT) return CSA_ERR_TIMEOUT;
+  return f ? CSA_ERR_DEVICE_FAULT : CSA_OK;
+}
+
+const char* csa_status_string(csa_status_t s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case CSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case CSA_ERR_CUDA: return "CUDA launch or runtime error";
+    case CSA_ERR_DEVICE_FAULT: return "device-detected fault (see status flags)";
+    case CSA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+// csa_append: fused pair pooling + FP4 quantisation + paged cache write, and
+// the FP8 window write, for the new tokens of a decode / verify step.
+//
+// [SGL] "DeepSeek-V4.1 Flash on SGLang: from 35 to 873 tokens/s",
+//   "Architecture changes and KV cache compression": three global caches pool
+//   every two tokens into one entry, the last keeps one entry per token; the
+//   entries are FP4, 288 B main KV and 68 B indexer K.
+//   "DSpark adaptation and optimization": pair pooling, quantisation and the
+//   main-KV write are one kernel, reused for index-K; within a request the
+//   previous token is read directly and only the first row needs the saved one.
+// [VLLM] "DeepSeek-V4.1-Flash runs 5.3x faster on vLLM...", "SWA bounded
+//   replay": the window is uncompressed FP8 over the most recent 128 positions.
+//
+// One warp per new token.  Lane l owns latent elements 16l..16l+15 (exactly
+// one NVFP4 block) and key elements 4l..4l+3 (8 lanes per MXFP4 block).
+#include "csa_device.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+
+namespace {
+
+constexpr int kWarps = 8;
+
+// kReadOnly: the source is not written by this kernel (then the read-only
+// data path may be used); the pending buffer is read and written in place.
+template <bool kReadOnly = true>
+__device__ __forceinline__ void load_bf16x16(const uint16_t* src, float (&x)[16]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  const uint4 a = kReadOnly ? __ldg(s) : s[0], b = kReadOnly ? __ldg(s + 1) : s[1];
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <bool kReadOnly = true>
+__device__ __forceinline__ void load_bf16x4(const uint16_t* src, float (&y)[4]) {
+  const uint2* s = reinterpret_cast<const uint2*>(src);
+  const uint2 a = kReadOnly ? __ldg(s) : s[0];
+  y[0] = __uint_as_float(a.x << 16);
+  y[1] = __uint_as_float(a.x & 0xFFFF0000u);
+  y[2] = __uint_as_float(a.y << 16);
+  y[3] = __uint_as_float(a.y & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
+  const int t = blockIdx.x * kWarps + warp_id();
+  if (t >= a.total_tokens) return;
+  const int lane = lane_id();
+
+  // request of token t: the largest b with tok_off[b] <= t
+  int lo = 0, hi = a.num_requests - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.tok_off + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int t0 = __ldg(a.tok_off + b);
+  const int T = __ldg(a.tok_off + b + 1) - t0;
+  const int j = t - t0;
+  if (j < 0 || j >= T) {
+    if (lane == 0) raise_flag(a.status, CSA_FLAG_APPEND);
+    return;
+  }
+  const int p0 = __ldg(a.pos0 + b);
+  const int p = p0 + j;
+  if (p0 < 0 || p < 0) {
+    if (lane == 0) raise_flag(a.status, CSA_FLAG_APPEND);
+    return;
+  }
+
+  float x[16];
+  load_bf16x16(a.kv_in + (size_t)t * D + lane * 16, x);
+
+  // ---- FP8 window slot of this token: scale = amax / 448, codes = E4M3(x / scale)
+  if (a.win_codes != nullptr) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = warp_max(amax);
+    const size_t slot = (size_t)b * a.win_cap + (size_t)(p % a.win_cap);
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    float s = 0.0f;
+    if (amax != 0.0f) {
+      s = __fdiv_rn(amax, 448.0f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) packed[i >> 2] |= e4m3_rne_sat(__fdiv_rn(x[i], s)) << (8 * (i & 3));
+    }
+    *reinterpret_cast<uint4*>(a.win_codes + slot * D + lane * 16) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    if (lane == 0) a.win_scale[slot] = s;
+  }
+
+  // ---- cache entry completed by this token
+  if (p % a.P == a.P - 1) {
+    const int e = p / a.P;
+    float y[4];
+    load_bf16x4(a.idx_in + (size_t)t * DI + lane * 4, y);
+    if (a.P == 2) {
+      const uint16_t* pkv = (j == 0) ? a.pending + (size_t)b * (D + DI) : a.kv_in + (size_t)(t - 1) * D;
+      const uint16_t* pix = (j == 0) ? a.pending + (size_t)b * (D + DI) + D : a.idx_in + (size_t)(t - 1) * DI;
+      float xp[16], yp[4];
+      if (j == 0) {
+        load_bf16x16<false>(pkv + lane * 16, xp);
+        load_bf16x4<false>(pix + lane * 4, yp);
+      } else {
+        load_bf16x16(pkv + lane * 16, xp);
+        load_bf16x4(pix + lane * 4, yp);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = (xp[i] + x[i]) * 0.5f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) y[i] = (yp[i] + y[i]) * 0.5f;
+    }
+    const int lp = e / PAGE, slot = e % PAGE;
+    int page = -1;
+    if (lp < a.max_pages) page = __ldg(a.page_table + (size_t)b * a.max_pages + lp);
+    if (page < 0 || page >= a.num_pages) {
+      if (lane == 0) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
+    } else {
+      // NVFP4 block (this lane's 16 values): S = E4M3(amax/6), codes = e2m1(x/s)
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      const uint32_t S = e4m3_rne_sat(__fdiv_rn(amax, 6.0f));
+      const float s = e4m3_value(S);
+      uint32_t lo32 = 0u, hi32 = 0u;
+      if (s != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) lo32 |= e2m1_rne(__fdiv_rn(x[i], s)) << (4 * i);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hi32 |= e2m1_rne(__fdiv_rn(x[8 + i], s)) << (4 * i);
+      }
+      uint8_t* kvp = a.kv_pool + (size_t)page * KV_PAGE;
+      *reinterpret_cast<uint2*>(kvp + slot * 256 + lane * 8) = make_uint2(lo32, hi32);
+      kvp[KV_SCALE_OFF + slot * 32 + lane] = (uint8_t)S;
+
+      // MXFP4 block of 32 = lanes 8k..8k+7: scale 2^E, E = floor(log2 amax) - 2
+      float am = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 4));
+      const uint32_t E8 = e8m0_block_code(am);
+      uint32_t codes = 0u;
+      if (am != 0.0f) {
+        const float inv = e8m0_inv_scale(E8);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) codes |= e2m1_rne(y[i] * inv) << (4 * i);
+      }
+      uint8_t* ixp = a.idx_pool + (size_t)page * IDX_PAGE;
+      *reinterpret_cast<uint16_t*>(ixp + slot * 64 + lane * 2) = (uint16_t)codes;
+      if ((lane & 7) == 0) ixp[IDX_SCALE_OFF + slot * 4 + (lane >> 3)] = (uint8_t)E8;
+    }
+  }
+
+  // ---- pending token: written by the warp of the request's first new token,
+  // after its own read of the old pending token (so in-place is safe).
+  if (a.P == 2 && j == 0 && ((p0 + T - 1) & 1) == 0) {
+    __syncwarp();
+    const size_t tl = (size_t)t0 + T - 1;
+    const uint4* skv = reinterpret_cast<const uint4*>(a.kv_in + tl * D);
+    const uint4* six = reinterpret_cast<const uint4*>(a.idx_in + tl * DI);
+    uint4* dst = reinterpret_cast<uint4*>(a.pending + (size_t)b * (D + DI));
+    dst[lane] = __ldg(skv + lane);
+    dst[32 + lane] = __ldg(skv + 32 + lane);
+    if (lane < 16) dst[64 + lane] = __ldg(six + lane);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
+  if (a.total_tokens <= 0) return cudaSuccess;
+  const int blocks = (a.total_tokens + kWarps - 1) / kWarps;
+  k_append<<<blocks, kWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

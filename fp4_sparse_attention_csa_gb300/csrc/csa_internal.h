@@ -1,0 +1,84 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/csa.h"
+
+namespace csa {
+
+struct AppendArgs {
+  uint8_t* kv_pool;
+  uint8_t* idx_pool;
+  const int32_t* page_table;
+  int32_t num_pages, num_requests, max_pages, P;
+  uint8_t* win_codes;
+  float* win_scale;
+  int32_t win_cap;
+  const int32_t* pos0;
+  const int32_t* tok_off;
+  int32_t total_tokens;
+  const uint16_t* kv_in;
+  const uint16_t* idx_in;
+  uint16_t* pending;
+  uint32_t* status;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+
+// Indexer score: one CTA walks (request, row group, 128-entry tile) work items.
+struct ScoreArgs {
+  const int32_t* page_table;
+  int32_t num_pages, num_requests, max_pages, P;
+  const int32_t* row_req;
+  const int32_t* row_pos;
+  int32_t num_rows, Hi, group_rows;   // rows scored together per MMA
+  int32_t max_entries;                 // host bound on entries per row
+  const uint16_t* q_idx;               // bf16 [R, Hi, 128]
+  const float* w;                      // [R, Hi]
+  float* scores;                       // [R, ld]
+  int64_t ld;
+  uint32_t* status;
+};
+// tmaps: 3-D tensor maps over idx_pool: [0] data (64 B x 64 entries x pages),
+// [1] scales (256 B x 1 x pages).
+cudaError_t launch_index_score(const ScoreArgs& a, const void* tmap_data, const void* tmap_scale,
+                               int num_sms, cudaStream_t stream);
+
+struct TopkArgs {
+  const float* scores;
+  int64_t ld;
+  int32_t num_rows;
+  const int32_t* n_valid;  // [R] or null (then n(r) comes from row_pos / P)
+  const int32_t* row_pos;
+  int32_t P;
+  int32_t max_n;
+  int32_t* out;            // [R, 512]
+  uint32_t* status;
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
+
+struct AttnArgs {
+  const uint8_t* kv_pool;
+  const int32_t* page_table;
+  int32_t num_pages, num_requests, max_pages, P;
+  const uint8_t* win_codes;
+  const float* win_scale;
+  int32_t win_cap;
+  const int32_t* row_req;
+  const int32_t* row_pos;
+  int32_t num_rows, H;
+  const int32_t* topk;      // [R, 512]
+  const uint16_t* q;        // bf16 [R, H, 512]
+  float softmax_scale;
+  uint16_t* out;            // bf16 [R, H, 512]
+  float* lse;               // [R, H] or null
+  float* part;              // split partials (o, m, l) or null when splits == 1
+  int32_t splits;
+  uint32_t* status;
+};
+cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+size_t attn_partial_bytes(int32_t num_rows, int32_t n_heads, int32_t splits);
+int32_t attn_choose_splits(int32_t num_rows, int num_sms);
+
+}  // namespace csa

@@ -1,0 +1,494 @@
+// csa_index_score: score[r, i] = sum_h w[r,h] * relu(qhat[r,h] . khat[i])
+// over the paged MXFP4 indexer cache, as a block-scaled FP4 tcgen05 MMA.
+//
+// [SGL] "DeepSeek-V4.1 Flash on SGLang: from 35 to 873 tokens/s",
+//   "Architecture changes and KV cache compression": the indexer K entries are
+//   FP4 (68 B) and the indexer picks the top 512 global positions;
+//   "DSpark adaptation and optimization": the valid-length check is fused with
+//   candidate handling (rows only score their visible entries).
+//
+// Two kernels:
+//  k_score_prep  block 0 builds the segment table (a segment = up to
+//                `group_rows` consecutive rows of one request, scored by one
+//                MMA N dimension); blocks 1..R quantise each row's q_idx to
+//                MXFP4 straight into the shared-memory image the MMA reads
+//                (64-byte swizzled K-major rows + one E8M0 byte per 32).
+//  k_index_score persistent, one CTA per SM, 12 warps:
+//                warp 0  TMA producer: two indexer pages (128 entries) per
+//                        work item into an 8-stage ring (data with 64 B swizzle,
+//                        scales plain); the segment's q image by bulk copy.
+//                warp 1  MMA issuer: rearranges the E8M0 bytes into the
+//                        tcgen05 scale-factor layout, tcgen05.cp to TMEM, two
+//                        kind::mxf4 MMAs (K = 64 each) per N chunk of 128.
+//                        A = 128 entries x 128 dims, B = rows*heads x 128 dims,
+//                        D = fp32 [entry lane, row*head column] in TMEM.
+//                warps 4-7, 8-11  epilogue groups (one per TMEM accumulator
+//                        buffer): per entry lane, sum_h w*relu(D) in head order,
+//                        coalesced fp32 score stores.
+#include <cuda.h>
+
+#include "csa_device.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+
+namespace {
+
+struct Seg {
+  int32_t b, r0, nrows, n;
+};
+
+constexpr int kStages = 8;
+constexpr int kThreads = 384;
+constexpr int kTileEntries = 128;
+constexpr int kStageA = 8192;        // 128 entries x 64 B (two pages)
+constexpr int kStageSF = 512;        // 128 entries x 4 E8M0 bytes (raw page order)
+constexpr int kMaxN = CSA_MAX_ROW_GROUP_COLS;  // rows x padded heads per MMA group
+constexpr int kQData = kMaxN * 64;   // 24576
+constexpr int kQSF = kMaxN * 4;      // 1536
+constexpr int kTmemSF = 0, kTmemD = 32;
+
+struct ScoreSmem {
+  uint8_t a[kStages][kStageA];                 // 1024-aligned
+  uint8_t qdata[2][kQData];                    // 1024-aligned (24576 = 24 * 1024)
+  uint8_t sfa_raw[kStages][kStageSF];
+  uint8_t sfa_atom[kStages][kStageSF];
+  uint8_t sfb_raw[2][kQSF];
+  uint8_t sfb_atom[2][kQSF];
+  uint64_t full[kStages], empty[kStages];
+  uint64_t tfull[2], tempty[2];
+  uint64_t qfull[2], qempty[2];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+__host__ __device__ inline int hi_pad(int Hi) { return (Hi + 7) & ~7; }
+// MMA N for a group of N score columns: a multiple of 16, at least 64
+// (columns past N multiply stale rows of the B buffer and are never read).
+__host__ __device__ inline int mma_n(int N) { return N < 64 ? 64 : (N + 15) & ~15; }
+
+// Workspace carve-out of the score step (after the status word).
+struct ScoreWs {
+  int32_t* nseg;       // [1] segments, [2] total items at [1]
+  Seg* seg;            // [R]
+  int32_t* tile_pref;  // [R + 1]
+  uint8_t* qimg;       // [R * Hi_pad * 64]
+  uint8_t* qsf;        // [R * Hi_pad * 4]
+};
+
+__device__ __host__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+__host__ __device__ inline ScoreWs carve_score_ws(uint8_t* base, int R, int Hi) {
+  ScoreWs w;
+  size_t o = kStatusBytes;
+  w.nseg = reinterpret_cast<int32_t*>(base + o);
+  o = align256(o + 16);
+  w.seg = reinterpret_cast<Seg*>(base + o);
+  o = align256(o + sizeof(Seg) * (size_t)(R > 0 ? R : 1));
+  w.tile_pref = reinterpret_cast<int32_t*>(base + o);
+  o = align256(o + sizeof(int32_t) * (size_t)(R + 1));
+  w.qimg = base + o;
+  o = align256(o + (size_t)R * hi_pad(Hi) * 64);
+  w.qsf = base + o;
+  return w;
+}
+
+__device__ __forceinline__ int lower_bound_req(const int32_t* row_req, int R, int v) {
+  int lo = 0, hi = R;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(row_req + mid) < v) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim = 128).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* sm_warp) {
+  const int lane = lane_id(), w = warp_id();
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm_warp[w] = x;
+  __syncthreads();
+  int off = 0, tot = 0;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+    if (i < w) off += sm_warp[i];
+    tot += sm_warp[i];
+  }
+  __syncthreads();
+  *total = tot;
+  return off + x - v;
+}
+
+__global__ void __launch_bounds__(128) k_score_prep(ScoreArgs a, uint8_t* ws) {
+  const int R = a.num_rows, Hi = a.Hi, Hp = hi_pad(Hi);
+  ScoreWs W = carve_score_ws(ws, R, Hi);
+  if (blockIdx.x == 0) {
+    // ---- segment table: rows grouped by request, at most group_rows per segment
+    __shared__ int sm_warp[4];
+    __shared__ int carry_seg;
+    if (threadIdx.x == 0) carry_seg = 0;
+    __syncthreads();
+    for (int base = 0; base < R; base += 128) {
+      const int r = base + threadIdx.x;
+      int start = 0;
+      int b = 0, k_in_req = 0;
+      if (r < R) {
+        b = __ldg(a.row_req + r);
+        if (b < 0 || b >= a.num_requests || (r > 0 && __ldg(a.row_req + r - 1) > b))
+          raise_flag(a.status, CSA_FLAG_ROW_INVALID);
+        k_in_req = r - lower_bound_req(a.row_req, R, b);
+        start = (k_in_req % a.group_rows) == 0;
+      }
+      int tot;
+      const int sid = block_exclusive_scan(start, &tot, sm_warp) + carry_seg;
+      if (start) {
+        const int rend = lower_bound_req(a.row_req, R, b + 1);
+        const int nrows = max(0, min(a.group_rows, rend - r));
+        int n = 0;
+        for (int k = 0; k < nrows; ++k) n = max(n, (__ldg(a.row_pos + r + k) + 1) / a.P);
+        const int cap = min(a.max_entries, a.max_pages * PAGE);
+        if (n > cap || b < 0 || b >= a.num_requests) {
+          raise_flag(a.status, CSA_FLAG_ROW_INVALID);
+          n = (b < 0 || b >= a.num_requests) ? 0 : min(n, cap);
+        }
+        Seg s;
+        s.b = b; s.r0 = r; s.nrows = nrows; s.n = n;
+        W.seg[sid] = s;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) carry_seg += tot;
+      __syncthreads();
+    }
+    const int S = carry_seg;
+    // ---- tile prefix over segments
+    __shared__ int carry_t;
+    if (threadIdx.x == 0) carry_t = 0;
+    __syncthreads();
+    for (int base = 0; base < S; base += 128) {
+      const int s = base + threadIdx.x;
+      const int t = (s < S) ? (W.seg[s].n + kTileEntries - 1) / kTileEntries : 0;
+      int tot;
+      const int ex = block_exclusive_scan(t, &tot, sm_warp) + carry_t;
+      if (s < S) W.tile_pref[s] = ex;
+      __syncthreads();
+      if (threadIdx.x == 0) carry_t += tot;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      W.tile_pref[S] = carry_t;
+      W.nseg[0] = S;
+      W.nseg[1] = carry_t;
+    }
+    return;
+  }
+  // ---- MXFP4 quantisation of row r's indexer queries into the MMA B image.
+  // Head h of row r is image row n = r*Hp + h; its 4 blocks of 32 values are
+  // the 4 16-byte chunks of a 64-byte row, stored with the 64-byte swizzle
+  // (chunk c at c ^ ((n >> 1) & 3)) that the MMA descriptor expects.
+  const int r = blockIdx.x - 1;
+  for (int job = threadIdx.x; job < Hp * 4; job += blockDim.x) {
+    const int h = job >> 2, kb = job & 3;
+    const size_t n = (size_t)r * Hp + h;
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t E8 = 0u;
+    if (h < Hi) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.q_idx + ((size_t)r * Hi + h) * DI + kb * 32);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = __ldg(src + i);
+        const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[8 * i + 2 * k] = __uint_as_float(ww[k] << 16);
+          v[8 * i + 2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u);
+        }
+      }
+      float am = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(v[i]));
+      E8 = e8m0_block_code(am);
+      if (am != 0.0f) {
+        const float inv = e8m0_inv_scale(E8);
+        uint32_t wv[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) wv[i >> 3] |= e2m1_rne(v[i] * inv) << (4 * (i & 7));
+        out = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+    }
+    const int sw = kb ^ (int)((n >> 1) & 3);
+    *reinterpret_cast<uint4*>(W.qimg + n * 64 + sw * 16) = out;
+    W.qsf[n * 4 + kb] = (uint8_t)E8;
+  }
+}
+
+// Rearrange 4-byte scale words of up to 128 rows into the tcgen05 scale-factor
+// atom: the word of row m goes to word 4*(m % 32) + m / 32 (32 rows x 16 B,
+// row m%32 holding the words of rows m%32, +32, +64, +96).
+__device__ __forceinline__ void sf_to_atom(const uint8_t* raw, uint8_t* atom, int lane) {
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(raw);
+  uint4 v;
+  v.x = src[lane];
+  v.y = src[lane + 32];
+  v.z = src[lane + 64];
+  v.w = src[lane + 96];
+  reinterpret_cast<uint4*>(atom)[lane] = v;
+}
+
+__device__ __forceinline__ int find_seg(const int32_t* pref, int S, int item) {
+  int lo = 0, hi = S - 1;  // largest s with pref[s] <= item
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Next (segment, tile) in item order, skipping segments without tiles.
+__device__ __forceinline__ void advance(const int32_t* pref, int S, int& seg, int& tile) {
+  if (++tile == pref[seg + 1] - pref[seg]) {
+    tile = 0;
+    ++seg;
+    while (seg < S && pref[seg + 1] == pref[seg]) ++seg;
+  }
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ScoreSmem& sm, uint32_t* status) {
+  if (mbar_wait(bar, parity)) return true;
+  raise_flag(status, CSA_FLAG_TIMEOUT);
+  atomicExch(&sm.abort_flag, 1);
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_index_score(ScoreArgs a, uint8_t* ws, const __grid_constant__ CUtensorMap tmap_data,
+                  const __grid_constant__ CUtensorMap tmap_scale) {
+  extern __shared__ uint8_t smem_raw[];
+  ScoreSmem& sm = *reinterpret_cast<ScoreSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int Hi = a.Hi, Hp = hi_pad(Hi);
+  ScoreWs W = carve_score_ws(ws, a.num_rows, Hi);
+  const int warp = warp_id(), lane = lane_id();
+
+  const int S = W.nseg[0], total = W.nseg[1];
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  const int beg = min(total, (int)blockIdx.x * per), end = min(total, beg + per);
+
+  // TMEM accumulator buffers: D(d) at column kTmemD + d * dstride
+  const int npad_max = mma_n(a.group_rows * Hp);       // largest MMA N of any segment
+  const int dstride = npad_max + 16;
+  const int nbuf = (2 * dstride <= 512 - kTmemD) ? 2 : 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&sm.tfull[d], 1);
+      mbar_init(&sm.tempty[d], 4);
+      mbar_init(&sm.qfull[d], 1);
+      mbar_init(&sm.qempty[d], 1);
+    }
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(&sm.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (beg < end) {
+    if (warp == 0 && lane == 0) {
+      // ================= TMA producer =================
+      int seg = find_seg(W.tile_pref, S, beg);
+      int tile = beg - W.tile_pref[seg];
+      int nq = 0;
+      for (int it = 0; beg + it < end; ++it) {
+        if (sm.abort_flag) break;
+        const Seg sg = W.seg[seg];
+        if (it == 0 || tile == 0) {
+          const int par = nq & 1;
+          if (nq >= 2 && !wait_or_abort(&sm.qempty[par], ((nq >> 1) - 1) & 1, sm, a.status)) break;
+          const uint32_t bytes_d = (uint32_t)(sg.nrows * Hp * 64), bytes_s = (uint32_t)(sg.nrows * Hp * 4);
+          mbar_expect_tx(&sm.qfull[par], bytes_d + bytes_s);
+          if (bytes_d > 0) {   // nrows in [1, group_rows] whenever the segment has tiles
+            bulk_load(sm.qdata[par], W.qimg + (size_t)sg.r0 * Hp * 64, bytes_d, &sm.qfull[par]);
+            bulk_load(sm.sfb_raw[par], W.qsf + (size_t)sg.r0 * Hp * 4, bytes_s, &sm.qfull[par]);
+          }
+          ++nq;
+        }
+        const int s = it % kStages;
+        if (it >= kStages && !wait_or_abort(&sm.empty[s], ((it / kStages) - 1) & 1, sm, a.status)) break;
+        const int npages = (sg.n + PAGE - 1) / PAGE;
+        int pg[2] = {-1, -1};
+        uint32_t bytes = 0;
+        for (int h = 0; h < 2; ++h) {
+          const int lp = 2 * tile + h;
+          if (lp < npages) {
+            const int p = __ldg(a.page_table + (size_t)sg.b * a.max_pages + lp);
+            if (p >= 0 && p < a.num_pages) {
+              pg[h] = p;
+              bytes += 4096 + 256;
+            } else {
+              raise_flag(a.status, CSA_FLAG_PAGE_OOB);
+            }
+          }
+        }
+        mbar_expect_tx(&sm.full[s], bytes);
+        for (int h = 0; h < 2; ++h) {
+          if (pg[h] < 0) continue;
+          tma_load_3d(sm.a[s] + 4096 * h, &tmap_data, &sm.full[s], 0, 0, pg[h]);
+          tma_load_2d(sm.sfa_raw[s] + 256 * h, &tmap_scale, &sm.full[s], 0, pg[h]);
+        }
+        advance(W.tile_pref, S, seg, tile);
+      }
+    } else if (warp == 1) {
+      // ================= MMA issuer =================
+      int seg = find_seg(W.tile_pref, S, beg);
+      int tile = beg - W.tile_pref[seg];
+      int nq = 0, par = 0;
+      int N = 0;
+      for (int it = 0; beg + it < end; ++it) {
+        if (sm.abort_flag) break;
+        const Seg sg = W.seg[seg];
+        if (it == 0 || tile == 0) {
+          par = nq & 1;
+          if (!wait_or_abort(&sm.qfull[par], (nq >> 1) & 1, sm, a.status)) break;
+          N = sg.nrows * Hp;
+          const int natoms = (N + 127) / 128;
+          for (int c = 0; c < natoms; ++c) {
+            // rows beyond N inside the last atom hold stale bytes; their D
+            // columns are never read.
+            sf_to_atom(sm.sfb_raw[par] + 512 * c, sm.sfb_atom[par] + 512 * c, lane);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc_fence_after();
+            for (int c = 0; c < natoms; ++c)
+              tmem_cp_32x128b_x4(tmem + kTmemSF + 8 + 12 * par + 4 * c,
+                                 smem_desc(smem_u32(sm.sfb_atom[par] + 512 * c), 16, 128, kSwizzleNone));
+          }
+          ++nq;
+        }
+        const int s = it % kStages;
+        if (!wait_or_abort(&sm.full[s], (it / kStages) & 1, sm, a.status)) break;
+        sf_to_atom(sm.sfa_raw[s], sm.sfa_atom[s], lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int d = it % nbuf, k = it / nbuf;
+        if (k >= 1 && !wait_or_abort(&sm.tempty[d], (k - 1) & 1, sm, a.status)) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sfa = tmem + kTmemSF + 4 * d;
+          tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[s]), 16, 128, kSwizzleNone));
+          const uint32_t abase = smem_u32(sm.a[s]);
+          const uint32_t bbase = smem_u32(sm.qdata[par]);
+          const uint32_t dcol = tmem + kTmemD + d * dstride;
+          const int Nm = mma_n(N);
+          for (int c = 0; c * 128 < Nm; ++c) {
+            const uint32_t Nc = (uint32_t)min(128, Nm - c * 128);
+            const uint32_t sfb = tmem + kTmemSF + 8 + 12 * par + 4 * c;
+            const uint32_t bchunk = bbase + c * 128 * 64;
+            mma_mxf4(dcol + c * 128, smem_desc(abase, 16, 512, kSwizzle64B),
+                     smem_desc(bchunk, 16, 512, kSwizzle64B), idesc_mxf4(128, Nc, 0, 0), sfa, sfb, 0u);
+            mma_mxf4(dcol + c * 128, smem_desc(abase + 32, 16, 512, kSwizzle64B),
+                     smem_desc(bchunk + 32, 16, 512, kSwizzle64B), idesc_mxf4(128, Nc, 2, 2), sfa, sfb, 1u);
+          }
+          tc_commit(&sm.empty[s]);
+          tc_commit(&sm.tfull[d]);
+        }
+        const bool seg_end = (tile + 1 == (W.tile_pref[seg + 1] - W.tile_pref[seg])) || (beg + it + 1 == end);
+        if (seg_end && lane == 0) tc_commit(&sm.qempty[par]);
+        __syncwarp();
+        advance(W.tile_pref, S, seg, tile);
+      }
+    } else if (warp >= 4 && (warp - 4) / 4 < nbuf) {
+      // ================= epilogue =================
+      const int grp = (warp - 4) / 4;
+      const int q = warp & 3;                       // TMEM lane quarter of this warp
+      const int m = 32 * q + lane;                  // entry within the tile
+      int seg = find_seg(W.tile_pref, S, beg);
+      int tile = beg - W.tile_pref[seg];
+      for (int it = 0; beg + it < end; ++it) {
+        const Seg sg = W.seg[seg];
+        const int cur_tile = tile;
+        advance(W.tile_pref, S, seg, tile);
+        if (it % nbuf != grp) continue;
+        if (sm.abort_flag) break;
+        const int d = it % nbuf, k = it / nbuf;
+        if (!wait_or_abort(&sm.tfull[d], k & 1, sm, a.status)) break;
+        tc_fence_after();
+        const int i = cur_tile * kTileEntries + m;
+        const int lp = i / PAGE;
+        bool page_ok = false;
+        if (i < sg.n) {
+          const int p = __ldg(a.page_table + (size_t)sg.b * a.max_pages + lp);
+          page_ok = (p >= 0 && p < a.num_pages);
+        }
+        const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + kTmemD + d * dstride;
+        for (int kr = 0; kr < sg.nrows; ++kr) {
+          const int r = sg.r0 + kr;
+          const float* wr = a.w + (size_t)r * Hi;
+          float acc = 0.0f;
+          for (int h0 = 0; h0 < Hi; h0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(dbase + kr * Hp + h0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (h0 + j < Hi) {
+                const float dot = __uint_as_float(v[j]);
+                const float rl = dot > 0.0f ? dot : 0.0f;
+                acc = __fadd_rn(acc, __fmul_rn(__ldg(wr + h0 + j), rl));
+              }
+            }
+          }
+          const int nr = (__ldg(a.row_pos + r) + 1) / a.P;
+          if (i < nr && i < sg.n) a.scores[(size_t)r * a.ld + i] = page_ok ? acc : -INFINITY;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tempty[d]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+size_t score_ws_bytes(int32_t R, int32_t Hi) {
+  ScoreWs w = carve_score_ws(nullptr, R, Hi);
+  return reinterpret_cast<size_t>(w.qsf) + align256((size_t)R * hi_pad(Hi) * 4);
+}
+
+int score_group_rows(int32_t Hi) { return kMaxN / hi_pad(Hi); }
+
+cudaError_t launch_index_score(const ScoreArgs& a, const void* tmap_data, const void* tmap_scale, int num_sms,
+                               cudaStream_t stream) {
+  if (a.num_rows <= 0) return cudaSuccess;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(a.status);
+  k_score_prep<<<1 + a.num_rows, 128, 0, stream>>>(a, ws);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(ScoreSmem) + 1024;
+  e = cudaFuncSetAttribute(k_index_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const CUtensorMap* td = reinterpret_cast<const CUtensorMap*>(tmap_data);
+  const CUtensorMap* ts = reinterpret_cast<const CUtensorMap*>(tmap_scale);
+  k_index_score<<<num_sms, kThreads, smem, stream>>>(a, ws, *td, *ts);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,214 @@
+/*
+ * csa.h -- C ABI of the compressed-sparse-attention (CSA) decode hot path for
+ * GB300 (sm_103a): FP4 paged cache append, FP4 indexer score, exact top-512,
+ * and sparse MQA attention over the selected FP4 entries plus an FP8 window.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [SGL]  "DeepSeek-V4.1 Flash on SGLang: from 35 to 873 tokens/s"
+ *         - "Architecture changes and KV cache compression": global KV caches
+ *           store FP4 entries of 288 B (main KV) and 68 B (indexer K); three
+ *           caches pool every two tokens into one entry, one keeps one entry
+ *           per token; only the top 512 global positions take part in
+ *           attention; 890 B per token is the logical size and the allocated
+ *           layout may differ.
+ *         - "Small-operator fusion and GEMV": pooling, FP4 quantisation and the
+ *           cache write are fused; per-step request indices are built once and
+ *           shared across layers.
+ *         - "DSpark adaptation and optimization": up to 6 verify rows per
+ *           request; the valid-length check is fused with candidate handling;
+ *           post-top-k score check, invalid-position filtering and KV page
+ *           address translation are one step; pair pooling, quantisation and
+ *           the main-KV write are one kernel, the first row reading the saved
+ *           previous token.
+ *  [VLLM] "DeepSeek-V4.1-Flash runs 5.3x faster on vLLM after three weeks of
+ *         optimization" - "SWA bounded replay...": the local window is
+ *         uncompressed FP8 over the most recent 128 positions; "CUDA graphs and
+ *         the new kernels": decode steps are captured in CUDA graphs.
+ *
+ * FORMAT (this library's byte layout; the pages fix only the entry sizes)
+ *  - e2m1 codes: bit 3 sign, magnitude 0..7 = {0,.5,1,1.5,2,3,4,6}; element
+ *    2j in the low nibble of byte j.  E4M3 = OCP FP8 "fn" (max 448);
+ *    E8M0 = 2^(code-127).
+ *  - Main-KV entry (288 B): 512 e2m1 + one E4M3 scale per 16 values (NVFP4:
+ *    s = E4M3(amax/6), codes = RNE(x/s)).
+ *  - Indexer-K entry (68 B): 128 e2m1 + one E8M0 scale per 32 values (MXFP4,
+ *    OCP MX rule: scale 2^(floor(log2 amax) - 2)).
+ *  - Pages of 64 entries, data block then scale block, so every TMA stride is
+ *    a multiple of 16 B:
+ *      main-KV page 18432 B: entry e data at 256*e, scales at 16384 + 32*e
+ *      indexer page  4352 B: entry e data at  64*e, scales at  4096 +  4*e
+ *    page_table[b*max_pages_per_req + j] = physical page of request b's j-th
+ *    logical page; the same id indexes both pools.
+ *  - Entry e of a request pools tokens P*e .. P*e+P-1 (P = pool_ratio, 2 or 1):
+ *    x = (t0 + t1) * 0.5 in fp32.  A row at position t sees entries
+ *    e < floor((t+1)/P) and window positions max(0,t-127)..t.
+ *  - FP8 window ring: token at position p of request b lives in slot
+ *    b*capacity + p % capacity: 512 E4M3 codes + one fp32 scale (amax/448).
+ *
+ * CONVENTIONS
+ *  - All pointers are device pointers unless marked "host".  The caller owns
+ *    and frees every buffer; the library never allocates, frees or
+ *    synchronises (except csa_check_device_status).  All work is enqueued on
+ *    `stream`, so calls can be captured in a CUDA graph.
+ *  - bf16 tensors are passed as void* (IEEE bfloat16 bit patterns).
+ *  - Pools, pages, q, out and the window must be 16-byte aligned; the pools
+ *    128-byte aligned.
+ *  - Host-detectable errors return before any launch.  Faults only the device
+ *    can see (page id out of range, a row seeing more entries than its pages
+ *    hold, rows not grouped by request, a top-k index outside the row's
+ *    visible range, a bounded wait that ran out) never trap: the unit is
+ *    skipped (outputs zero / -1) and a flag is OR-ed into the status word at
+ *    the head of the workspace; read it with csa_check_device_status().
+ *  - Calls that run concurrently need distinct workspaces.
+ */
+#ifndef CSA_H
+#define CSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CSA_API __attribute__((visibility("default")))
+#else
+#define CSA_API
+#endif
+
+#define CSA_D                 512   /* main latent width                        */
+#define CSA_DI                128   /* indexer key width                        */
+#define CSA_TOPK              512   /* selected global positions per row        */
+#define CSA_WINDOW            128   /* FP8 window positions per row             */
+#define CSA_PAGE_ENTRIES      64
+#define CSA_KV_ENTRY_BYTES    288
+#define CSA_IDX_ENTRY_BYTES   68
+#define CSA_KV_PAGE_BYTES     18432
+#define CSA_IDX_PAGE_BYTES    4352
+#define CSA_MAX_HEADS         64    /* attention heads per row (16, 32 or 64)   */
+#define CSA_MAX_IDX_HEADS     128   /* indexer heads per row                    */
+#define CSA_MAX_ROW_GROUP_COLS 384  /* rows-per-request x indexer heads scored
+                                       together; larger groups are split        */
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARGUMENT = 1,    /* NULL / misaligned pointer, bad size       */
+  CSA_ERR_UNSUPPORTED = 2,         /* shape outside the compiled limits         */
+  CSA_ERR_WORKSPACE_TOO_SMALL = 3,
+  CSA_ERR_CUDA = 4,                /* a launch or runtime call failed           */
+  CSA_ERR_DEVICE_FAULT = 5,        /* device status word has a fault flag       */
+  CSA_ERR_TIMEOUT = 6              /* device status word has the timeout flag   */
+} csa_status_t;
+
+/* Device status flags (csa_check_device_status). */
+#define CSA_FLAG_PAGE_OOB    0x1u   /* page id or logical page out of range     */
+#define CSA_FLAG_ROW_INVALID 0x2u   /* bad row_req / rows not grouped / n > cap  */
+#define CSA_FLAG_TOPK_OOB    0x4u   /* selected index outside the visible range */
+#define CSA_FLAG_TIMEOUT     0x8u   /* a bounded device wait ran out             */
+#define CSA_FLAG_APPEND      0x10u  /* token offsets inconsistent with total    */
+
+/* Paged FP4 cache (caller-owned device memory). */
+typedef struct {
+  void*          kv_pool;          /* num_pages * 18432 B, 128-B aligned          */
+  void*          idx_pool;         /* num_pages *  4352 B, 128-B aligned          */
+  const int32_t* page_table;       /* [num_requests, max_pages_per_req]           */
+  int32_t        num_pages;
+  int32_t        num_requests;
+  int32_t        max_pages_per_req;
+  int32_t        pool_ratio;       /* 2 (pair pooled) or 1 (one entry per token)  */
+} csa_cache_t;
+
+/* FP8 local window ring. */
+typedef struct {
+  uint8_t* e4m3;                   /* [num_requests, capacity, 512]               */
+  float*   scale;                  /* [num_requests, capacity]                    */
+  int32_t  capacity;               /* >= 128 + (rows per request) - 1             */
+} csa_window_t;
+
+/* Query rows of one decode step, built once per step and shared by every
+ * layer that reads the same cache ([SGL] "Small-operator fusion and GEMV"). */
+typedef struct {
+  int32_t        num_rows;         /* R                                           */
+  const int32_t* row_req;          /* [R] request of each row, non-decreasing      */
+  const int32_t* row_pos;          /* [R] token position of each row              */
+  int32_t        max_entries;      /* host bound: max over rows of (pos+1)/P      */
+  int32_t        max_rows_per_req; /* host bound on rows sharing one request      */
+} csa_rows_t;
+
+/* Workspace sizing: op = one of the CSA_OP_* values. */
+enum { CSA_OP_APPEND = 0, CSA_OP_INDEX_SCORE = 1, CSA_OP_TOPK = 2,
+       CSA_OP_SPARSE_ATTN = 3, CSA_OP_DECODE = 4 };
+CSA_API size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int32_t n_heads);
+
+/* csa_append -- pool, quantise and write new tokens ([SGL] "DSpark adaptation
+ * and optimization": fused pair pooling + quantisation + main-KV write, reused
+ * for index-K; [SGL] "Architecture changes...": 2:1 pooling or 1:1).
+ *  pos0      [B]   position of each request's first new token
+ *  tok_off   [B+1] request b's new tokens are rows tok_off[b]..tok_off[b+1]-1
+ *  total_tokens    host copy of tok_off[B] (grid size)
+ *  kv_in     bf16 [total_tokens, 512]; idx_in bf16 [total_tokens, 128]
+ *  pending   bf16 [B, 640] in/out: the unpaired last token of each request
+ *            (512 latent then 128 key).  Read when pos0 is odd (P = 2),
+ *            written when the last new token is left unpaired.
+ *  window    nullable; when given, every new token is also written as FP8.
+ *  Entries are complete when their last token arrives; a row must only see
+ *  complete entries.  ws may be NULL (ws_bytes 0): faults are then not
+ *  reported. */
+CSA_API csa_status_t csa_append(const csa_cache_t* cache, const csa_window_t* window,
+                        const int32_t* pos0, const int32_t* tok_off, int32_t total_tokens,
+                        const void* kv_in, const void* idx_in, void* pending,
+                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* csa_index_score -- score[r,i] = sum_h w[r,h] * relu(qhat[r,h] . khat[i]) for
+ * i < n(r), with qhat = MXFP4(q_idx) and khat the cached MXFP4 indexer keys,
+ * as a block-scaled FP4 tensor-core product ([SGL] "Architecture changes...":
+ * the indexer decides which 512 global positions attend).
+ *  q_idx bf16 [R, Hi, 128]; w fp32 [R, Hi]; scores fp32 [R, ld], ld >= max_entries,
+ *  entries i >= n(r) are left untouched.  Hi <= 128. */
+CSA_API csa_status_t csa_index_score(const csa_cache_t* cache, const csa_rows_t* rows,
+                             int32_t n_idx_heads, const void* q_idx, const float* w,
+                             float* scores, int32_t ld, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/* csa_topk -- exact top-512 of scores[r, 0..n_valid[r]) by (score desc, index
+ * asc), written in ascending index order and padded with -1 ([SGL]
+ * "Architecture changes...": top 512 global positions; "DSpark adaptation and
+ * optimization": invalid-position filtering).  k must be 512. max_n is a host
+ * bound on n_valid.  -0.0 and +0.0 compare equal; NaN scores are unsupported. */
+CSA_API csa_status_t csa_topk(int32_t num_rows, const float* scores, int32_t ld,
+                      const int32_t* n_valid, int32_t max_n, int32_t k, int32_t* out_idx,
+                      void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* csa_sparse_attn -- for each row and head: softmax attention of q over the
+ * dequantised FP4 main-KV entries listed in topk_idx (ascending, -1 skipped;
+ * page translation done here, [SGL] "DSpark adaptation and optimization") and
+ * the FP8 window positions max(0,t-127)..t ([VLLM] "SWA bounded replay").
+ * K = V = the shared 512-d latent (MQA).  Split over key blocks with a
+ * log-sum-exp merge.
+ *  q bf16 [R, H, 512]; out bf16 [R, H, 512]; lse fp32 [R, H] (nullable). */
+CSA_API csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* window,
+                             const csa_rows_t* rows, const int32_t* topk_idx,
+                             int32_t n_heads, const void* q, float softmax_scale,
+                             void* out, float* lse, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/* csa_decode -- index score -> top-512 -> sparse attention in one call, all on
+ * `stream`.  topk_out [R, 512] is optional (nullable). */
+CSA_API csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window,
+                        const csa_rows_t* rows, int32_t n_idx_heads, const void* q_idx,
+                        const float* w, int32_t n_heads, const void* q, float softmax_scale,
+                        void* out, float* lse, int32_t* topk_out,
+                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, returns the status word's flags in *flags_out (host)
+ * and clears it.  Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_FAULT. */
+CSA_API csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out);
+
+CSA_API const char* csa_status_string(csa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H */

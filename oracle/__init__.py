@@ -229,7 +229,7 @@ def decode(cache, row_req, row_pos, q_idx, w, q, softmax_scale, threads=1):
     return out, lse, topk, scores
 
 
-def build_cache(wl, requests=None, upto="ctx", window=True):
+def build_cache(wl, requests=None, upto="ctx", window=True, threads=1):
     """Build the oracle cache of workload `wl` from its seeded tokens.
 
     upto="ctx": all tokens (history + the step's new ones);
@@ -237,10 +237,13 @@ def build_cache(wl, requests=None, upto="ctx", window=True):
     Only `requests` (default: all) are filled.  Tokens older than the window
     are appended without the window write, which leaves the same state (the
     ring keeps only the last win_cap positions) at a fraction of the cost.
+    Requests own disjoint pages, so they are built in parallel when
+    threads > 1.
     """
     reqs = list(range(wl.B)) if requests is None else list(requests)
     cache = Cache(wl.num_pages, wl.page_table, wl.P, wl.win_cap, window=window)
-    for b in reqs:
+
+    def one(b):
         stop = int(wl.ctx_len[b] if upto == "ctx" else wl.hist_len[b])
         cut = max(0, stop - wl.win_cap) if window else stop
         for lo, hi, win in ((0, cut, False), (cut, stop, window)):
@@ -253,4 +256,12 @@ def build_cache(wl, requests=None, upto="ctx", window=True):
                 tok_off[b + 1:] = c1 - c0
                 rc = cache.append(pos0, tok_off, x, y, window=win)
                 assert rc == 0, rc
+
+    if threads > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, reqs))
+    else:
+        for b in reqs:
+            one(b)
     return cache

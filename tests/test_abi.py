@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/csa.h declares; host-side argument checks reject bad calls before any
+launch.  CPU only: no call here reaches a kernel."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import fp4_sparse_attention_csa_gb300 as csa
+from fp4_sparse_attention_csa_gb300 import build as csa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    csa_build.build()
+    return csa.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "csa.h")).read()
+    return sorted(set(re.findall(r"CSA_API\s+[\w\s\*]+?\b(csa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_five_entry_points():
+    names = declared_functions()
+    for n in ("csa_append", "csa_index_score", "csa_topk", "csa_sparse_attn", "csa_decode"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert C.cast(getattr(lib, name), C.c_void_p).value
+
+
+def test_status_strings(lib):
+    for s, name in csa.STATUS_NAMES.items():
+        assert csa.csa_status_string(s)
+    assert csa.csa_status_string(0) == "ok"
+
+
+def test_null_arguments_are_rejected_before_launch(lib):
+    assert lib.csa_append(None, None, None, None, 0, None, None, None, None, 0, None) == 1
+    assert lib.csa_index_score(None, None, 16, None, None, None, 0, None, 0, None) == 1
+    assert lib.csa_topk(1, None, 512, None, 512, 256, None, None, 0, None) == 2      # k != 512
+    assert lib.csa_topk(1, None, 512, None, 512, 512, None, None, 0, None) == 1
+    assert lib.csa_sparse_attn(None, None, None, None, 64, None, 1.0, None, None, None, 0, None) == 1
+    assert lib.csa_decode(None, None, None, 64, None, None, 64, None, 1.0, None, None, None, None, 0, None) == 1
+
+
+def test_bad_cache_descriptors(lib):
+    buf = (C.c_uint8 * 256)()
+    base = C.addressof(buf)
+    aligned = (base + 127) & ~127
+    pt = (C.c_int32 * 4)()
+    cache = csa.CsaCache(aligned, aligned, C.addressof(pt), 1, 1, 1, 3)   # pool ratio 3
+    assert lib.csa_append(C.byref(cache), None, C.addressof(pt), C.addressof(pt), 0, None, None, None,
+                          None, 0, None) == 1
+    cache = csa.CsaCache(aligned + 8, aligned, C.addressof(pt), 1, 1, 1, 2)  # misaligned pool
+    assert lib.csa_append(C.byref(cache), None, C.addressof(pt), C.addressof(pt), 0, None, None, None,
+                          None, 0, None) == 1
+
+
+def test_workspace_sizes_without_device(lib):
+    assert csa.csa_workspace_size(csa.OP_APPEND, 0, 0, 0) == 256
+    assert csa.csa_workspace_size(csa.OP_TOPK, 10, 1000, 0) == 256
+    assert csa.csa_workspace_size(csa.OP_INDEX_SCORE, 192, 3000, 64) >= 192 * 128 * 68
+    assert csa.csa_workspace_size(99, 1, 1, 1) == 0

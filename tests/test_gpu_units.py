@@ -1,0 +1,250 @@
+"""GPU parity of each C-ABI entry point against the CPU oracle, at sizes the
+oracle finishes in seconds but that span several tiles, pages and ragged
+tails, plus the edge cases of the method (n = 0, n < 512, n = 512, odd and
+even positions, the pending token, rows sharing a request)."""
+import numpy as np
+import pytest
+import torch
+
+import judge
+import oracle
+import fp4_sparse_attention_csa_gb300 as csa
+from fp4_sparse_attention_csa_gb300 import workloads as W
+from fp4_sparse_attention_csa_gb300.session import DeviceState
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    csa.build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+
+
+def _pools_equal(st, ref):
+    assert np.array_equal(st.kv_pool.cpu().numpy(), ref.kv_pool), "main-KV pool bytes differ"
+    assert np.array_equal(st.idx_pool.cpu().numpy(), ref.idx_pool), "indexer pool bytes differ"
+    if ref.win_codes is not None:
+        assert np.array_equal(st.win_codes.cpu().numpy(), ref.win_codes), "window codes differ"
+        assert np.array_equal(st.win_scale.cpu().numpy(), ref.win_scale), "window scales differ"
+
+
+# ---------------------------------------------------------------- append (J-1)
+@pytest.mark.parametrize("P", [2, 1])
+def test_append_bit_exact_history_and_step(P):
+    ctx = [1, 2, 3, 63, 64, 65, 129, 300, 1025, 2048]
+    new = [1, 2, 1, 6, 3, 1, 6, 2, 5, 1]
+    wl = W.custom("app", 11, ctx, new, H=16, Hi=16, P=P, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    rc, flags = csa.csa_check_device_status(st.ws_append)
+    assert rc == 0 and flags == 0
+    ref = oracle.build_cache(wl, upto="hist")
+    x, y = wl.step_tokens()
+    assert ref.append(wl.step_pos0, wl.step_tok_off, x, y) == 0
+    _pools_equal(st, ref)
+    if P == 2:
+        pend = st.pending.view(torch.uint16).cpu().numpy()
+        odd = (wl.ctx_len % 2) == 1                  # an unpaired last token exists
+        assert np.array_equal(pend[odd], ref.pending[odd])
+
+
+def test_append_token_by_token_equals_bulk():
+    wl = W.custom("tbt", 12, [37, 40, 9], [1, 1, 1], H=16, Hi=16)
+    bulk = DeviceState(wl)
+    bulk.build_history()
+    one = DeviceState(wl)
+    for p in range(int(wl.hist_len.max())):
+        active = [b for b in range(wl.B) if p < wl.hist_len[b]]
+        pos0 = np.zeros(wl.B, np.int32)
+        cnt = np.zeros(wl.B, np.int64)
+        xs, ys = [], []
+        for b in active:
+            x, y = wl.tokens(b, p, p + 1)
+            pos0[b], cnt[b] = p, 1
+            xs.append(x)
+            ys.append(y)
+        one.append(pos0, np.concatenate([[0], np.cumsum(cnt)]), np.concatenate(xs), np.concatenate(ys))
+    torch.cuda.synchronize()
+    assert torch.equal(bulk.kv_pool, one.kv_pool) and torch.equal(bulk.idx_pool, one.idx_pool)
+    assert torch.equal(bulk.win_codes, one.win_codes) and torch.equal(bulk.win_scale, one.win_scale)
+
+
+def test_append_flags_bad_page_without_writing():
+    wl = W.custom("bad", 13, [200], [1], H=16, Hi=16)
+    st = DeviceState(wl)
+    st.page_table[0, 1] = wl.num_pages + 5            # entries 64..127 point outside the pool
+    st.build_history()
+    rc, flags = csa.csa_check_device_status(st.ws_append)
+    assert rc == 5 and (flags & csa.FLAG_PAGE_OOB)
+    # entries 64..127 were not written anywhere; the other pages hold data
+    kv = st.kv_pool.view(wl.num_pages, -1)
+    assert int(kv[int(wl.page_table[0, 0])].count_nonzero()) > 0
+
+
+# ------------------------------------------------------------ index score
+@pytest.mark.parametrize("Hi,rows", [(16, 1), (64, 1), (64, 6), (16, 24), (32, 3)])
+def test_index_score_matches_oracle(Hi, rows):
+    ctx = [2, 127, 128, 129, 257, 1024 + 7, 1030, 4096 + 77]
+    wl = W.custom("score", 21 + Hi + rows, [c + rows for c in ctx], [rows] * len(ctx), H=16, Hi=Hi, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    ld = ((wl.max_entries + 63) // 64) * 64
+    scores = torch.full((wl.R, ld), float("nan"), device="cuda")
+    ws = torch.zeros(csa.csa_workspace_size(csa.OP_INDEX_SCORE, wl.R, wl.max_entries, 16), dtype=torch.uint8,
+                     device="cuda")
+    csa.csa_index_score(st.cache, s["rows"], Hi, s["q_idx"], s["w"], scores, ld, ws)
+    rc, flags = csa.csa_check_device_status(ws)
+    assert rc == 0 and flags == 0, flags
+    ref = oracle.build_cache(wl)
+    q_idx, w, _ = wl.step_queries()
+    ref_sc = oracle.index_score(ref, wl.row_req, wl.row_pos, q_idx, w, ld)
+    got = scores.cpu().numpy()
+    n = wl.row_entries()
+    exact = total = 0
+    for r in range(wl.R):
+        g, o = got[r, :n[r]], ref_sc[r, :n[r]]
+        np.testing.assert_allclose(g, o, rtol=1e-6, atol=0)
+        exact += int((g == o).sum())
+        total += int(n[r])
+        assert np.isnan(got[r, n[r]:]).all(), "scores past the visible range must be untouched"
+    assert exact >= 0.99 * total, (exact, total)
+
+
+def test_identical_entries_score_identically():
+    """Bitwise-identical indexer entries get bitwise-identical scores wherever
+    they sit in a tile or page."""
+    wl = W.custom("ident", 31, [3000], [1], H=16, Hi=64, P=1)
+    st = DeviceState(wl)
+    x, y = wl.tokens(0, 0, 3000)
+    y[:] = y[17]
+    st.append(np.zeros(1, np.int32), np.array([0, 3000], np.int32), x, y)
+    s = st.step_inputs()
+    ld = 3008
+    scores = torch.zeros((1, ld), device="cuda")
+    ws = torch.zeros(csa.csa_workspace_size(csa.OP_INDEX_SCORE, 1, 3000, 16), dtype=torch.uint8, device="cuda")
+    csa.csa_index_score(st.cache, s["rows"], 64, s["q_idx"], s["w"], scores, ld, ws)
+    g = scores[0, :3000].cpu().numpy()
+    assert len(set(g.tolist())) == 1
+
+
+# ------------------------------------------------------------------- top-k
+@pytest.mark.parametrize("n", [0, 1, 300, 511, 512, 513, 1000, 5000, 70000, 262144])
+def test_topk_exact_with_ties(n):
+    g = np.random.default_rng(n)
+    R = 3
+    ld = max(64, ((n + 63) // 64) * 64)
+    sc = (g.integers(0, 200, (R, ld)) / 8).astype(np.float32)    # many exact ties
+    sc[1] = -sc[1]                                                  # negative scores
+    sc[2, : n // 2] = 0.0
+    sc[2, n // 3: n // 2] = -0.0                                    # -0 equals +0
+    nv = np.array([n, n, n], np.int32)
+    out = torch.empty((R, 512), dtype=torch.int32, device="cuda")
+    csa.csa_topk(R, torch.from_numpy(sc).cuda(), ld, torch.from_numpy(nv).cuda(), n, 512, out)
+    got = out.cpu().numpy()
+    for r in range(R):
+        assert np.array_equal(got[r], oracle.topk_row(sc[r], n)), r
+
+
+def test_topk_rows_of_different_lengths():
+    g = np.random.default_rng(5)
+    R, ld = 9, 40000
+    sc = g.standard_normal((R, ld)).astype(np.float32)
+    nv = np.array([0, 5, 512, 513, 1000, 17000, 39999, 40000, 600], np.int32)
+    out = torch.empty((R, 512), dtype=torch.int32, device="cuda")
+    csa.csa_topk(R, torch.from_numpy(sc).cuda(), ld, torch.from_numpy(nv).cuda(), ld, 512, out)
+    got = out.cpu().numpy()
+    for r in range(R):
+        assert np.array_equal(got[r], oracle.topk_row(sc[r], int(nv[r]))), r
+
+
+# --------------------------------------------------------------- attention
+@pytest.mark.parametrize("H,ctx,rows", [(16, [1, 2, 100, 700, 1025, 3000], 1), (64, [300, 2100], 1),
+                                        (32, [1500, 2000], 6)])
+def test_sparse_attention_matches_oracle(H, ctx, rows):
+    wl = W.custom("attn", 41 + H, ctx, [min(rows, c) for c in ctx], H=H, Hi=16, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    ref = oracle.build_cache(wl)
+    q_idx, w, q = wl.step_queries()
+    _, _, topk, _ = oracle.decode(ref, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale)
+    tk = torch.from_numpy(topk).cuda()
+    out = torch.empty((wl.R, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((wl.R, H), device="cuda")
+    ws = torch.zeros(csa.csa_workspace_size(csa.OP_SPARSE_ATTN, wl.R, wl.max_entries, H), dtype=torch.uint8,
+                     device="cuda")
+    csa.csa_sparse_attn(st.cache, st.window, s["rows"], tk, H, s["q"], wl.softmax_scale, out, lse, ws)
+    rc, flags = csa.csa_check_device_status(ws)
+    assert rc == 0 and flags == 0, flags
+    o_ref = np.zeros((wl.R, H, 512), np.float32)
+    l_ref = np.zeros((wl.R, H), np.float32)
+    for r in range(wl.R):
+        o_ref[r], l_ref[r] = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], topk[r], q[r],
+                                                  wl.softmax_scale)
+    norm, l2 = judge.check_attention(out.float().cpu().numpy(), o_ref, lse.cpu().numpy(), l_ref)
+    print(f"attention H={H}: max normalised err {norm:.2e}, rel L2 {l2:.2e}")
+
+
+def test_attention_many_rows_single_split():
+    """Enough rows that each row runs in one CTA (no split merge)."""
+    ctx = list(np.random.default_rng(7).integers(600, 1400, 160))
+    wl = W.custom("attn1", 47, ctx, [1] * 160, H=16, Hi=16)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    st.step_decode(s)
+    rc, flags = csa.csa_check_device_status(s["ws"])
+    assert rc == 0 and flags == 0
+    ref = oracle.build_cache(wl)
+    q_idx, w, q = wl.step_queries()
+    out, lse, topk, scores = oracle.decode(ref, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale, threads=8)
+    gt = s["topk"].cpu().numpy()
+    n = wl.row_entries()
+    for r in range(wl.R):
+        judge.check_topk_row(gt[r], scores[r], int(n[r]))
+    judge.check_attention(s["out"].float().cpu().numpy(), out, s["lse"].cpu().numpy(), lse)
+
+
+# ------------------------------------------------------------------ decode
+@pytest.mark.parametrize("H,Hi,rows", [(16, 16, 1), (64, 64, 6), (32, 32, 2)])
+def test_decode_end_to_end(H, Hi, rows):
+    ctx = [1, 3, 513 * 2, 1024 + 1, 2500, 5000 + 3]
+    wl = W.custom("dec", 51 + rows, ctx, [min(rows, c) for c in ctx], H=H, Hi=Hi, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    st.step_decode(s)
+    rc, flags = csa.csa_check_device_status(s["ws"])
+    assert rc == 0 and flags == 0, flags
+    ref = oracle.build_cache(wl)
+    q_idx, w, q = wl.step_queries()
+    _, _, _, scores = oracle.decode(ref, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale)
+    gt = s["topk"].cpu().numpy()
+    n = wl.row_entries()
+    o_ref = np.zeros((wl.R, H, 512), np.float32)
+    l_ref = np.zeros((wl.R, H), np.float32)
+    for r in range(wl.R):
+        judge.check_topk_row(gt[r], scores[r], int(n[r]))
+        o_ref[r], l_ref[r] = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], gt[r], q[r], wl.softmax_scale)
+    judge.check_attention(s["out"].float().cpu().numpy(), o_ref, s["lse"].cpu().numpy(), l_ref)
+
+
+def test_decode_is_deterministic():
+    wl = W.custom("det", 61, [3000, 5000], [2, 1], H=64, Hi=64)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    st.step_decode(s)
+    o1, t1 = s["out"].clone(), s["topk"].clone()
+    st.step_decode(s)
+    assert torch.equal(o1, s["out"]) and torch.equal(t1, s["topk"])
