@@ -1,0 +1,332 @@
+"""Benchmark of one CSA decode step on GB300: csa_append of the step's new
+tokens + csa_decode (indexer score -> exact top-512 -> sparse attention), on
+the serving-batch workload (128 requests x 1 row, 64 heads, log-uniform
+4k-128k token contexts pooled 2:1, shuffled pages).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload cfg4|cfg3|...]
+
+Prints one JSON line.  value = query rows/s over all ranks; the L2 is flushed
+(a 2 x L2 write) before every timed step; timing with CUDA events on the
+launching stream.  --impl reference times the CPU oracle on the host cores on
+a bounded sample of the same workload.  With N > 1 (torchrun) every rank runs
+an independent replica (the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp4_sparse_attention_csa_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode query rows/s (csa_append + csa_decode step)"
+CFG_OF = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(wl, topk=None):
+    """Unique bytes one step must move (the method's own traffic only)."""
+    n_row = wl.row_entries().astype(np.int64)
+    req_n = np.zeros(wl.B, np.int64)
+    np.maximum.at(req_n, wl.row_req, n_row)
+    idx = int(req_n.sum()) * 68                           # each request's visible indexer entries once
+    pages = int(((req_n + 63) // 64).sum()) * 4
+    if topk is not None:                                  # per-request union of the selected entries
+        gather = 0
+        for b in range(wl.B):
+            sel = topk[wl.row_req == b]
+            gather += int(np.unique(sel[sel >= 0]).size) * 288
+    else:
+        gather = int(np.minimum(n_row, 512).sum()) * 288
+    win = 0
+    for b in range(wl.B):                                 # unique window tokens per request
+        pos = wl.row_pos[wl.row_req == b]
+        if pos.size:
+            win += int(pos.max() - max(0, pos.min() - 127) + 1) * 516
+    R = wl.R
+    q = R * wl.H * 512 * 2 + R * wl.Hi * 128 * 2 + R * wl.Hi * 4
+    out = R * wl.H * 512 * 2 + R * wl.H * 4 + R * 512 * 4
+    T = int(wl.new_tok.sum())
+    new_entries = 0
+    for b in range(wl.B):
+        p0, p1 = int(wl.hist_len[b]), int(wl.ctx_len[b])
+        new_entries += p1 // wl.P - p0 // wl.P
+    append = T * 640 * 2 + new_entries * 356 + T * 516
+    score_bytes = idx + pages + R * wl.Hi * 128 * 2 + R * wl.Hi * 4 + int(n_row.sum()) * 4
+    return {"total": idx + pages + gather + win + q + out + append, "index_score": score_bytes,
+            "idx": idx, "gather": gather, "window": win, "q_out": q + out, "append": append}
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_reference(args, wl, cfg):
+    """Time the CPU oracle as it stands on a bounded sample of the workload."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    rows = list(range(min(wl.R, args.ref_rows)))
+    reqs = sorted(set(int(wl.row_req[r]) for r in rows))
+    ref = oracle.build_cache(wl, requests=reqs, threads=cores)
+    q_idx, w, q = wl.step_queries()
+    rr, rp = wl.row_req[rows], wl.row_pos[rows]
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle.decode(ref, rr, rp, q_idx[rows], w[rows], q[rows], wl.softmax_scale, threads=cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.decode(ref, rr, rp, q_idx[rows], w[rows], q[rows], wl.softmax_scale, threads=cores)
+        times.append(time.perf_counter() - t0)
+    value = len(rows) / float(np.mean(times))
+    sample = f"{len(rows)} rows of {wl.name} (requests {reqs[0]}..{reqs[-1]}); score + top-512 + attention"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": W.CONFIG_NAMES[cfg], "rows_per_step": len(rows)},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, rows_cap, budget_s=20.0):
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    rows = list(range(min(wl.R, rows_cap)))
+    reqs = sorted(set(int(wl.row_req[r]) for r in rows))
+    ref = oracle.build_cache(wl, requests=reqs, threads=cores)
+    q_idx, w, q = wl.step_queries()
+    rr, rp = wl.row_req[rows], wl.row_pos[rows]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(ref, rr, rp, q_idx[rows], w[rows], q[rows], wl.softmax_scale, threads=cores)
+        done += len(rows)
+        el = time.perf_counter() - t0
+        if el > budget_s * 0.5 or done >= 4 * len(rows):
+            break
+    return {"value": done / el, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} rows of {wl.name} (requests {reqs[0]}..{reqs[-1]}), x{done // len(rows)}; "
+                      f"score + top-512 + attention, {cores} threads"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="cfg4", choices=sorted(CFG_OF))
+    ap.add_argument("--ref-rows", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    cfg = CFG_OF[args.workload]
+    wl = W.config(cfg)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, wl, cfg)
+        return
+
+    import torch
+    import fp4_sparse_attention_csa_gb300 as csa
+    from fp4_sparse_attention_csa_gb300.session import DeviceState
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if not os.path.exists(csa.lib_path()):
+        raise SystemExit("libcsa.so is not built: run python -c 'import __graft_entry__ as g; g.build()'")
+
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+
+    def step():
+        st.step_append(s)
+        st.step_decode(s)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    rc, flags = csa.csa_check_device_status(s["ws"])
+    if rc != 0:
+        raise SystemExit(f"device status {rc} flags {flags:#x}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = np.array([a.elapsed_time(b) for a, b in zip(starts, ends)])
+    total_ms = float(step_ms.sum())
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    rows_total = wl.R * args.steps * world
+    value = rows_total / (total_ms / 1e3)
+
+    # ---- dominant kernel: index score (prep + k_index_score), same inputs, L2 flushed
+    ld = ((wl.max_entries + 63) // 64) * 64
+    scores = torch.empty((wl.R, ld), device="cuda")
+    ws_s = torch.zeros(csa.csa_workspace_size(csa.OP_INDEX_SCORE, wl.R, wl.max_entries, wl.H),
+                       dtype=torch.uint8, device="cuda")
+    sc_ms = []
+    for i in range(max(20, min(args.steps, 100))):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        csa.csa_index_score(st.cache, s["rows"], wl.Hi, s["q_idx"], s["w"], scores, ld, ws_s)
+        e1.record(stream)
+        sc_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    sc_ms = np.array([a.elapsed_time(b) for a, b in sc_ms][3:])
+
+    topk = s["topk"].cpu().numpy()
+    ab = algorithmic_bytes(wl, topk)
+    peak, peak_kind = peaks()
+    path_gbs = ab["total"] / (np.median(step_ms) / 1e3) / 1e9
+    score_gbs = ab["index_score"] / (np.mean(sc_ms) / 1e3) / 1e9
+
+    # ---- end to end: pinned host inputs -> device, step, result -> host
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: s[k].cpu().pin_memory() for k in ("q_idx", "w", "q", "kv_new", "idx_new")}
+        host_out = torch.empty(s["out"].shape, dtype=s["out"].dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = host_out.numel() * host_out.element_size()
+        torch.cuda.synchronize()
+        ev = []
+        for i in range(args.steps):
+            flush.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for k, v in host_in.items():
+                s[k].copy_(v, non_blocking=True)
+            step()
+            host_out.copy_(s["out"], non_blocking=True)
+            a1.record(stream)
+            ev.append((a0, a1))
+        torch.cuda.synchronize()
+        e2e_ms = float(sum(a.elapsed_time(b) for a, b in ev))
+        e2e = {"value": wl.R * args.steps * world / (e2e_ms / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    attn_splits = max(1, min(5, sms // max(wl.R, 1)))          # the library's split rule
+    launches_per_step = 1 + 4 + (1 if attn_splits > 1 else 0)  # append, prep, score, top-k, attention, merge
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, rows_cap=args.ref_rows)
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp4xfp4->f32 score, f16xf16->f32 attention",
+        "data": "synthetic",
+        "config": {"workload": W.CONFIG_NAMES[cfg], "rows_per_step": wl.R, "heads": wl.H,
+                   "indexer_heads": wl.Hi, "max_entries": wl.max_entries,
+                   "l2": "flushed before every timed step (2 x L2 write, untimed)",
+                   "step_ms_median": float(np.median(step_ms)), "step_ms_p10": float(np.percentile(step_ms, 10)),
+                   "step_ms_p90": float(np.percentile(step_ms, 90)),
+                   "path_unique_bytes": ab["total"], "path_gbs": path_gbs,
+                   "path_frac_of_hbm": path_gbs / peak, "path_frac_of_8tbs": path_gbs / 8000.0,
+                   "bytes": ab, "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "index score (k_score_prep + k_index_score)",
+                     "achieved": score_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": score_gbs / peak, "traffic": None,
+                     "launch_ms_mean": float(np.mean(sc_ms)), "algorithmic_bytes": ab["index_score"]},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -81,8 +81,11 @@ __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
   float x[16];
   load_bf16x16(a.kv_in + (size_t)t * D + lane * 16, x);
 
-  // ---- FP8 window slot of this token: scale = amax / 448, codes = E4M3(x / scale)
-  if (a.win_codes != nullptr) {
+  // ---- FP8 window slot of this token: scale = amax / 448, codes = E4M3(x / scale).
+  // Only the last win_cap tokens of the request in this call are written: an
+  // older token's slot is taken by a newer one of the same call, and writing
+  // both would race.
+  if (a.win_codes != nullptr && j >= T - a.win_cap) {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));

@@ -152,7 +152,9 @@ CSA_API size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entr
  *  pending   bf16 [B, 640] in/out: the unpaired last token of each request
  *            (512 latent then 128 key).  Read when pos0 is odd (P = 2),
  *            written when the last new token is left unpaired.
- *  window    nullable; when given, every new token is also written as FP8.
+ *  window    nullable; when given, the new tokens are also written to the FP8
+ *            ring (of a call's tokens for one request only the last `capacity`
+ *            land there, which is the ring's content after the call).
  *  Entries are complete when their last token arrives; a row must only see
  *  complete entries.  ws may be NULL (ws_bytes 0): faults are then not
  *  reported. */
