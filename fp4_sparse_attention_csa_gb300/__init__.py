@@ -68,11 +68,12 @@ def lib():
             L.csa_topk.argtypes = [i32, vp, i32, vp, i32, i32, vp, vp, sz, vp]
             L.csa_sparse_attn.argtypes = [vp, vp, vp, vp, i32, vp, f32, vp, vp, vp, sz, vp]
             L.csa_decode.argtypes = [vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
+            L.csa_index_score_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp]
             L.csa_check_device_status.argtypes = [vp, vp, C.POINTER(C.c_uint32)]
             L.csa_status_string.argtypes = [i32]
             L.csa_status_string.restype = C.c_char_p
             for fn in ("csa_append", "csa_index_score", "csa_topk", "csa_sparse_attn", "csa_decode",
-                       "csa_check_device_status"):
+                       "csa_index_score_noalloc", "csa_check_device_status"):
                 getattr(L, fn).restype = C.c_int
             _lib = L
     return _lib
@@ -132,6 +133,13 @@ def csa_index_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, stream=N
     rc = lib().csa_index_score(C.byref(cache), C.byref(rows), int(n_idx_heads), _ptr(q_idx), _ptr(w),
                                _ptr(scores), int(ld), _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "csa_index_score")
+
+
+def csa_index_score_noalloc(cache, rows, n_idx_heads, q_idx, w, scores, ld, stream=None):
+    """csa_index_score with the library's fixed scratch array (no workspace)."""
+    rc = lib().csa_index_score_noalloc(C.byref(cache), C.byref(rows), int(n_idx_heads), _ptr(q_idx), _ptr(w),
+                                       _ptr(scores), int(ld), _stream(stream))
+    _check(rc, "csa_index_score_noalloc")
 
 
 def csa_topk(num_rows, scores, ld, n_valid, max_n, k, out_idx, ws=None, stream=None):

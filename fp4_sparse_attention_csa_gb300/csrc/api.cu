@@ -325,3 +325,58 @@ const char* csa_status_string(csa_status_t s) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// csa_index_score_noalloc: the index score with its scratch in a fixed device
+// array owned by this library, for callers that cannot allocate (see csa.h).
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = CSA_NOALLOC_SCRATCH_BYTES;
+// One copy per GPU that loads the library, alive until the process exits.
+// Host code must not use this name as an address: the device address comes
+// from cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_scratch_once[kMaxDevices];
+void* g_scratch_ptr[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current) on its first call.
+cudaError_t noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_scratch_once[dev], [dev] {
+    void* p = nullptr;
+    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    g_scratch_ptr[dev] = p;
+  });
+  if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" csa_status_t csa_index_score_noalloc(const csa_cache_t* cache, const csa_rows_t* rows,
+                                                int32_t n_idx_heads, const void* q_idx, const float* w,
+                                                float* scores, int32_t ld, cudaStream_t stream) {
+  csa_status_t s = check_cache(cache);
+  if (s != CSA_OK) return s;
+  if ((s = check_rows(rows, cache)) != CSA_OK) return s;
+  if (n_idx_heads < 1 || n_idx_heads > CSA_MAX_IDX_HEADS) return CSA_ERR_UNSUPPORTED;
+  if (rows->num_rows == 0) return CSA_OK;
+  if (!q_idx || !w || !scores || !aligned(q_idx, 16) || !aligned(w, 4) || !aligned(scores, 4))
+    return CSA_ERR_INVALID_ARGUMENT;
+  if (ld < rows->max_entries || ld < 1) return CSA_ERR_INVALID_ARGUMENT;
+  if (score_ws_bytes(rows->num_rows, n_idx_heads) > kNoAllocScratchBytes) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  if (noalloc_scratch(&ws) != cudaSuccess) return CSA_ERR_CUDA;
+  // every call starts with a clear status word; the rest of the scratch is
+  // fully rewritten by the score step before it is read
+  if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  return run_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, stream);
+}

@@ -204,6 +204,30 @@ CSA_API csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* wi
                         void* out, float* lse, int32_t* topk_out,
                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* csa_index_score_noalloc -- the same scores as csa_index_score, without a
+ * workspace argument.  The pages have no counterpart to this entry point; it
+ * exists for callers that cannot call cudaMalloc: a serving loop that reserves
+ * all of its device memory at start-up and may not allocate while it decodes
+ * (an allocation can synchronise the device and stall the other streams), or
+ * a plain C host that embeds this library and has no device allocator of its
+ * own.  Its scratch is a fixed array of CSA_NOALLOC_SCRATCH_BYTES inside this
+ * library, present on every GPU that loads the library until the process
+ * exits; nothing is allocated or freed.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - Every call shares the one array and leaves its contents behind (the
+ *    status word is cleared at the start of each call, the rest is rewritten
+ *    before it is read).  Calls that overlap on the GPU -- other streams, or
+ *    other host threads without ordering between them -- race on the array.
+ *  - Scratch need is about num_rows x 8*ceil(n_idx_heads/8) x 68 B; a call
+ *    that needs more than the array returns CSA_ERR_WORKSPACE_TOO_SMALL before
+ *    any launch.  Device-detected faults are not reported by this variant.
+ *  Arguments are those of csa_index_score without ws / ws_bytes. */
+#define CSA_NOALLOC_SCRATCH_BYTES (4u << 20)
+CSA_API csa_status_t csa_index_score_noalloc(const csa_cache_t* cache, const csa_rows_t* rows,
+                                             int32_t n_idx_heads, const void* q_idx, const float* w,
+                                             float* scores, int32_t ld, cudaStream_t stream);
+
 /* Synchronises `stream`, returns the status word's flags in *flags_out (host)
  * and clears it.  Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_FAULT. */
 CSA_API csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out);
