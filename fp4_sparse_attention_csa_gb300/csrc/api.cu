@@ -121,7 +121,16 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
   a.row_pos = rows->row_pos;
   a.num_rows = rows->num_rows;
   a.Hi = Hi;
-  a.group_rows = score_group_rows(Hi);
+  // rows scored by one MMA: all of a request's rows when at least two TMEM
+  // accumulator buffers still fit, so the epilogue can overlap the MMAs
+  {
+    const int hp = (Hi + 7) & ~7;
+    int g = rows->max_rows_per_req < 1 ? 1 : rows->max_rows_per_req;
+    const int two_buf = (216 / hp) > 0 ? 216 / hp : 1;
+    if (g > two_buf) g = two_buf;
+    if (g > score_group_rows(Hi)) g = score_group_rows(Hi);
+    a.group_rows = g;
+  }
   a.max_entries = rows->max_entries;
   a.q_idx = static_cast<const uint16_t*>(q_idx);
   a.w = w;

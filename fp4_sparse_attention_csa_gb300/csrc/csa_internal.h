@@ -39,6 +39,7 @@ struct ScoreArgs {
   float* scores;                       // [R, ld]
   int64_t ld;
   uint32_t* status;
+  int32_t grid;                        // score CTAs (set by the launcher)
 };
 // tmaps: 3-D tensor maps over idx_pool: [0] data (64 B x 64 entries x pages),
 // [1] scales (256 B x 1 x pages).

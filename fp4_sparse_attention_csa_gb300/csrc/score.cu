@@ -39,14 +39,22 @@ struct Seg {
 };
 
 constexpr int kStages = 8;
-constexpr int kThreads = 384;
+constexpr int kMaxBuf = 4;                     // TMEM accumulator buffers = epilogue groups
+constexpr int kThreads = 128 + 128 * kMaxBuf;  // warps 0-3: producer, MMA, 2 idle; then groups
+constexpr int kEpiWarps = 4 * kMaxBuf;
 constexpr int kTileEntries = 128;
 constexpr int kStageA = 8192;        // 128 entries x 64 B (two pages)
 constexpr int kStageSF = 512;        // 128 entries x 4 E8M0 bytes (raw page order)
 constexpr int kMaxN = CSA_MAX_ROW_GROUP_COLS;  // rows x padded heads per MMA group
 constexpr int kQData = kMaxN * 64;   // 24576
 constexpr int kQSF = kMaxN * 4;      // 1536
-constexpr int kTmemSF = 0, kTmemD = 32;
+constexpr int kItemCap = 1024;       // work items per table chunk
+constexpr int kMaxGroupRows = 64;    // rows per segment (kMaxN / 8 heads at least)
+constexpr int kTmemSFA = 0, kTmemSFB = 16, kTmemD = 48;
+
+struct Item {
+  int32_t seg, tile, pg0, pg1;       // local segment index, tile in segment, pages (-1: none)
+};
 
 struct ScoreSmem {
   uint8_t a[kStages][kStageA];                 // 1024-aligned
@@ -55,8 +63,13 @@ struct ScoreSmem {
   uint8_t sfa_atom[kStages][kStageSF];
   uint8_t sfb_raw[2][kQSF];
   uint8_t sfb_atom[2][kQSF];
+  Item items[kItemCap];
+  Seg segs[kItemCap];
+  int32_t pref[kItemCap + 1];
+  float wseg[kEpiWarps][kMaxN];
+  int32_t rown[kEpiWarps][kMaxGroupRows];
   uint64_t full[kStages], empty[kStages];
-  uint64_t tfull[2], tempty[2];
+  uint64_t tfull[kMaxBuf], tempty[kMaxBuf];
   uint64_t qfull[2], qempty[2];
   uint32_t tmem_base;
   int32_t abort_flag;
@@ -68,8 +81,11 @@ __host__ __device__ inline int hi_pad(int Hi) { return (Hi + 7) & ~7; }
 __host__ __device__ inline int mma_n(int N) { return N < 64 ? 64 : (N + 15) & ~15; }
 
 // Workspace carve-out of the score step (after the status word).
+constexpr int kMaxGrid = 1024;
+
 struct ScoreWs {
-  int32_t* nseg;       // [1] segments, [2] total items at [1]
+  int32_t* nseg;       // [0] segments, [1] total work items (128-entry tiles)
+  int32_t* cta_seg;    // [kMaxGrid] segment holding each score CTA's first item
   Seg* seg;            // [R]
   int32_t* tile_pref;  // [R + 1]
   uint8_t* qimg;       // [R * Hi_pad * 64]
@@ -83,6 +99,8 @@ __host__ __device__ inline ScoreWs carve_score_ws(uint8_t* base, int R, int Hi) 
   size_t o = kStatusBytes;
   w.nseg = reinterpret_cast<int32_t*>(base + o);
   o = align256(o + 16);
+  w.cta_seg = reinterpret_cast<int32_t*>(base + o);
+  o = align256(o + sizeof(int32_t) * kMaxGrid);
   w.seg = reinterpret_cast<Seg*>(base + o);
   o = align256(o + sizeof(Seg) * (size_t)(R > 0 ? R : 1));
   w.tile_pref = reinterpret_cast<int32_t*>(base + o);
@@ -183,6 +201,23 @@ __global__ void __launch_bounds__(128) k_score_prep(ScoreArgs a, uint8_t* ws) {
       W.nseg[0] = S;
       W.nseg[1] = carry_t;
     }
+    __syncthreads();
+    // first segment of every score CTA's contiguous item range
+    const int total = carry_t;
+    const int per = (total + a.grid - 1) / a.grid;
+    for (int g = threadIdx.x; g < a.grid; g += blockDim.x) {
+      const int item = g * per;
+      int seg = S;
+      if (item < total) {
+        int lo = 0, hi = S - 1;              // largest s with tile_pref[s] <= item
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (W.tile_pref[mid] <= item) lo = mid; else hi = mid - 1;
+        }
+        seg = lo;
+      }
+      W.cta_seg[g] = seg;
+    }
     return;
   }
   // ---- MXFP4 quantisation of row r's indexer queries into the MMA B image.
@@ -239,24 +274,6 @@ __device__ __forceinline__ void sf_to_atom(const uint8_t* raw, uint8_t* atom, in
   reinterpret_cast<uint4*>(atom)[lane] = v;
 }
 
-__device__ __forceinline__ int find_seg(const int32_t* pref, int S, int item) {
-  int lo = 0, hi = S - 1;  // largest s with pref[s] <= item
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pref[mid] <= item) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-// Next (segment, tile) in item order, skipping segments without tiles.
-__device__ __forceinline__ void advance(const int32_t* pref, int S, int& seg, int& tile) {
-  if (++tile == pref[seg + 1] - pref[seg]) {
-    tile = 0;
-    ++seg;
-    while (seg < S && pref[seg + 1] == pref[seg]) ++seg;
-  }
-}
-
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ScoreSmem& sm, uint32_t* status) {
   if (mbar_wait(bar, parity)) return true;
   raise_flag(status, CSA_FLAG_TIMEOUT);
@@ -271,25 +288,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   ScoreSmem& sm = *reinterpret_cast<ScoreSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int Hi = a.Hi, Hp = hi_pad(Hi);
   ScoreWs W = carve_score_ws(ws, a.num_rows, Hi);
-  const int warp = warp_id(), lane = lane_id();
+  const int warp = warp_id(), lane = lane_id(), tid = threadIdx.x;
 
   const int S = W.nseg[0], total = W.nseg[1];
   const int per = (total + gridDim.x - 1) / gridDim.x;
   const int beg = min(total, (int)blockIdx.x * per), end = min(total, beg + per);
 
-  // TMEM accumulator buffers: D(d) at column kTmemD + d * dstride
+  // TMEM: scale factors in columns [0, 48), accumulator buffer d at
+  // kTmemD + d * dstride; one epilogue warp group per buffer.
   const int npad_max = mma_n(a.group_rows * Hp);       // largest MMA N of any segment
   const int dstride = npad_max + 16;
-  const int nbuf = (2 * dstride <= 512 - kTmemD) ? 2 : 1;
+  const int nbuf = min(kMaxBuf, (512 - kTmemD) / dstride);
 
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    for (int d = 0; d < 2; ++d) {
+    for (int d = 0; d < kMaxBuf; ++d) {
       mbar_init(&sm.tfull[d], 1);
       mbar_init(&sm.tempty[d], 4);
+    }
+    for (int d = 0; d < 2; ++d) {
       mbar_init(&sm.qfull[d], 1);
       mbar_init(&sm.qempty[d], 1);
     }
@@ -302,79 +322,115 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (beg < end) {
+  // role state that persists across work chunks
+  int p_nq = 0, p_gseg = -1;                 // producer: q images loaded, current segment
+  int m_nq = 0, m_gseg = -1, m_par = 0, m_N = 0;
+  int e_gseg = -1;                           // epilogue: segment whose w / n are staged
+  const int grp = (warp >= 4) ? (warp - 4) >> 2 : -1;
+
+  int seg0 = (beg < end) ? W.cta_seg[blockIdx.x] : S;
+  int it_base = 0;
+  for (int c0 = beg; c0 < end;) {
+    // ---- work table for items [c0, c1): local segment window, pages -----------
+    const int nsw = min(S - seg0, kItemCap);
+    for (int j = tid; j <= nsw; j += kThreads) sm.pref[j] = W.tile_pref[seg0 + j];
+    for (int j = tid; j < nsw; j += kThreads) sm.segs[j] = W.seg[seg0 + j];
+    __syncthreads();
+    const int c1 = min(min(end, c0 + kItemCap), sm.pref[nsw]);
+    const int m = c1 - c0;
+    if (m <= 0) {                            // only empty segments in this window
+      seg0 += nsw;
+      __syncthreads();
+      continue;
+    }
+    for (int i = tid; i < m; i += kThreads) {
+      const int item = c0 + i;
+      int lo = 0, hi = nsw - 1;              // largest j with pref[j] <= item
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sm.pref[mid] <= item) lo = mid; else hi = mid - 1;
+      }
+      const Seg sg = sm.segs[lo];
+      const int tile = item - sm.pref[lo];
+      const int npages = (sg.n + PAGE - 1) / PAGE;
+      int pg[2] = {-1, -1};
+      for (int h = 0; h < 2; ++h) {
+        const int lp = 2 * tile + h;
+        if (lp < npages) {
+          const int p = __ldg(a.page_table + (size_t)sg.b * a.max_pages + lp);
+          if (p >= 0 && p < a.num_pages) pg[h] = p;
+          else raise_flag(a.status, CSA_FLAG_PAGE_OOB);
+        }
+      }
+      Item e;
+      e.seg = lo;
+      e.tile = tile;
+      e.pg0 = pg[0];
+      e.pg1 = pg[1];
+      sm.items[i] = e;
+    }
+    __syncthreads();
+
     if (warp == 0 && lane == 0) {
       // ================= TMA producer =================
-      int seg = find_seg(W.tile_pref, S, beg);
-      int tile = beg - W.tile_pref[seg];
-      int nq = 0;
-      for (int it = 0; beg + it < end; ++it) {
+      for (int i = 0; i < m; ++i) {
         if (sm.abort_flag) break;
-        const Seg sg = W.seg[seg];
-        if (it == 0 || tile == 0) {
-          const int par = nq & 1;
-          if (nq >= 2 && !wait_or_abort(&sm.qempty[par], ((nq >> 1) - 1) & 1, sm, a.status)) break;
+        const int it = it_base + i;
+        const Item e = sm.items[i];
+        const int gseg = seg0 + e.seg;
+        if (gseg != p_gseg) {
+          const Seg sg = sm.segs[e.seg];
+          const int par = p_nq & 1;
+          if (p_nq >= 2 && !wait_or_abort(&sm.qempty[par], ((p_nq >> 1) - 1) & 1, sm, a.status)) break;
           const uint32_t bytes_d = (uint32_t)(sg.nrows * Hp * 64), bytes_s = (uint32_t)(sg.nrows * Hp * 4);
           mbar_expect_tx(&sm.qfull[par], bytes_d + bytes_s);
-          if (bytes_d > 0) {   // nrows in [1, group_rows] whenever the segment has tiles
+          if (bytes_d > 0) {   // nrows is in [1, group_rows] whenever the segment has tiles
             bulk_load(sm.qdata[par], W.qimg + (size_t)sg.r0 * Hp * 64, bytes_d, &sm.qfull[par]);
             bulk_load(sm.sfb_raw[par], W.qsf + (size_t)sg.r0 * Hp * 4, bytes_s, &sm.qfull[par]);
           }
-          ++nq;
+          ++p_nq;
+          p_gseg = gseg;
         }
         const int s = it % kStages;
         if (it >= kStages && !wait_or_abort(&sm.empty[s], ((it / kStages) - 1) & 1, sm, a.status)) break;
-        const int npages = (sg.n + PAGE - 1) / PAGE;
-        int pg[2] = {-1, -1};
-        uint32_t bytes = 0;
-        for (int h = 0; h < 2; ++h) {
-          const int lp = 2 * tile + h;
-          if (lp < npages) {
-            const int p = __ldg(a.page_table + (size_t)sg.b * a.max_pages + lp);
-            if (p >= 0 && p < a.num_pages) {
-              pg[h] = p;
-              bytes += 4096 + 256;
-            } else {
-              raise_flag(a.status, CSA_FLAG_PAGE_OOB);
-            }
-          }
-        }
+        const uint32_t bytes = (e.pg0 >= 0 ? 4352u : 0u) + (e.pg1 >= 0 ? 4352u : 0u);
         mbar_expect_tx(&sm.full[s], bytes);
-        for (int h = 0; h < 2; ++h) {
-          if (pg[h] < 0) continue;
-          tma_load_3d(sm.a[s] + 4096 * h, &tmap_data, &sm.full[s], 0, 0, pg[h]);
-          tma_load_2d(sm.sfa_raw[s] + 256 * h, &tmap_scale, &sm.full[s], 0, pg[h]);
+        if (e.pg0 >= 0) {
+          tma_load_3d(sm.a[s], &tmap_data, &sm.full[s], 0, 0, e.pg0);
+          tma_load_2d(sm.sfa_raw[s], &tmap_scale, &sm.full[s], 0, e.pg0);
         }
-        advance(W.tile_pref, S, seg, tile);
+        if (e.pg1 >= 0) {
+          tma_load_3d(sm.a[s] + 4096, &tmap_data, &sm.full[s], 0, 0, e.pg1);
+          tma_load_2d(sm.sfa_raw[s] + 256, &tmap_scale, &sm.full[s], 0, e.pg1);
+        }
       }
     } else if (warp == 1) {
       // ================= MMA issuer =================
-      int seg = find_seg(W.tile_pref, S, beg);
-      int tile = beg - W.tile_pref[seg];
-      int nq = 0, par = 0;
-      int N = 0;
-      for (int it = 0; beg + it < end; ++it) {
+      for (int i = 0; i < m; ++i) {
         if (sm.abort_flag) break;
-        const Seg sg = W.seg[seg];
-        if (it == 0 || tile == 0) {
-          par = nq & 1;
-          if (!wait_or_abort(&sm.qfull[par], (nq >> 1) & 1, sm, a.status)) break;
-          N = sg.nrows * Hp;
-          const int natoms = (N + 127) / 128;
-          for (int c = 0; c < natoms; ++c) {
-            // rows beyond N inside the last atom hold stale bytes; their D
-            // columns are never read.
-            sf_to_atom(sm.sfb_raw[par] + 512 * c, sm.sfb_atom[par] + 512 * c, lane);
-          }
+        const int it = it_base + i;
+        const Item e = sm.items[i];
+        const int gseg = seg0 + e.seg;
+        if (gseg != m_gseg) {
+          // the previous segment's q buffer is free once its MMAs complete
+          if (m_nq >= 1 && lane == 0) tc_commit(&sm.qempty[(m_nq - 1) & 1]);
+          m_par = m_nq & 1;
+          if (!wait_or_abort(&sm.qfull[m_par], (m_nq >> 1) & 1, sm, a.status)) break;
+          m_N = sm.segs[e.seg].nrows * Hp;
+          const int natoms = (m_N + 127) / 128;
+          // rows past N inside the last atom hold stale bytes; their D columns are never read
+          for (int c = 0; c < natoms; ++c)
+            sf_to_atom(sm.sfb_raw[m_par] + 512 * c, sm.sfb_atom[m_par] + 512 * c, lane);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             tc_fence_after();
             for (int c = 0; c < natoms; ++c)
-              tmem_cp_32x128b_x4(tmem + kTmemSF + 8 + 12 * par + 4 * c,
-                                 smem_desc(smem_u32(sm.sfb_atom[par] + 512 * c), 16, 128, kSwizzleNone));
+              tmem_cp_32x128b_x4(tmem + kTmemSFB + 12 * m_par + 4 * c,
+                                 smem_desc(smem_u32(sm.sfb_atom[m_par] + 512 * c), 16, 128, kSwizzleNone));
           }
-          ++nq;
+          ++m_nq;
+          m_gseg = gseg;
         }
         const int s = it % kStages;
         if (!wait_or_abort(&sm.full[s], (it / kStages) & 1, sm, a.status)) break;
@@ -385,15 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (k >= 1 && !wait_or_abort(&sm.tempty[d], (k - 1) & 1, sm, a.status)) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t sfa = tmem + kTmemSF + 4 * d;
+          const uint32_t sfa = tmem + kTmemSFA + 4 * d;
           tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[s]), 16, 128, kSwizzleNone));
           const uint32_t abase = smem_u32(sm.a[s]);
-          const uint32_t bbase = smem_u32(sm.qdata[par]);
+          const uint32_t bbase = smem_u32(sm.qdata[m_par]);
           const uint32_t dcol = tmem + kTmemD + d * dstride;
-          const int Nm = mma_n(N);
+          const int Nm = mma_n(m_N);
           for (int c = 0; c * 128 < Nm; ++c) {
             const uint32_t Nc = (uint32_t)min(128, Nm - c * 128);
-            const uint32_t sfb = tmem + kTmemSF + 8 + 12 * par + 4 * c;
+            const uint32_t sfb = tmem + kTmemSFB + 12 * m_par + 4 * c;
             const uint32_t bchunk = bbase + c * 128 * 64;
             mma_mxf4(dcol + c * 128, smem_desc(abase, 16, 512, kSwizzle64B),
                      smem_desc(bchunk, 16, 512, kSwizzle64B), idesc_mxf4(128, Nc, 0, 0), sfa, sfb, 0u);
@@ -403,38 +459,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(&sm.empty[s]);
           tc_commit(&sm.tfull[d]);
         }
-        const bool seg_end = (tile + 1 == (W.tile_pref[seg + 1] - W.tile_pref[seg])) || (beg + it + 1 == end);
-        if (seg_end && lane == 0) tc_commit(&sm.qempty[par]);
         __syncwarp();
-        advance(W.tile_pref, S, seg, tile);
       }
-    } else if (warp >= 4 && (warp - 4) / 4 < nbuf) {
-      // ================= epilogue =================
-      const int grp = (warp - 4) / 4;
+    } else if (grp >= 0 && grp < nbuf) {
+      // ================= epilogue group grp =================
       const int q = warp & 3;                       // TMEM lane quarter of this warp
-      const int m = 32 * q + lane;                  // entry within the tile
-      int seg = find_seg(W.tile_pref, S, beg);
-      int tile = beg - W.tile_pref[seg];
-      for (int it = 0; beg + it < end; ++it) {
-        const Seg sg = W.seg[seg];
-        const int cur_tile = tile;
-        advance(W.tile_pref, S, seg, tile);
-        if (it % nbuf != grp) continue;
+      const int mrow = 32 * q + lane;               // entry within the tile
+      float* ew = sm.wseg[warp - 4];                // this warp's copy of the segment's w
+      int32_t* en = sm.rown[warp - 4];              // and of its rows' visible lengths
+      int i = grp - (it_base % nbuf);
+      if (i < 0) i += nbuf;
+      for (; i < m; i += nbuf) {
         if (sm.abort_flag) break;
+        const int it = it_base + i;
+        const Item e = sm.items[i];
+        const Seg sg = sm.segs[e.seg];
+        const int gseg = seg0 + e.seg;
+        if (gseg != e_gseg) {                       // stage this segment's weights and row lengths
+          __syncwarp();                             // (per warp: no cross-warp barrier here)
+          for (int x = lane; x < sg.nrows * Hi; x += 32) ew[x] = __ldg(a.w + (size_t)sg.r0 * Hi + x);
+          for (int x = lane; x < sg.nrows; x += 32) en[x] = (__ldg(a.row_pos + sg.r0 + x) + 1) / a.P;
+          __syncwarp();
+          e_gseg = gseg;
+        }
         const int d = it % nbuf, k = it / nbuf;
         if (!wait_or_abort(&sm.tfull[d], k & 1, sm, a.status)) break;
         tc_fence_after();
-        const int i = cur_tile * kTileEntries + m;
-        const int lp = i / PAGE;
-        bool page_ok = false;
-        if (i < sg.n) {
-          const int p = __ldg(a.page_table + (size_t)sg.b * a.max_pages + lp);
-          page_ok = (p >= 0 && p < a.num_pages);
-        }
+        const int ient = e.tile * kTileEntries + mrow;
+        const bool page_ok = (mrow < 64) ? (e.pg0 >= 0) : (e.pg1 >= 0);
         const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + kTmemD + d * dstride;
         for (int kr = 0; kr < sg.nrows; ++kr) {
-          const int r = sg.r0 + kr;
-          const float* wr = a.w + (size_t)r * Hi;
+          const float* wr = ew + kr * Hi;
           float acc = 0.0f;
           for (int h0 = 0; h0 < Hi; h0 += 16) {
             uint32_t v[16];
@@ -445,18 +500,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (h0 + j < Hi) {
                 const float dot = __uint_as_float(v[j]);
                 const float rl = dot > 0.0f ? dot : 0.0f;
-                acc = __fadd_rn(acc, __fmul_rn(__ldg(wr + h0 + j), rl));
+                acc = __fadd_rn(acc, __fmul_rn(wr[h0 + j], rl));
               }
             }
           }
-          const int nr = (__ldg(a.row_pos + r) + 1) / a.P;
-          if (i < nr && i < sg.n) a.scores[(size_t)r * a.ld + i] = page_ok ? acc : -INFINITY;
+          if (ient < en[kr] && ient < sg.n)
+            a.scores[(size_t)(sg.r0 + kr) * a.ld + ient] = page_ok ? acc : -INFINITY;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.tempty[d]);
       }
     }
+    // ---- chunk done: every role has finished with this work table ----------------
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    seg0 += sm.items[m - 1].seg;
+    it_base += m;
+    c0 = c1;
+    __syncthreads();
   }
   tc_fence_before();
   __syncthreads();
@@ -479,7 +542,9 @@ cudaError_t launch_index_score(const ScoreArgs& a, const void* tmap_data, const 
                                cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;
   uint8_t* ws = reinterpret_cast<uint8_t*>(a.status);
-  k_score_prep<<<1 + a.num_rows, 128, 0, stream>>>(a, ws);
+  ScoreArgs ap = a;
+  ap.grid = num_sms < kMaxGrid ? num_sms : kMaxGrid;
+  k_score_prep<<<1 + a.num_rows, 128, 0, stream>>>(ap, ws);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(ScoreSmem) + 1024;
@@ -487,7 +552,7 @@ cudaError_t launch_index_score(const ScoreArgs& a, const void* tmap_data, const 
   if (e != cudaSuccess) return e;
   const CUtensorMap* td = reinterpret_cast<const CUtensorMap*>(tmap_data);
   const CUtensorMap* ts = reinterpret_cast<const CUtensorMap*>(tmap_scale);
-  k_index_score<<<num_sms, kThreads, smem, stream>>>(a, ws, *td, *ts);
+  k_index_score<<<ap.grid, kThreads, smem, stream>>>(ap, ws, *td, *ts);
   return cudaGetLastError();
 }
 
