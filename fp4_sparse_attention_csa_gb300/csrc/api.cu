@@ -1,9 +1,6 @@
 // The C ABI (include/csa.h): argument validation, workspace carving, TMA
 // tensor-map encoding and kernel launches.  No allocation, no host sync
 // except in csa_check_device_status.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -24,47 +21,11 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) & ~(a - 1); }
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-bool get_encode() {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode != nullptr;
-}
-
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   return n;
-}
-
-// Indexer pool as TMA tensors: data [pages][64 entries][64 B] with the 64-byte
-// swizzle the MMA descriptor expects, and scales [pages][256 B].
-bool encode_idx_maps(const csa_cache_t* c, CUtensorMap* data, CUtensorMap* scale) {
-  if (!get_encode()) return false;
-  const cuuint64_t dims_d[3] = {64, 64, (cuuint64_t)c->num_pages};
-  const cuuint64_t strides_d[2] = {64, CSA_IDX_PAGE_BYTES};
-  const cuuint32_t box_d[3] = {64, 64, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = g_encode(data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c->idx_pool, dims_d, strides_d, box_d, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return false;
-  const cuuint64_t dims_s[2] = {256, (cuuint64_t)c->num_pages};
-  const cuuint64_t strides_s[1] = {CSA_IDX_PAGE_BYTES};
-  const cuuint32_t box_s[2] = {256, 1};
-  r = g_encode(scale, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, static_cast<uint8_t*>(c->idx_pool) + 4096, dims_s,
-               strides_s, box_s, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
 }
 
 csa_status_t check_cache(const csa_cache_t* c) {
@@ -109,9 +70,8 @@ csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_E
 
 csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t Hi, const void* q_idx,
                        const float* w, float* scores, int64_t ld, void* ws, cudaStream_t stream) {
-  CUtensorMap tm_data, tm_scale;
-  if (!encode_idx_maps(cache, &tm_data, &tm_scale)) return CSA_ERR_CUDA;
   ScoreArgs a;
+  a.idx_pool = cache->idx_pool;
   a.page_table = cache->page_table;
   a.num_pages = cache->num_pages;
   a.num_requests = cache->num_requests;
@@ -137,7 +97,7 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
   a.scores = scores;
   a.ld = ld;
   a.status = static_cast<uint32_t*>(ws);
-  return from_cuda(launch_index_score(a, &tm_data, &tm_scale, num_sms(), stream));
+  return from_cuda(launch_index_score(a, num_sms(), stream));
 }
 
 csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,

@@ -160,8 +160,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
         for (int i = 0; i < 4; ++i) codes |= e2m1_rne(y[i] * inv) << (4 * i);
       }
       uint8_t* ixp = a.idx_pool + (size_t)page * IDX_PAGE;
-      *reinterpret_cast<uint16_t*>(ixp + slot * 64 + lane * 2) = (uint16_t)codes;
-      if ((lane & 7) == 0) ixp[IDX_SCALE_OFF + slot * 4 + (lane >> 3)] = (uint8_t)E8;
+      *reinterpret_cast<uint16_t*>(ixp + idx_data_off(slot, 2 * lane)) = (uint16_t)codes;
+      if ((lane & 7) == 0) ixp[idx_scale_off(slot, lane >> 3)] = (uint8_t)E8;
     }
   }
 

@@ -26,8 +26,9 @@ struct AppendArgs {
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 
-// Indexer score: one CTA walks (request, row group, 128-entry tile) work items.
+// Indexer score: k_score_prep + the persistent tcgen05 score kernel.
 struct ScoreArgs {
+  const void* idx_pool;
   const int32_t* page_table;
   int32_t num_pages, num_requests, max_pages, P;
   const int32_t* row_req;
@@ -38,13 +39,10 @@ struct ScoreArgs {
   const float* w;                      // [R, Hi]
   float* scores;                       // [R, ld]
   int64_t ld;
-  uint32_t* status;
+  uint32_t* status;                    // head of the workspace
   int32_t grid;                        // score CTAs (set by the launcher)
 };
-// tmaps: 3-D tensor maps over idx_pool: [0] data (64 B x 64 entries x pages),
-// [1] scales (256 B x 1 x pages).
-cudaError_t launch_index_score(const ScoreArgs& a, const void* tmap_data, const void* tmap_scale,
-                               int num_sms, cudaStream_t stream);
+cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, cudaStream_t stream);
 
 struct TopkArgs {
   const float* scores;

@@ -10,23 +10,26 @@
 // Two kernels:
 //  k_score_prep  block 0 builds the segment table (a segment = up to
 //                `group_rows` consecutive rows of one request, scored by one
-//                MMA N dimension); blocks 1..R quantise each row's q_idx to
-//                MXFP4 straight into the shared-memory image the MMA reads
-//                (64-byte swizzled K-major rows + one E8M0 byte per 32).
-//  k_index_score persistent, one CTA per SM, 12 warps:
-//                warp 0  TMA producer: two indexer pages (128 entries) per
-//                        work item into an 8-stage ring (data with 64 B swizzle,
-//                        scales plain); the segment's q image by bulk copy.
-//                warp 1  MMA issuer: rearranges the E8M0 bytes into the
-//                        tcgen05 scale-factor layout, tcgen05.cp to TMEM, two
-//                        kind::mxf4 MMAs (K = 64 each) per N chunk of 128.
-//                        A = 128 entries x 128 dims, B = rows*heads x 128 dims,
-//                        D = fp32 [entry lane, row*head column] in TMEM.
-//                warps 4-7, 8-11  epilogue groups (one per TMEM accumulator
-//                        buffer): per entry lane, sum_h w*relu(D) in head order,
-//                        coalesced fp32 score stores.
-#include <cuda.h>
-
+//                MMA N dimension) and each score CTA's first segment; blocks
+//                1..R quantise each row's q_idx to MXFP4 straight into the
+//                shared-memory image the MMA reads.
+//  k_index_score persistent, one CTA per SM.  A work table of (segment, tile,
+//                pages) items is built in shared memory first, so no role
+//                touches global metadata per tile.  Roles:
+//                4 producer warps  one bulk copy per indexer page (4352 B: the
+//                        page layout is already the MMA operand layout), two
+//                        pages = one 128-entry tile per stage, 12 stages; the
+//                        copy engine is fed by several warps because one
+//                        warp's copy issue rate caps its bandwidth.
+//                scale warp  gathers the tile's E8M0 bytes into the tcgen05
+//                        scale-factor atom (and the q scales per segment).
+//                MMA thread  tcgen05.cp of the scales, two kind::mxf4 MMAs
+//                        (K = 64 each) per 128-column N chunk; A = 128 entries
+//                        x 128 dims, B = rows*heads x 128 dims, D = fp32 [entry
+//                        lane, row*head column] in TMEM.
+//                4 epilogue warp groups on 4 TMEM accumulator buffers: per
+//                        entry lane, sum_h w*relu(D) in head order, coalesced
+//                        fp32 score stores.
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
@@ -38,17 +41,19 @@ struct Seg {
   int32_t b, r0, nrows, n;
 };
 
-constexpr int kStages = 8;
+constexpr int kStages = 12;
 constexpr int kMaxBuf = 4;                     // TMEM accumulator buffers = epilogue groups
-constexpr int kThreads = 128 + 128 * kMaxBuf;  // warps 0-3: producer, MMA, 2 idle; then groups
+constexpr int kProducers = 4;                  // producer warps: 0, 3 and the last two
+constexpr int kWarps = 4 + 4 * kMaxBuf + 2;
+constexpr int kThreads = 32 * kWarps;
 constexpr int kEpiWarps = 4 * kMaxBuf;
 constexpr int kTileEntries = 128;
-constexpr int kStageA = 8192;        // 128 entries x 64 B (two pages)
-constexpr int kStageSF = 512;        // 128 entries x 4 E8M0 bytes (raw page order)
+constexpr int kStageA = 2 * IDX_PAGE;          // two whole pages = 16 groups of 544 B
+constexpr int kStageSF = 512;                  // scale-factor atom of 128 rows
 constexpr int kMaxN = CSA_MAX_ROW_GROUP_COLS;  // rows x padded heads per MMA group
 constexpr int kQData = kMaxN * 64;   // 24576
 constexpr int kQSF = kMaxN * 4;      // 1536
-constexpr int kItemCap = 1024;       // work items per table chunk
+constexpr int kItemCap = 512;        // work items per table chunk
 constexpr int kMaxGroupRows = 64;    // rows per segment (kMaxN / 8 heads at least)
 constexpr int kTmemSFA = 0, kTmemSFB = 16, kTmemD = 48;
 
@@ -57,9 +62,8 @@ struct Item {
 };
 
 struct ScoreSmem {
-  uint8_t a[kStages][kStageA];                 // 1024-aligned
   uint8_t qdata[2][kQData];                    // 1024-aligned (24576 = 24 * 1024)
-  uint8_t sfa_raw[kStages][kStageSF];
+  uint8_t a[kStages][kStageA];                 // 16-aligned (8704 = 544 * 16)
   uint8_t sfa_atom[kStages][kStageSF];
   uint8_t sfb_raw[2][kQSF];
   uint8_t sfb_atom[2][kQSF];
@@ -68,9 +72,9 @@ struct ScoreSmem {
   int32_t pref[kItemCap + 1];
   float wseg[kEpiWarps][kMaxN];
   int32_t rown[kEpiWarps][kMaxGroupRows];
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full[kStages], empty[kStages], sfready[kStages];
   uint64_t tfull[kMaxBuf], tempty[kMaxBuf];
-  uint64_t qfull[2], qempty[2];
+  uint64_t qfull[2], qempty[2], qready[2];
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -281,14 +285,17 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sc
   return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    k_index_score(ScoreArgs a, uint8_t* ws, const __grid_constant__ CUtensorMap tmap_data,
-                  const __grid_constant__ CUtensorMap tmap_scale) {
+__device__ __forceinline__ int producer_index(int warp) {
+  return warp == 0 ? 0 : (warp == 3 ? 1 : (warp >= kWarps - 2 ? warp - (kWarps - 2) + 2 : -1));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_t* ws) {
   extern __shared__ uint8_t smem_raw[];
   ScoreSmem& sm = *reinterpret_cast<ScoreSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int Hi = a.Hi, Hp = hi_pad(Hi);
   ScoreWs W = carve_score_ws(ws, a.num_rows, Hi);
   const int warp = warp_id(), lane = lane_id(), tid = threadIdx.x;
+  const uint8_t* ipool = static_cast<const uint8_t*>(a.idx_pool);
 
   const int S = W.nseg[0], total = W.nseg[1];
   const int per = (total + gridDim.x - 1) / gridDim.x;
@@ -304,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.sfready[s], 1);
     }
     for (int d = 0; d < kMaxBuf; ++d) {
       mbar_init(&sm.tfull[d], 1);
@@ -312,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int d = 0; d < 2; ++d) {
       mbar_init(&sm.qfull[d], 1);
       mbar_init(&sm.qempty[d], 1);
+      mbar_init(&sm.qready[d], 1);
     }
     sm.abort_flag = 0;
     fence_barrier_init();
@@ -322,11 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  // role state that persists across work chunks
-  int p_nq = 0, p_gseg = -1;                 // producer: q images loaded, current segment
-  int m_nq = 0, m_gseg = -1, m_par = 0, m_N = 0;
-  int e_gseg = -1;                           // epilogue: segment whose w / n are staged
-  const int grp = (warp >= 4) ? (warp - 4) >> 2 : -1;
+  // Role state kept across work chunks.  A segment's ordinal within this CTA
+  // (ord) picks its q buffer (ord & 1) and the phases of the q barriers.
+  const int prod = producer_index(warp);
+  int f_s = 0, f_use = 0, f_ord = -1;                        // scale-factor warp
+  int m_ord = -1, m_par = 0, m_N = 0;                        // MMA issuer
+  int m_s = 0, m_use = 0, m_d = 0, m_round = 0;
+  int e_gseg = -1, e_round = 0;                              // epilogue
+  int last_ord = -1;                                         // ordinal of the previous chunk's last item
+  int ord_base = 0;                                          // ordinal of this chunk's first segment
 
   int seg0 = (beg < end) ? W.cta_seg[blockIdx.x] : S;
   int it_base = 0;
@@ -371,98 +384,123 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    if (warp == 0 && lane == 0) {
-      // ================= TMA producer =================
-      for (int i = 0; i < m; ++i) {
+    if (prod >= 0 && lane == 0) {
+      // ================= producers: items it with it % kProducers == prod =================
+      int i = prod - (it_base % kProducers);
+      if (i < 0) i += kProducers;
+      for (; i < m; i += kProducers) {
         if (sm.abort_flag) break;
         const int it = it_base + i;
         const Item e = sm.items[i];
-        const int gseg = seg0 + e.seg;
-        if (gseg != p_gseg) {
+        const int ord = ord_base + e.seg;
+        const int prev_ord = (i > 0) ? ord_base + sm.items[i - 1].seg : last_ord;
+        if (ord != prev_ord) {                         // first item of a segment: load its q image
           const Seg sg = sm.segs[e.seg];
-          const int par = p_nq & 1;
-          if (p_nq >= 2 && !wait_or_abort(&sm.qempty[par], ((p_nq >> 1) - 1) & 1, sm, a.status)) break;
+          const int par = ord & 1;
+          if (ord >= 2 && !wait_or_abort(&sm.qempty[par], ((ord >> 1) - 1) & 1, sm, a.status)) break;
           const uint32_t bytes_d = (uint32_t)(sg.nrows * Hp * 64), bytes_s = (uint32_t)(sg.nrows * Hp * 4);
           mbar_expect_tx(&sm.qfull[par], bytes_d + bytes_s);
           if (bytes_d > 0) {   // nrows is in [1, group_rows] whenever the segment has tiles
             bulk_load(sm.qdata[par], W.qimg + (size_t)sg.r0 * Hp * 64, bytes_d, &sm.qfull[par]);
             bulk_load(sm.sfb_raw[par], W.qsf + (size_t)sg.r0 * Hp * 4, bytes_s, &sm.qfull[par]);
           }
-          ++p_nq;
-          p_gseg = gseg;
         }
-        const int s = it % kStages;
-        if (it >= kStages && !wait_or_abort(&sm.empty[s], ((it / kStages) - 1) & 1, sm, a.status)) break;
-        const uint32_t bytes = (e.pg0 >= 0 ? 4352u : 0u) + (e.pg1 >= 0 ? 4352u : 0u);
+        const int s = it % kStages, use = it / kStages;
+        if (use > 0 && !wait_or_abort(&sm.empty[s], (use - 1) & 1, sm, a.status)) break;
+        const uint32_t bytes = (e.pg0 >= 0 ? (uint32_t)IDX_PAGE : 0u) + (e.pg1 >= 0 ? (uint32_t)IDX_PAGE : 0u);
         mbar_expect_tx(&sm.full[s], bytes);
-        if (e.pg0 >= 0) {
-          tma_load_3d(sm.a[s], &tmap_data, &sm.full[s], 0, 0, e.pg0);
-          tma_load_2d(sm.sfa_raw[s], &tmap_scale, &sm.full[s], 0, e.pg0);
-        }
-        if (e.pg1 >= 0) {
-          tma_load_3d(sm.a[s] + 4096, &tmap_data, &sm.full[s], 0, 0, e.pg1);
-          tma_load_2d(sm.sfa_raw[s] + 256, &tmap_scale, &sm.full[s], 0, e.pg1);
-        }
+        if (e.pg0 >= 0) bulk_load(sm.a[s], ipool + (size_t)e.pg0 * IDX_PAGE, IDX_PAGE, &sm.full[s]);
+        if (e.pg1 >= 0) bulk_load(sm.a[s] + IDX_PAGE, ipool + (size_t)e.pg1 * IDX_PAGE, IDX_PAGE, &sm.full[s]);
       }
-    } else if (warp == 1) {
-      // ================= MMA issuer =================
+    } else if (warp == 2) {
+      // ================= scale-factor warp =================
       for (int i = 0; i < m; ++i) {
         if (sm.abort_flag) break;
-        const int it = it_base + i;
         const Item e = sm.items[i];
-        const int gseg = seg0 + e.seg;
-        if (gseg != m_gseg) {
-          // the previous segment's q buffer is free once its MMAs complete
-          if (m_nq >= 1 && lane == 0) tc_commit(&sm.qempty[(m_nq - 1) & 1]);
-          m_par = m_nq & 1;
-          if (!wait_or_abort(&sm.qfull[m_par], (m_nq >> 1) & 1, sm, a.status)) break;
-          m_N = sm.segs[e.seg].nrows * Hp;
-          const int natoms = (m_N + 127) / 128;
+        const int ord = ord_base + e.seg;
+        if (ord != f_ord) {
+          const int par = ord & 1;
+          if (!wait_or_abort(&sm.qfull[par], (ord >> 1) & 1, sm, a.status)) break;
+          const int natoms = (sm.segs[e.seg].nrows * Hp + 127) / 128;
           // rows past N inside the last atom hold stale bytes; their D columns are never read
           for (int c = 0; c < natoms; ++c)
-            sf_to_atom(sm.sfb_raw[m_par] + 512 * c, sm.sfb_atom[m_par] + 512 * c, lane);
+            sf_to_atom(sm.sfb_raw[par] + 512 * c, sm.sfb_atom[par] + 512 * c, lane);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            tc_fence_after();
-            for (int c = 0; c < natoms; ++c)
-              tmem_cp_32x128b_x4(tmem + kTmemSFB + 12 * m_par + 4 * c,
-                                 smem_desc(smem_u32(sm.sfb_atom[m_par] + 512 * c), 16, 128, kSwizzleNone));
-          }
-          ++m_nq;
-          m_gseg = gseg;
+          if (lane == 0) mbar_arrive(&sm.qready[par]);
+          f_ord = ord;
         }
-        const int s = it % kStages;
-        if (!wait_or_abort(&sm.full[s], (it / kStages) & 1, sm, a.status)) break;
-        sf_to_atom(sm.sfa_raw[s], sm.sfa_atom[s], lane);
+        if (!wait_or_abort(&sm.full[f_s], f_use & 1, sm, a.status)) break;
+        // entry row r of the tile: page r / 64, group (r % 64) / 8, scale word (r % 8)
+        const uint8_t* st = sm.a[f_s];
+        uint32_t wv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane + 32 * j;
+          wv[j] = *reinterpret_cast<const uint32_t*>(st + (r >> 6) * IDX_PAGE + idx_scale_off(r & 63, 0));
+        }
+        reinterpret_cast<uint4*>(sm.sfa_atom[f_s])[lane] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         fence_proxy_async_smem();
         __syncwarp();
-        const int d = it % nbuf, k = it / nbuf;
-        if (k >= 1 && !wait_or_abort(&sm.tempty[d], (k - 1) & 1, sm, a.status)) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sfa = tmem + kTmemSFA + 4 * d;
-          tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[s]), 16, 128, kSwizzleNone));
-          const uint32_t abase = smem_u32(sm.a[s]);
-          const uint32_t bbase = smem_u32(sm.qdata[m_par]);
-          const uint32_t dcol = tmem + kTmemD + d * dstride;
-          const int Nm = mma_n(m_N);
-          for (int c = 0; c * 128 < Nm; ++c) {
-            const uint32_t Nc = (uint32_t)min(128, Nm - c * 128);
-            const uint32_t sfb = tmem + kTmemSFB + 12 * m_par + 4 * c;
-            const uint32_t bchunk = bbase + c * 128 * 64;
-            mma_mxf4(dcol + c * 128, smem_desc(abase, 16, 512, kSwizzle64B),
-                     smem_desc(bchunk, 16, 512, kSwizzle64B), idesc_mxf4(128, Nc, 0, 0), sfa, sfb, 0u);
-            mma_mxf4(dcol + c * 128, smem_desc(abase + 32, 16, 512, kSwizzle64B),
-                     smem_desc(bchunk + 32, 16, 512, kSwizzle64B), idesc_mxf4(128, Nc, 2, 2), sfa, sfb, 1u);
-          }
-          tc_commit(&sm.empty[s]);
-          tc_commit(&sm.tfull[d]);
+        if (lane == 0) mbar_arrive(&sm.sfready[f_s]);
+        if (++f_s == kStages) {
+          f_s = 0;
+          ++f_use;
         }
-        __syncwarp();
       }
-    } else if (grp >= 0 && grp < nbuf) {
+    } else if (warp == 1 && lane == 0) {
+      // ================= MMA issuer (one thread) =================
+      for (int i = 0; i < m; ++i) {
+        if (sm.abort_flag) break;
+        const Item e = sm.items[i];
+        const int ord = ord_base + e.seg;
+        if (ord != m_ord) {
+          // the previous segment's q buffer is free once its MMAs complete
+          if (m_ord >= 0) tc_commit(&sm.qempty[m_ord & 1]);
+          m_par = ord & 1;
+          if (!wait_or_abort(&sm.qready[m_par], (ord >> 1) & 1, sm, a.status)) break;
+          m_N = sm.segs[e.seg].nrows * Hp;
+          const int natoms = (m_N + 127) / 128;
+          tc_fence_after();
+          for (int c = 0; c < natoms; ++c)
+            tmem_cp_32x128b_x4(tmem + kTmemSFB + 12 * m_par + 4 * c,
+                               smem_desc(smem_u32(sm.sfb_atom[m_par] + 512 * c), 16, 128, kSwizzleNone));
+          m_ord = ord;
+        }
+        if (!wait_or_abort(&sm.sfready[m_s], m_use & 1, sm, a.status)) break;
+        if (m_round > 0 && !wait_or_abort(&sm.tempty[m_d], (m_round - 1) & 1, sm, a.status)) break;
+        tc_fence_after();
+        const uint32_t sfa = tmem + kTmemSFA + 4 * m_d;
+        tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[m_s]), 16, 128, kSwizzleNone));
+        // A: the two pages as they landed: 8-entry groups IDX_GROUP apart, 16-byte
+        // core matrices 128 B apart along K (no swizzle); second K half at +256 B
+        const uint32_t abase = smem_u32(sm.a[m_s]);
+        const uint32_t bbase = smem_u32(sm.qdata[m_par]);
+        const uint32_t dcol = tmem + kTmemD + m_d * dstride;
+        const int Nm = mma_n(m_N);
+        for (int c = 0; c * 128 < Nm; ++c) {
+          const uint32_t Nc = (uint32_t)min(128, Nm - c * 128);
+          const uint32_t sfb = tmem + kTmemSFB + 12 * m_par + 4 * c;
+          const uint32_t bchunk = bbase + c * 128 * 64;
+          mma_mxf4(dcol + c * 128, smem_desc(abase, 128, IDX_GROUP, kSwizzleNone),
+                   smem_desc(bchunk, 16, 512, kSwizzle64B), idesc_mxf4(128, Nc, 0, 0), sfa, sfb, 0u);
+          mma_mxf4(dcol + c * 128, smem_desc(abase + 256, 128, IDX_GROUP, kSwizzleNone),
+                   smem_desc(bchunk + 32, 16, 512, kSwizzle64B), idesc_mxf4(128, Nc, 2, 2), sfa, sfb, 1u);
+        }
+        tc_commit(&sm.empty[m_s]);
+        tc_commit(&sm.tfull[m_d]);
+        if (++m_s == kStages) {
+          m_s = 0;
+          ++m_use;
+        }
+        if (++m_d == nbuf) {
+          m_d = 0;
+          ++m_round;
+        }
+      }
+    } else if (warp >= 4 && warp < 4 + kEpiWarps && ((warp - 4) >> 2) < nbuf) {
       // ================= epilogue group grp =================
+      const int grp = (warp - 4) >> 2;
       const int q = warp & 3;                       // TMEM lane quarter of this warp
       const int mrow = 32 * q + lane;               // entry within the tile
       float* ew = sm.wseg[warp - 4];                // this warp's copy of the segment's w
@@ -471,7 +509,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (i < 0) i += nbuf;
       for (; i < m; i += nbuf) {
         if (sm.abort_flag) break;
-        const int it = it_base + i;
         const Item e = sm.items[i];
         const Seg sg = sm.segs[e.seg];
         const int gseg = seg0 + e.seg;
@@ -482,16 +519,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           e_gseg = gseg;
         }
-        const int d = it % nbuf, k = it / nbuf;
-        if (!wait_or_abort(&sm.tfull[d], k & 1, sm, a.status)) break;
+        if (!wait_or_abort(&sm.tfull[grp], e_round & 1, sm, a.status)) break;
         tc_fence_after();
         const int ient = e.tile * kTileEntries + mrow;
         const bool page_ok = (mrow < 64) ? (e.pg0 >= 0) : (e.pg1 >= 0);
-        const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + kTmemD + d * dstride;
+        const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + kTmemD + grp * dstride;
         for (int kr = 0; kr < sg.nrows; ++kr) {
           const float* wr = ew + kr * Hi;
           float acc = 0.0f;
-          for (int h0 = 0; h0 < Hi; h0 += 16) {
+          int h0 = 0;
+          for (; h0 + 32 <= Hi; h0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(dbase + kr * Hp + h0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float dot = __uint_as_float(v[j]);
+              acc = __fadd_rn(acc, __fmul_rn(wr[h0 + j], dot > 0.0f ? dot : 0.0f));
+            }
+          }
+          for (; h0 < Hi; h0 += 16) {
             uint32_t v[16];
             tmem_ld16(dbase + kr * Hp + h0, v);
             tmem_ld_wait();
@@ -499,8 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 16; ++j) {
               if (h0 + j < Hi) {
                 const float dot = __uint_as_float(v[j]);
-                const float rl = dot > 0.0f ? dot : 0.0f;
-                acc = __fadd_rn(acc, __fmul_rn(wr[h0 + j], rl));
+                acc = __fadd_rn(acc, __fmul_rn(wr[h0 + j], dot > 0.0f ? dot : 0.0f));
               }
             }
           }
@@ -509,13 +555,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.tempty[d]);
+        if (lane == 0) mbar_arrive(&sm.tempty[grp]);
+        ++e_round;
       }
     }
     // ---- chunk done: every role has finished with this work table ----------------
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    last_ord = ord_base + sm.items[m - 1].seg;
+    ord_base = last_ord;
     seg0 += sm.items[m - 1].seg;
     it_base += m;
     c0 = c1;
@@ -538,8 +587,7 @@ size_t score_ws_bytes(int32_t R, int32_t Hi) {
 
 int score_group_rows(int32_t Hi) { return kMaxN / hi_pad(Hi); }
 
-cudaError_t launch_index_score(const ScoreArgs& a, const void* tmap_data, const void* tmap_scale, int num_sms,
-                               cudaStream_t stream) {
+cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;
   uint8_t* ws = reinterpret_cast<uint8_t*>(a.status);
   ScoreArgs ap = a;
@@ -550,9 +598,7 @@ cudaError_t launch_index_score(const ScoreArgs& a, const void* tmap_data, const 
   const size_t smem = sizeof(ScoreSmem) + 1024;
   e = cudaFuncSetAttribute(k_index_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const CUtensorMap* td = reinterpret_cast<const CUtensorMap*>(tmap_data);
-  const CUtensorMap* ts = reinterpret_cast<const CUtensorMap*>(tmap_scale);
-  k_index_score<<<ap.grid, kThreads, smem, stream>>>(ap, ws, *td, *ts);
+  k_index_score<<<ap.grid, kThreads, smem, stream>>>(ap, ws);
   return cudaGetLastError();
 }
 

@@ -33,10 +33,14 @@
  *    s = E4M3(amax/6), codes = RNE(x/s)).
  *  - Indexer-K entry (68 B): 128 e2m1 + one E8M0 scale per 32 values (MXFP4,
  *    OCP MX rule: scale 2^(floor(log2 amax) - 2)).
- *  - Pages of 64 entries, data block then scale block, so every TMA stride is
- *    a multiple of 16 B:
+ *  - Pages of 64 entries:
  *      main-KV page 18432 B: entry e data at 256*e, scales at 16384 + 32*e
- *      indexer page  4352 B: entry e data at  64*e, scales at  4096 +  4*e
+ *      indexer page  4352 B: 8 groups of 544 B, group g = entries 8g..8g+7;
+ *        data byte k (0..63) of entry 8g+r at 544*g + 128*(k/16) + 16*r + k%16
+ *        (16-byte core matrices of 8 entries, the tensor-core operand order),
+ *        scale byte b (0..3) of entry 8g+r at 544*g + 512 + 4*r + b.
+ *    A whole indexer page is therefore one contiguous copy that lands in
+ *    shared memory as an MMA operand (8-entry groups 544 B apart).
  *    page_table[b*max_pages_per_req + j] = physical page of request b's j-th
  *    logical page; the same id indexes both pools.
  *  - Entry e of a request pools tokens P*e .. P*e+P-1 (P = pool_ratio, 2 or 1):

@@ -171,10 +171,16 @@ class Cache:
                 self.kv_pool[base + 16384 + (e % 64) * 32: base + 16384 + (e % 64) * 32 + 32])
 
     def idx_entry(self, b, e):
+        """(data[64], scales[4]) of indexer entry e: 8-entry groups of 544 B,
+        data byte k of slot 8g+r at 544g + 128(k//16) + 16r + k%16, scale byte
+        j at 544g + 512 + 4r + j."""
         page = int(self.page_table[b, e // 64])
-        base = page * IDX_PAGE
-        return (self.idx_pool[base + (e % 64) * 64: base + (e % 64) * 64 + 64],
-                self.idx_pool[base + 4096 + (e % 64) * 4: base + 4096 + (e % 64) * 4 + 4])
+        base = page * IDX_PAGE + 544 * ((e % 64) // 8)
+        r = (e % 64) % 8
+        k = np.arange(64)
+        data = self.idx_pool[base + 128 * (k // 16) + 16 * r + k % 16]
+        sc = self.idx_pool[base + 512 + 4 * r + np.arange(4)]
+        return data, sc
 
     def window_slot(self, b, p):
         s = b * self.win_cap + p % self.win_cap

@@ -17,10 +17,11 @@
  * [SGL] "Architecture changes and KV cache compression": a main-KV entry is
  * 288 bytes and an indexer-K entry 68 bytes.  Main KV = 512 e2m1 values
  * (256 B) + one E4M3 scale per 16 values (32 B); indexer K = 128 e2m1 values
- * (64 B) + one E8M0 scale per 32 values (4 B).  Pages hold 64 entries, data
- * block first, then the scale block:
- *   main-KV page  18432 B: entry e data at 256*e, scales at 16384 + 32*e
- *   indexer page   4352 B: entry e data at  64*e, scales at  4096 +  4*e
+ * (64 B) + one E8M0 scale per 32 values (4 B).  Pages hold 64 entries:
+ *   main-KV page 18432 B: entry e data at 256*e, scales at 16384 + 32*e
+ *   indexer page  4352 B: 8 groups of 544 B, group g = entries 8g..8g+7:
+ *     data byte k (0..63) of entry 8g+r at 544*g + 128*(k/16) + 16*r + k%16,
+ *     scale byte b (0..3) of entry 8g+r at 544*g + 512 + 4*r + b.
  * Element 2j sits in the low nibble of byte j, element 2j+1 in the high one. */
 #define OR_D            512
 #define OR_DI           128
@@ -28,7 +29,15 @@
 #define OR_KV_PAGE      18432
 #define OR_KV_SCALE_OFF 16384
 #define OR_IDX_PAGE     4352
-#define OR_IDX_SCALE_OFF 4096
+#define OR_IDX_GROUP    544
+
+/* byte offsets of an indexer entry's data byte k / scale byte b in its page */
+static int64_t idx_data_off(int64_t slot, int k) {
+  return OR_IDX_GROUP * (slot / 8) + 128 * (k / 16) + 16 * (slot % 8) + k % 16;
+}
+static int64_t idx_scale_off(int64_t slot, int b) {
+  return OR_IDX_GROUP * (slot / 8) + 512 + 4 * (slot % 8) + b;
+}
 #define OR_TOPK         512
 #define OR_WINDOW       128
 
@@ -252,7 +261,10 @@ int or_append(const or_cache_t* c, const int32_t* pos0, const int32_t* tok_off,
       uint8_t* kvp = c->kv_pool + (int64_t)page * OR_KV_PAGE;
       uint8_t* ixp = c->idx_pool + (int64_t)page * OR_IDX_PAGE;
       or_quant_main_entry(x, kvp + slot * 256, kvp + OR_KV_SCALE_OFF + slot * 32);
-      or_quant_idx_entry(y, ixp + slot * 64, ixp + OR_IDX_SCALE_OFF + slot * 4);
+      uint8_t idata[64], iscale[4];
+      or_quant_idx_entry(y, idata, iscale);
+      for (int k = 0; k < 64; ++k) ixp[idx_data_off(slot, k)] = idata[k];
+      for (int b2 = 0; b2 < 4; ++b2) ixp[idx_scale_off(slot, b2)] = iscale[b2];
     }
     if (P == 2 && T > 0 && ((pos0[b] + T - 1) % 2) == 0) {
       uint16_t* dst = pending_out + (int64_t)b * (OR_D + OR_DI);
@@ -279,8 +291,9 @@ static int32_t row_visible(int32_t pos, int32_t P) { return (pos + 1) / P; }
 static void dequant_idx_entry(const or_cache_t* c, int32_t req, int32_t e, float* k128) {
   int32_t page = c->page_table[(int64_t)req * c->max_pages_per_req + e / OR_PAGE];
   const uint8_t* ixp = c->idx_pool + (int64_t)page * OR_IDX_PAGE;
-  const uint8_t* data = ixp + (e % OR_PAGE) * 64;
-  const uint8_t* sc = ixp + OR_IDX_SCALE_OFF + (e % OR_PAGE) * 4;
+  uint8_t data[64], sc[4];
+  for (int k = 0; k < 64; ++k) data[k] = ixp[idx_data_off(e % OR_PAGE, k)];
+  for (int b = 0; b < 4; ++b) sc[b] = ixp[idx_scale_off(e % OR_PAGE, b)];
   for (int d = 0; d < OR_DI; ++d) k128[d] = or_e2m1_decode(nibble(data, d)) * or_e8m0_decode(sc[d / 32]);
 }
 

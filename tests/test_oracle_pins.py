@@ -366,3 +366,20 @@ def test_window_quantiser_against_library_e4m3():
     assert s == np.float32(np.abs(x).max()) / np.float32(448)
     ref = torch.tensor(x / np.float32(s)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
     assert np.array_equal(codes, ref.numpy())
+
+
+def test_indexer_page_byte_layout():
+    """An indexer entry's bytes sit where the format description puts them:
+    8-entry groups of 544 B, data byte k of slot 8g+r at 544g + 128(k//16) +
+    16r + k%16, scale byte j at 544g + 512 + 4r + j."""
+    wl = W.custom("layout", 9, [2 * 29 + 2], [1], H=1, Hi=1, P=2)   # entries 0..29
+    cache = oracle.build_cache(wl)
+    x, y = wl.tokens(0, 0, 60)
+    yf = W.bf16_bits_to_f32(y)
+    e = 29                                                          # group 3, r = 5
+    data, sc = oracle.quant_idx_entry((yf[2 * e] + yf[2 * e + 1]) * np.float32(0.5))
+    page = int(wl.page_table[0, 0]) * 4352
+    for k in range(64):
+        assert cache.idx_pool[page + 544 * 3 + 128 * (k // 16) + 16 * 5 + k % 16] == data[k]
+    for j in range(4):
+        assert cache.idx_pool[page + 544 * 3 + 512 + 4 * 5 + j] == sc[j]
