@@ -52,7 +52,16 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+constexpr int kOffStage = 4096;      // token offsets staged in shared memory
+
 __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
+  // request lookup table: tok_off staged once per block (one coalesced read
+  // instead of a chain of dependent global loads per token)
+  __shared__ int32_t s_off[kOffStage + 1];
+  const bool staged = a.num_requests + 1 <= kOffStage + 1;
+  if (staged)
+    for (int i = threadIdx.x; i <= a.num_requests; i += blockDim.x) s_off[i] = __ldg(a.tok_off + i);
+  __syncthreads();
   const int t = blockIdx.x * kWarps + warp_id();
   if (t >= a.total_tokens) return;
   const int lane = lane_id();
@@ -61,11 +70,12 @@ __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
   int lo = 0, hi = a.num_requests - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(a.tok_off + mid) <= t) lo = mid; else hi = mid - 1;
+    const int v = staged ? s_off[mid] : __ldg(a.tok_off + mid);
+    if (v <= t) lo = mid; else hi = mid - 1;
   }
   const int b = lo;
-  const int t0 = __ldg(a.tok_off + b);
-  const int T = __ldg(a.tok_off + b + 1) - t0;
+  const int t0 = staged ? s_off[b] : __ldg(a.tok_off + b);
+  const int T = (staged ? s_off[b + 1] : __ldg(a.tok_off + b + 1)) - t0;
   const int j = t - t0;
   if (j < 0 || j >= T) {
     if (lane == 0) raise_flag(a.status, CSA_FLAG_APPEND);

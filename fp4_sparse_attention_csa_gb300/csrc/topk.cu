@@ -8,15 +8,19 @@
 //   return every visible index, the rest of the row is -1).
 //
 // One thread-block cluster of C CTAs per row; CTA k owns a contiguous slice of
-// the row and stages its keys in shared memory.  Keys are the order-preserving
-// uint32 image of the fp32 scores (-0 folded onto +0).  Three radix passes
-// (11, 11 and 10 bits) find the exact 512th-largest key T: each CTA builds a
-// histogram of the keys that match the prefix so far (warp-aggregated shared
-// atomics), the cluster sums the C histograms through distributed shared
-// memory, and every CTA walks the summed histogram from the top.  A final
-// index-ordered ballot compaction writes every key > T and the lowest-index
-// keys == T until 512 are taken.  Cluster barriers are hardware barriers, so
-// there is no spin-wait here.
+// the row, staged in shared memory as order-preserving uint32 keys (-0 folded
+// onto +0).  The 512th-largest key T is found in two steps:
+//   1. a 4096-bin histogram in *value* space between the row's min and max
+//      (binning is monotone, so every key in a higher bin is larger); the
+//      cluster sums the C histograms through distributed shared memory and
+//      finds the bin holding rank 512;
+//   2. that bin's keys (usually a handful) are gathered into CTA 0, which runs
+//      a radix select over them for the exact key T.
+// If the bin holds more than kCandCap keys, or the value range is not finite,
+// a three-pass radix select over all keys (11/11/10 bits) is used instead.
+// A final index-ordered ballot compaction writes every key > T and the
+// lowest-index keys == T until 512 are taken.  Cluster barriers are hardware
+// barriers, so there is no spin-wait here.
 #include <cooperative_groups.h>
 
 #include "csa_device.cuh"
@@ -30,7 +34,8 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins = 2048;
+constexpr int kBins = 4096;
+constexpr int kCandCap = 4096;
 constexpr int kStageMax = 32768;   // keys staged per CTA (128 KB)
 constexpr int kMaxCluster = 8;
 
@@ -39,21 +44,86 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
-struct Pass {
-  int shift;      // bit position of this digit
-  int bits;       // digit width
+struct alignas(16) TopkSmem {
+  uint64_t stage_bar;
+  uint32_t hist[kBins];
+  uint32_t cand_key[kCandCap];
+  uint32_t cand_cnt;
+  uint32_t warp_a[kWarps], warp_b[kWarps];
+  float fmin, fmax;
+  uint32_t sel_bin, sel_need, sel_T, sel_take, sel_mode;
+  uint32_t cta_gt, cta_eq;
 };
-__constant__ Pass kPasses[3] = {{21, 11}, {10, 11}, {0, 10}};
+
+// Block-wide: find the bin holding the `need`-th largest among `nb` bins whose
+// counts come from `count(bin)`.  Writes bin and the rank left inside it.
+template <typename F>
+__device__ void find_bin(F count, int nb, uint32_t need, TopkSmem& sm, uint32_t* bin_out, uint32_t* need_out) {
+  const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
+  const int per = nb / kThreads;                        // bins per thread (nb multiple of 512)
+  uint32_t c[8];
+  uint32_t mine = 0;
+  for (int j = 0; j < per; ++j) {
+    c[j] = count(per * tid + j);
+    mine += c[j];
+  }
+  uint32_t incl = mine;                                  // suffix sums over higher threads
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  if (lane == 0) sm.warp_a[warp] = incl;
+  __syncthreads();
+  uint32_t acc = incl - mine;
+  for (int w2 = warp + 1; w2 < kWarps; ++w2) acc += sm.warp_a[w2];
+  for (int j = per - 1; j >= 0; --j) {
+    if (acc < need && acc + c[j] >= need) {
+      *bin_out = (uint32_t)(per * tid + j);
+      *need_out = need - acc;
+    }
+    acc += c[j];
+  }
+  __syncthreads();
+}
+
+// Radix select over `m` keys in shared memory (one CTA): the need-th largest
+// key T and how many keys are strictly larger.
+__device__ void radix_select_block(const uint32_t* keys, int m, uint32_t need, TopkSmem& sm, uint32_t* T_out,
+                                   uint32_t* gt_out) {
+  uint32_t prefix = 0, mask = 0;
+  uint32_t rem = need;
+  const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+  for (int p = 0; p < 3; ++p) {
+    const int sh = shifts[p], nbv = 1 << widths[p];
+    for (int i = threadIdx.x; i < kBins; i += kThreads) sm.hist[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < m; i += kThreads) {
+      const uint32_t k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> sh) & (uint32_t)(nbv - 1)], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) sm.sel_bin = 0xFFFFFFFFu;
+    __syncthreads();
+    find_bin([&](int b) { return b < nbv ? sm.hist[b] : 0u; }, 2048, rem, sm, &sm.sel_bin, &sm.sel_need);
+    prefix |= sm.sel_bin << sh;
+    mask |= (uint32_t)(nbv - 1) << sh;
+    rem = sm.sel_need;
+    __syncthreads();
+  }
+  *T_out = prefix;
+  *gt_out = need - rem;
+}
 
 __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int slice_cap, int staged) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) uint8_t smem[];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);                 // [kBins]
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kBins * 4);     // [slice_cap] when staged
-  __shared__ uint32_t s_warp[kWarps][2];
-  __shared__ uint32_t s_cta_counts[2];      // this CTA's (gt, eq) for the final pass
-  __shared__ uint32_t s_sel[4];             // prefix, remaining, threshold state
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + sizeof(TopkSmem));  // [slice_cap] when staged
 
   const int r = blockIdx.y;
   const int k = (int)cluster.block_rank();
@@ -71,78 +141,178 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int sli
       for (int i = tid; i < TOPK; i += kThreads) out[i] = i < n ? i : -1;
     return;                        // uniform across the cluster: no cluster barrier below is reached
   }
-  const int per = (n + C - 1) / C;
+  const int per = (((n + C - 1) / C) + 3) & ~3;        // slices start on 16-byte boundaries
   const int lo = min(n, k * per), hi = min(n, lo + per);
   const int len = hi - lo;
+
+  // ---- stage the slice (one bulk copy of its 16-byte part, plain loads for the
+  // tail), then convert to keys and take the local value range --------------------------
+  float vmin = INFINITY, vmax = -INFINITY;
   if (staged) {
-    for (int i = tid; i < len; i += kThreads) keys[i] = score_key(__ldg(row + lo + i));
+    const int body = len & ~3;
+    if (tid == 0) {
+      mbar_init(&sm.stage_bar, 1);
+      fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      mbar_expect_tx(&sm.stage_bar, (uint32_t)body * 4u);
+      if (body > 0) bulk_load(keys, row + lo, (uint32_t)body * 4u, &sm.stage_bar);
+    }
+    if (tid < len - body) keys[body + tid] = __float_as_uint(__ldg(row + lo + body + tid));
+    if (!mbar_wait(&sm.stage_bar, 0)) {
+      if (tid == 0) raise_flag(a.status, CSA_FLAG_TIMEOUT);
+    }
+    __syncthreads();
+    for (int i = tid; i < len; i += kThreads) {
+      float v = __uint_as_float(keys[i]);
+      if (v == 0.0f) v = 0.0f;                          // fold -0 onto +0
+      vmin = fminf(vmin, v);
+      vmax = fmaxf(vmax, v);
+      keys[i] = score_key(v);
+    }
+  } else {
+    for (int i0 = tid * 4; i0 < len; i0 += kThreads * 4) {
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = (i0 + j < len) ? __ldg(row + lo + i0 + j) : NAN;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (i0 + j < len) {
+          vmin = fminf(vmin, v[j]);
+          vmax = fmaxf(vmax, v[j]);
+        }
+      }
+    }
   }
   auto key_at = [&](int i) -> uint32_t { return staged ? keys[i] : score_key(__ldg(row + lo + i)); };
-
-  uint32_t prefix = 0, prefix_mask = 0;
-  int remaining = TOPK;            // how many still to take at or below the prefix
-  for (int p = 0; p < 3; ++p) {
-    const int shift = kPasses[p].shift, bits = kPasses[p].bits, nb = 1 << bits;
-    for (int i = tid; i < kBins; i += kThreads) hist[i] = 0u;
-    __syncthreads();
-    for (int base = 0; base < len; base += kThreads) {
-      const int i = base + tid;
-      bool take = false;
-      uint32_t bin = 0;
-      if (i < len) {
-        const uint32_t key = key_at(i);
-        take = (key & prefix_mask) == prefix;
-        bin = (key >> shift) & (uint32_t)(nb - 1);
-      }
-      const uint32_t active = __ballot_sync(0xFFFFFFFFu, take);
-      if (take) {
-        const uint32_t peers = __match_any_sync(active, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-      }
-    }
-    cluster.sync();                // every CTA's histogram is complete
-    // Sum the cluster's histograms and find the bin holding the remaining-th
-    // largest key: thread t owns bins [4t, 4t+4) (nb <= 2048 = 4 * 512).
-    uint32_t c4[4] = {0u, 0u, 0u, 0u};
-    for (int j = 0; j < 4; ++j) {
-      const int bin = 4 * tid + j;
-      if (bin < nb) {
-        for (int q = 0; q < C; ++q) c4[j] += *cluster.map_shared_rank(hist + bin, q);
-      }
-    }
-    // exclusive count of keys in bins above this thread's bins
-    uint32_t mine = c4[0] + c4[1] + c4[2] + c4[3];
-    uint32_t incl = mine;          // suffix sum over threads > tid, via reversed scan
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
-      if (lane + o < 32) incl += y;
-    }
-    if (lane == 0) s_warp[warp][0] = incl;
-    __syncthreads();
-    uint32_t above = incl - mine;  // later lanes of this warp
-    for (int w2 = warp + 1; w2 < kWarps; ++w2) above += s_warp[w2][0];
-    // bins 4t+3 .. 4t from the top
-    uint32_t acc = above;
-    for (int j = 3; j >= 0; --j) {
-      const int bin = 4 * tid + j;
-      if (bin < nb && acc < (uint32_t)remaining && acc + c4[j] >= (uint32_t)remaining) {
-        s_sel[0] = (uint32_t)bin;
-        s_sel[1] = (uint32_t)remaining - acc;
-      }
-      acc += c4[j];
-    }
-    cluster.sync();                // all remote reads of this pass are done
-    const uint32_t bin = s_sel[0];
-    remaining = (int)s_sel[1];
-    prefix |= bin << shift;
-    prefix_mask |= (uint32_t)(nb - 1) << shift;
-    __syncthreads();
+  for (int o = 16; o > 0; o >>= 1) {
+    vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
+    vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, o));
   }
-  const uint32_t T = prefix;       // exact 512th-largest key; take `remaining` of the equal keys
+  if (lane == 0) {
+    sm.warp_a[warp] = __float_as_uint(vmin);
+    sm.warp_b[warp] = __float_as_uint(vmax);
+  }
+  for (int i = tid; i < kBins; i += kThreads) sm.hist[i] = 0u;
+  if (tid == 0) sm.cand_cnt = 0u;
+  __syncthreads();
+  if (tid == 0) {
+    float a0 = INFINITY, b0 = -INFINITY;
+    for (int w2 = 0; w2 < kWarps; ++w2) {
+      a0 = fminf(a0, __uint_as_float(sm.warp_a[w2]));
+      b0 = fmaxf(b0, __uint_as_float(sm.warp_b[w2]));
+    }
+    sm.fmin = a0;
+    sm.fmax = b0;
+  }
+  cluster.sync();
+  float smin = INFINITY, smax = -INFINITY;
+  for (int q = 0; q < C; ++q) {
+    const TopkSmem* rs = cluster.map_shared_rank(&sm, q);
+    smin = fminf(smin, rs->fmin);
+    smax = fmaxf(smax, rs->fmax);
+  }
+  const float range = smax - smin;
+  const bool binning = isfinite(range) && range > 0.0f;
+  const float scale = binning ? (float)kBins / range : 0.0f;
+  auto bin_of = [&](uint32_t key) -> uint32_t {
+    const float v = key_value(key);
+    const float f = (v - smin) * scale;
+    const int b = (int)f;
+    return (uint32_t)(b < 0 ? 0 : (b >= kBins ? kBins - 1 : b));
+  };
 
-  // ---- index-ordered compaction.  Warp w owns the contiguous chunk
-  // [w*cw, (w+1)*cw) of this CTA's slice.
+  uint32_t T = 0, take_eq = 0;
+  int mode = 0;                    // 0: value bins, 1: all keys equal, 2: radix fallback
+  if (!binning) mode = (range == 0.0f) ? 1 : 2;
+  if (mode == 1) {
+    T = score_key(smin);
+    take_eq = TOPK;
+  } else if (mode == 0) {
+    // ---- 4096-bin histogram in value space ------------------------------------------
+    for (int i = tid; i < len; i += kThreads) atomicAdd(&sm.hist[bin_of(key_at(i))], 1u);
+    cluster.sync();
+    find_bin(
+        [&](int b) {
+          uint32_t s = 0;
+          for (int q = 0; q < C; ++q) s += *cluster.map_shared_rank(&sm.hist[b], q);
+          return s;
+        },
+        kBins, TOPK, sm, &sm.sel_bin, &sm.sel_need);
+    const uint32_t tb = sm.sel_bin, need = sm.sel_need;
+    uint32_t in_bin = 0, before = 0;
+    for (int q = 0; q < C; ++q) {
+      const uint32_t c = *cluster.map_shared_rank(&sm.hist[tb], q);
+      in_bin += c;
+      if (q < k) before += c;
+    }
+    if (in_bin > (uint32_t)kCandCap) {
+      mode = 2;
+    } else {
+      // ---- gather the threshold bin's keys into CTA 0, select there -------------------
+      uint32_t* cand0 = cluster.map_shared_rank(sm.cand_key, 0);
+      for (int i0 = 0; i0 < len; i0 += kThreads) {
+        const int i = i0 + tid;
+        bool hit = false;
+        uint32_t key = 0;
+        if (i < len) {
+          key = key_at(i);
+          hit = bin_of(key) == tb;
+        }
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, hit);
+        uint32_t base = 0;
+        if (lane == 0 && bal) base = atomicAdd(&sm.cand_cnt, (uint32_t)__popc(bal));
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+        if (hit) cand0[before + base + __popc(bal & ((1u << lane) - 1u))] = key;
+      }
+      cluster.sync();
+      if (k == 0) {
+        uint32_t Tc, gt;
+        radix_select_block(sm.cand_key, (int)in_bin, need, sm, &Tc, &gt);
+        if (tid == 0) {
+          sm.sel_T = Tc;
+          sm.sel_take = need - gt;
+        }
+      }
+      cluster.sync();
+      const TopkSmem* s0 = cluster.map_shared_rank(&sm, 0);
+      T = s0->sel_T;
+      take_eq = s0->sel_take;
+    }
+  }
+  if (mode == 2) {
+    // ---- fallback: three radix passes over every key ----------------------------------
+    uint32_t prefix = 0, mask = 0, rem = TOPK;
+    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+    for (int p = 0; p < 3; ++p) {
+      const int sh = shifts[p], nbv = 1 << widths[p];
+      cluster.sync();              // everyone is done reading the previous histograms
+      for (int i = tid; i < kBins; i += kThreads) sm.hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < len; i += kThreads) {
+        const uint32_t key = key_at(i);
+        if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> sh) & (uint32_t)(nbv - 1)], 1u);
+      }
+      cluster.sync();
+      find_bin(
+          [&](int b) {
+            uint32_t s = 0;
+            if (b < nbv)
+              for (int q = 0; q < C; ++q) s += *cluster.map_shared_rank(&sm.hist[b], q);
+            return s;
+          },
+          2048, rem, sm, &sm.sel_bin, &sm.sel_need);
+      prefix |= sm.sel_bin << sh;
+      mask |= (uint32_t)(nbv - 1) << sh;
+      rem = sm.sel_need;
+    }
+    T = prefix;
+    take_eq = rem;
+  }
+
+  // ---- index-ordered compaction.  Warp w owns [w*cw, (w+1)*cw) of the slice.
   const int cw = (len + kWarps - 1) / kWarps;
   const int w0 = min(len, warp * cw), w1 = min(len, w0 + cw);
   uint32_t gt = 0, eq = 0;
@@ -154,30 +324,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int sli
     eq += __popc(__ballot_sync(0xFFFFFFFFu, i < w1 && key == T));
   }
   if (lane == 0) {
-    s_warp[warp][0] = gt;
-    s_warp[warp][1] = eq;
+    sm.warp_a[warp] = gt;
+    sm.warp_b[warp] = eq;
   }
   __syncthreads();
-  uint32_t gt_before = 0, eq_before = 0;
   if (tid == 0) {
     uint32_t g = 0, e = 0;
     for (int w2 = 0; w2 < kWarps; ++w2) {
-      g += s_warp[w2][0];
-      e += s_warp[w2][1];
+      g += sm.warp_a[w2];
+      e += sm.warp_b[w2];
     }
-    s_cta_counts[0] = g;
-    s_cta_counts[1] = e;
+    sm.cta_gt = g;
+    sm.cta_eq = e;
   }
   cluster.sync();
+  uint32_t gt_before = 0, eq_before = 0;
   for (int q = 0; q < k; ++q) {
-    gt_before += *cluster.map_shared_rank(&s_cta_counts[0], q);
-    eq_before += *cluster.map_shared_rank(&s_cta_counts[1], q);
+    const TopkSmem* rs = cluster.map_shared_rank(&sm, q);
+    gt_before += rs->cta_gt;
+    eq_before += rs->cta_eq;
   }
   for (int w2 = 0; w2 < warp; ++w2) {
-    gt_before += s_warp[w2][0];
-    eq_before += s_warp[w2][1];
+    gt_before += sm.warp_a[w2];
+    eq_before += sm.warp_b[w2];
   }
-  const uint32_t take_eq = (uint32_t)remaining;
   uint32_t sel_before = gt_before + min(eq_before, take_eq);
   uint32_t eq_rank = eq_before;
   for (int i0 = w0; i0 < w1; i0 += 32) {
@@ -199,18 +369,359 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int sli
   cluster.sync();                  // keep shared memory alive for remote readers
 }
 
+// ---------------------------------------------------------------------------
+// One CTA per row (rows up to kRowMax entries): the row is streamed from L2
+// with 16-byte loads -- value range, a kRowBins-bin value histogram, then every
+// entry at or above the threshold bin is compacted, in index order, into a
+// candidate list in shared memory, where the exact 512th key and the output
+// are resolved.  Shared memory stays small, so several rows run per SM.
+constexpr int kRowMax = 65536;
+constexpr int kRowBins = 2048;
+constexpr int kRowCap = 4096;
+
+struct alignas(16) RowSmem {
+  uint32_t hist[kBins];            // kRowBins used by the value pass; radix passes use 2048
+  uint32_t cand_key[kRowCap];
+  int32_t cand_idx[kRowCap];
+  uint32_t warp_a[kWarps], warp_b[kWarps];
+  uint32_t cnt, sel_bin, sel_need, T, take, fallback;
+  float fmin, fmax;
+};
+
+__device__ __forceinline__ void block_minmax(float& vmin, float& vmax, RowSmem& sm) {
+  const int lane = lane_id(), warp = warp_id();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
+    vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, o));
+  }
+  if (lane == 0) {
+    sm.warp_a[warp] = __float_as_uint(vmin);
+    sm.warp_b[warp] = __float_as_uint(vmax);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a0 = INFINITY, b0 = -INFINITY;
+    for (int w2 = 0; w2 < kWarps; ++w2) {
+      a0 = fminf(a0, __uint_as_float(sm.warp_a[w2]));
+      b0 = fmaxf(b0, __uint_as_float(sm.warp_b[w2]));
+    }
+    sm.fmin = a0;
+    sm.fmax = b0;
+  }
+  __syncthreads();
+  vmin = sm.fmin;
+  vmax = sm.fmax;
+}
+
+// Block-wide exclusive scan of one count per thread; returns the thread's
+// offset and the block total (uses warp_a).
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, RowSmem& sm) {
+  const int lane = lane_id(), warp = warp_id();
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm.warp_a[warp] = x;
+  __syncthreads();
+  uint32_t off = 0, tot = 0;
+  for (int w2 = 0; w2 < kWarps; ++w2) {
+    const uint32_t c = sm.warp_a[w2];
+    if (w2 < warp) off += c;
+    tot += c;
+  }
+  __syncthreads();
+  *total = tot;
+  return off + x - v;
+}
+
+__global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const float* row = a.scores + (size_t)r * a.ld;
+  int32_t* out = a.out + (size_t)r * TOPK;
+
+  int n = a.n_valid ? __ldg(a.n_valid + r) : (__ldg(a.row_pos + r) + 1) / a.P;
+  if (n < 0 || n > a.max_n) {
+    if (tid == 0) raise_flag(a.status, CSA_FLAG_ROW_INVALID);
+    n = n < 0 ? 0 : a.max_n;
+  }
+  if (n <= TOPK) {
+    for (int i = tid; i < TOPK; i += kThreads) out[i] = i < n ? i : -1;
+    return;
+  }
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  const int n4 = n >> 2;
+  auto fold = [](float v) { return v == 0.0f ? 0.0f : v; };   // -0 onto +0
+
+  // ---- pass 1: value range (four 16-byte loads in flight per thread) ---------------
+  float vmin = INFINITY, vmax = -INFINITY;
+  for (int b0 = tid; b0 < n4; b0 += 4 * kThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = b0 + j * kThreads;
+      v[j] = i < n4 ? __ldg(row4 + i) : make_float4(vmax, vmax, vmax, vmax);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (b0 + j * kThreads < n4) {
+        vmin = fminf(vmin, fminf(fminf(v[j].x, v[j].y), fminf(v[j].z, v[j].w)));
+        vmax = fmaxf(vmax, fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w)));
+      }
+    }
+  }
+  for (int i = 4 * n4 + tid; i < n; i += kThreads) {
+    const float v = __ldg(row + i);
+    vmin = fminf(vmin, v);
+    vmax = fmaxf(vmax, v);
+  }
+  for (int i = tid; i < kRowBins; i += kThreads) sm.hist[i] = 0u;
+  block_minmax(vmin, vmax, sm);
+  vmin = fold(vmin);
+  vmax = fold(vmax);
+  const float range = vmax - vmin;
+  if (range == 0.0f) {             // all equal: the lowest 512 indices
+    for (int i = tid; i < TOPK; i += kThreads) out[i] = i;
+    return;
+  }
+  const bool binning = isfinite(range) && isfinite((float)kRowBins / range);
+  const float scale = binning ? (float)kRowBins / range : 0.0f;
+  auto bin_of = [&](float v) -> int {
+    const int b = (int)((fold(v) - vmin) * scale);
+    return b < 0 ? 0 : (b >= kRowBins ? kRowBins - 1 : b);
+  };
+
+  uint32_t T = 0, take = 0;
+  bool done = false;
+  if (binning) {
+    // ---- pass 2: histogram --------------------------------------------------------
+    for (int b0 = tid; b0 < n4; b0 += 4 * kThreads) {
+      float4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = b0 + j * kThreads;
+        v[j] = i < n4 ? __ldg(row4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (b0 + j * kThreads < n4) {
+          atomicAdd(&sm.hist[bin_of(v[j].x)], 1u);
+          atomicAdd(&sm.hist[bin_of(v[j].y)], 1u);
+          atomicAdd(&sm.hist[bin_of(v[j].z)], 1u);
+          atomicAdd(&sm.hist[bin_of(v[j].w)], 1u);
+        }
+      }
+    }
+    for (int i = 4 * n4 + tid; i < n; i += kThreads) atomicAdd(&sm.hist[bin_of(__ldg(row + i))], 1u);
+    __syncthreads();
+    // find the bin of rank 512 (uses the cluster kernel's helper on a one-CTA view)
+    {
+      const int lane = lane_id(), warp = warp_id();
+      constexpr int per = kRowBins / kThreads;
+      uint32_t c[per], mine = 0;
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        c[j] = sm.hist[per * tid + j];
+        mine += c[j];
+      }
+      uint32_t incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      if (lane == 0) sm.warp_a[warp] = incl;
+      __syncthreads();
+      uint32_t acc = incl - mine;
+      for (int w2 = warp + 1; w2 < kWarps; ++w2) acc += sm.warp_a[w2];
+#pragma unroll
+      for (int j = per - 1; j >= 0; --j) {
+        if (acc < (uint32_t)TOPK && acc + c[j] >= (uint32_t)TOPK) sm.sel_bin = (uint32_t)(per * tid + j);
+        acc += c[j];
+      }
+      __syncthreads();
+    }
+    const int tb = (int)sm.sel_bin;
+    uint32_t above = 0;            // entries in bins >= tb: the candidate list
+    for (int b = tid; b < kRowBins; b += kThreads) above += (b >= tb) ? sm.hist[b] : 0u;
+    uint32_t m_total;
+    (void)block_scan(above, &m_total, sm);
+    if (m_total <= (uint32_t)kRowCap) {
+      // ---- pass 3: compact entries with bin >= tb, in index order; each thread
+      // takes a run of 16 consecutive entries per chunk -------------------------------
+      uint32_t base = 0;
+      for (int c0 = 0; c0 < n; c0 += 16 * kThreads) {
+        const int i0 = c0 + 16 * tid;
+        float v[16];
+        if (i0 + 15 < n) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 x = __ldg(row4 + (i0 >> 2) + q);
+            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = i0 + j < n ? __ldg(row + i0 + j) : vmin;
+        }
+        uint32_t bits = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (i0 + j < n && bin_of(v[j]) >= tb) bits |= 1u << j;
+        uint32_t tot;
+        uint32_t off = base + block_scan((uint32_t)__popc(bits), &tot, sm);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (bits & (1u << j)) {
+            sm.cand_key[off] = score_key(fold(v[j]));
+            sm.cand_idx[off] = i0 + j;
+            ++off;
+          }
+        }
+        base += tot;
+      }
+      __syncthreads();
+      // ---- exact 512th key among the candidates ----------------------------------
+      const int m = (int)m_total;
+      {
+        uint32_t prefix = 0, mask = 0, rem = TOPK;
+        const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+        for (int p = 0; p < 3; ++p) {
+          const int sh = shifts[p], nbv = 1 << widths[p];
+          for (int i = tid; i < 2048; i += kThreads) sm.hist[i] = 0u;
+          __syncthreads();
+          for (int i = tid; i < m; i += kThreads) {
+            const uint32_t kk = sm.cand_key[i];
+            if ((kk & mask) == prefix) atomicAdd(&sm.hist[(kk >> sh) & (uint32_t)(nbv - 1)], 1u);
+          }
+          __syncthreads();
+          const int lane = lane_id(), warp = warp_id();
+          constexpr int per = 2048 / kThreads;
+          uint32_t c[per], mine = 0;
+#pragma unroll
+          for (int j = 0; j < per; ++j) {
+            const int b = per * tid + j;
+            c[j] = b < nbv ? sm.hist[b] : 0u;
+            mine += c[j];
+          }
+          uint32_t incl = mine;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+            if (lane + o < 32) incl += y;
+          }
+          if (lane == 0) sm.warp_a[warp] = incl;
+          __syncthreads();
+          uint32_t acc = incl - mine;
+          for (int w2 = warp + 1; w2 < kWarps; ++w2) acc += sm.warp_a[w2];
+#pragma unroll
+          for (int j = per - 1; j >= 0; --j) {
+            if (acc < rem && acc + c[j] >= rem) {
+              sm.sel_bin = (uint32_t)(per * tid + j);
+              sm.sel_need = rem - acc;
+            }
+            acc += c[j];
+          }
+          __syncthreads();
+          prefix |= sm.sel_bin << sh;
+          mask |= (uint32_t)(nbv - 1) << sh;
+          rem = sm.sel_need;
+          __syncthreads();
+        }
+        T = prefix;
+        take = rem;
+      }
+      // ---- output: candidates are in index order ----------------------------------
+      uint32_t eq_base = 0, sel_base = 0;
+      for (int c0 = 0; c0 < m; c0 += kThreads) {
+        const int i = c0 + tid;
+        const uint32_t kk = i < m ? sm.cand_key[i] : 0u;
+        const uint32_t is_eq = (i < m && kk == T) ? 1u : 0u;
+        uint32_t tot_eq;
+        const uint32_t eq_rank = eq_base + block_scan(is_eq, &tot_eq, sm);
+        const uint32_t sel = (i < m && (kk > T || (is_eq && eq_rank < take))) ? 1u : 0u;
+        uint32_t tot_sel;
+        const uint32_t pos = sel_base + block_scan(sel, &tot_sel, sm);
+        if (sel && pos < (uint32_t)TOPK) out[pos] = sm.cand_idx[i];
+        eq_base += tot_eq;
+        sel_base += tot_sel;
+      }
+      done = true;
+    }
+  }
+  if (!done) {
+    // ---- fallback: radix select over the whole row, then an ordered pass ----------
+    uint32_t prefix = 0, mask = 0, rem = TOPK;
+    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+    for (int p = 0; p < 3; ++p) {
+      const int sh = shifts[p], nbv = 1 << widths[p];
+      for (int i = tid; i < 2048; i += kThreads) sm.hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < n; i += kThreads) {
+        const uint32_t kk = score_key(__ldg(row + i));
+        if ((kk & mask) == prefix) atomicAdd(&sm.hist[(kk >> sh) & (uint32_t)(nbv - 1)], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t acc = 0;
+        for (int b = nbv - 1; b >= 0; --b) {
+          const uint32_t c = sm.hist[b];
+          if (acc < rem && acc + c >= rem) {
+            sm.sel_bin = (uint32_t)b;
+            sm.sel_need = rem - acc;
+            break;
+          }
+          acc += c;
+        }
+      }
+      __syncthreads();
+      prefix |= sm.sel_bin << sh;
+      mask |= (uint32_t)(nbv - 1) << sh;
+      rem = sm.sel_need;
+      __syncthreads();
+    }
+    T = prefix;
+    take = rem;
+    uint32_t eq_base = 0, sel_base = 0;
+    for (int c0 = 0; c0 < n; c0 += kThreads) {
+      const int i = c0 + tid;
+      const uint32_t kk = i < n ? score_key(__ldg(row + i)) : 0u;
+      const uint32_t is_eq = (i < n && kk == T) ? 1u : 0u;
+      uint32_t tot_eq;
+      const uint32_t eq_rank = eq_base + block_scan(is_eq, &tot_eq, sm);
+      const uint32_t sel = (i < n && (kk > T || (is_eq && eq_rank < take))) ? 1u : 0u;
+      uint32_t tot_sel;
+      const uint32_t pos = sel_base + block_scan(sel, &tot_sel, sm);
+      if (sel && pos < (uint32_t)TOPK) out[pos] = i;
+      eq_base += tot_eq;
+      sel_base += tot_sel;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;
+  if (a.max_n <= kRowMax && (a.ld % 4) == 0 && ((uintptr_t)a.scores & 15u) == 0) {
+    const size_t smem = sizeof(RowSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_topk_row, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_topk_row<<<a.num_rows, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+  }
   int C = (a.max_n + kStageMax - 1) / kStageMax;
   C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
-  // smaller rows: split into up to 8 CTAs of >= 4096 keys for parallelism
-  while (C < kMaxCluster && (a.max_n + C - 1) / C > 8192 && (long long)a.num_rows * C < 296) C *= 2;
-  if (C > kMaxCluster) C = kMaxCluster;
-  const int slice_cap = (a.max_n + C - 1) / C;
+  // few rows: spread each row over more CTAs
+  while (2 * C <= kMaxCluster && (a.max_n + 2 * C - 1) / (2 * C) >= 4096 && (long long)a.num_rows * C * 2 <= 300)
+    C *= 2;
+  const int slice_cap = (((a.max_n + C - 1) / C) + 3) & ~3;   // matches the kernel's 16-byte slices
   const int staged = slice_cap <= kStageMax;
-  const size_t smem = kBins * 4 + (staged ? (size_t)slice_cap * 4 : 0);
+  const size_t smem = sizeof(TopkSmem) + (staged ? (size_t)slice_cap * 4 : 0);
   cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

@@ -151,6 +151,25 @@ def test_topk_exact_with_ties(n):
         assert np.array_equal(got[r], oracle.topk_row(sc[r], n)), r
 
 
+@pytest.mark.parametrize("n", [20000, 65536])
+def test_topk_candidate_overflow(n):
+    """More than 4096 entries tie at the 512th value: the per-row kernel's
+    candidate list overflows and the whole-row radix path decides."""
+    g = np.random.default_rng(n + 1)
+    R, ld = 2, n
+    sc = g.standard_normal((R, ld)).astype(np.float32)
+    sc[0, ::3] = 1.5                                 # a third of the row ties
+    sc[0, 7] = 9.0
+    sc[1, :] = np.float32(2.0) ** -140               # subnormal spread
+    sc[1, ::5] = np.float32(3.0) * np.float32(2.0) ** -140
+    nv = np.array([n, n], np.int32)
+    out = torch.empty((R, 512), dtype=torch.int32, device="cuda")
+    csa.csa_topk(R, torch.from_numpy(sc).cuda(), ld, torch.from_numpy(nv).cuda(), n, 512, out)
+    got = out.cpu().numpy()
+    for r in range(R):
+        assert np.array_equal(got[r], oracle.topk_row(sc[r], n)), r
+
+
 def test_topk_rows_of_different_lengths():
     g = np.random.default_rng(5)
     R, ld = 9, 40000
