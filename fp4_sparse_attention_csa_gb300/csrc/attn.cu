@@ -24,6 +24,12 @@
 // O^T accumulators live in TMEM and are rescaled when a head's max grows.
 // With several CTAs per row, partial (O, m, l) go to the workspace and a merge
 // kernel combines them by log-sum-exp.
+//
+// Latency: every selected entry's page is resolved once, up front, by all
+// threads together; the raw FP4/FP8 bytes of tile t+1 are loaded into
+// registers while tile t is dequantised and multiplied, so the HBM gather of
+// one tile overlaps the tensor-core and softmax work of the previous one.
+// Dequantisation uses the packed e2m1x2 / e4m3x2 -> f16x2 conversions.
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
@@ -31,9 +37,10 @@ namespace csa {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kTileKeys = 128;
-constexpr int kMaxTiles = TOPK / kTileKeys + 1;   // 4 global + 1 window
+constexpr int kMainTiles = TOPK / kTileKeys;      // 4
+constexpr int kMaxTiles = kMainTiles + 1;         // 4 global + 1 window
 constexpr int kMaxH = CSA_MAX_HEADS;             // 64
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -41,8 +48,8 @@ struct AttnSmem {
   uint8_t k[kTileKeys * D * 2];        // 131072, 1024-aligned: kc*16384 + (key/8)*1024 + (key%8)*128
   uint8_t q[kMaxH * D * 2];            // 65536: kc*(H*128) + (h/8)*1024 + (h%8)*128
   uint8_t p[kTileKeys * 128];          // 16384: (key/8)*1024 + (key%8)*128, heads along the row
-  __half2 e2m1_pair[256];              // byte -> (lo nibble, hi nibble) values
-  float e4m3_tab[256];
+  int32_t ent_pg[TOPK];                // page of each selected entry, -1 when none
+  uint8_t ent_slot[TOPK];
   float mu[kTileKeys];
   float red[4][kMaxH];                 // per-quarter partial max / sum
   float m_run[kMaxH], l_run[kMaxH], alpha[kMaxH];
@@ -55,9 +62,41 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// In-warp reduction of NV values per lane (NV = 8, 16 or 32) across the 32
+// Four FP4 pairs (the bytes of w, low byte first) -> four f16x2; in each the
+// low nibble (even dimension) lands in the low half.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
+// Two E4M3 pairs (the 16-bit halves of w) -> two f16x2, low byte -> low half.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t (&o)[2]) {
+  asm("{\n\t.reg .b16 h0, h1;\n\t"
+      "mov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+      : "=r"(o[0]), "=r"(o[1])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, __half2 s) {
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&x), s);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// In-warp reduction of NV values per lane (NV = 4, 8, 16 or 32) across the 32
 // lanes: recursive halving, then a butterfly over the remaining lane bits.
 // Lane l ends with the reduction of value index (l >> (5 - log2 NV)).
+template <int NV>
+struct RedShift {
+  static constexpr int v = NV == 32 ? 0 : (NV == 16 ? 1 : (NV == 8 ? 2 : 3));
+};
 template <int NV, bool kMax>
 __device__ __forceinline__ float warp_reduce_many(float (&v)[NV], int lane) {
   int cnt = NV;
@@ -77,8 +116,7 @@ __device__ __forceinline__ float warp_reduce_many(float (&v)[NV], int lane) {
     cnt = half;
   }
   float x = v[0];
-  // lanes that share the value index: reduce over the low lane bits
-  constexpr int kShift = (NV == 32) ? 0 : (NV == 16 ? 1 : 2);
+  constexpr int kShift = RedShift<NV>::v;
 #pragma unroll
   for (int o = 1; o < (1 << kShift); o <<= 1) {
     const float y = __shfl_xor_sync(0xFFFFFFFFu, x, o);
@@ -87,9 +125,44 @@ __device__ __forceinline__ float warp_reduce_many(float (&v)[NV], int lane) {
   return x;
 }
 
+// Raw bytes of one key's quarter (128 dims) of a tile, in registers.
+struct Raw {
+  uint4 d[8];      // main entry: d[0..3] = 64 FP4 bytes; window: 128 E4M3 codes
+  uint2 sc;        // main entry: the 8 E4M3 block scales of these 128 dims
+  float ws;        // window token: fp32 scale
+  int valid;
+};
+
+__device__ __forceinline__ void gather(const AttnArgs& a, const AttnSmem& sm, int r, int b, int pos,
+                                       int t, bool is_win, int key, int part, Raw& g) {
+  if (!is_win) {
+    const int j = t * kTileKeys + key;
+    const int pg = sm.ent_pg[j];
+    g.valid = pg >= 0;
+    if (pg >= 0) {
+      const uint8_t* src = a.kv_pool + (size_t)pg * KV_PAGE;
+      const int slot = sm.ent_slot[j];
+      const uint4* dp = reinterpret_cast<const uint4*>(src + slot * 256 + 64 * part);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) g.d[i] = __ldg(dp + i);
+      g.sc = __ldg(reinterpret_cast<const uint2*>(src + KV_SCALE_OFF + slot * 32 + 8 * part));
+    }
+  } else {
+    const int p = max(0, pos - (WIN - 1)) + key;
+    g.valid = p <= pos;
+    if (p <= pos) {
+      const size_t slot = (size_t)b * a.win_cap + (size_t)(p % a.win_cap);
+      const uint4* dp = reinterpret_cast<const uint4*>(a.win_codes + slot * D + 128 * part);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g.d[i] = __ldg(dp + i);
+      g.ws = __ldg(a.win_scale + slot);
+    }
+  }
+}
+
 template <int H>
 __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
-  constexpr int HH = H / 2;                       // heads per thread in the softmax
+  constexpr int HH = H / 4;                       // heads per thread in the softmax
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
@@ -107,11 +180,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const int tper = (ntiles + a.splits - 1) / a.splits;
   const int t_beg = min(ntiles, split * tper), t_end = min(ntiles, t_beg + tper);
 
-  // ---- setup: tables, barriers, TMEM, Q (bf16 -> fp16, K-major 128B swizzle)
+  // ---- setup: entry pages, barriers, TMEM, Q (bf16 -> fp16, K-major 128B swizzle)
   {
-    const uint32_t lo = tid & 15, hi = tid >> 4;
-    sm.e2m1_pair[tid] = __floats2half2_rn(e2m1_value(lo), e2m1_value(hi));
-    sm.e4m3_tab[tid] = e4m3_value((uint32_t)tid);
+    const int j = tid;                            // TOPK == kThreads
+    int pg = -1, slot = 0;
+    if (j < nsel && j >= t_beg * kTileKeys && j < min(t_end, gtiles) * kTileKeys) {
+      const int e = __ldg(a.topk + (size_t)r * TOPK + j);
+      if (e >= 0) {
+        if (e >= n || e / PAGE >= a.max_pages) {
+          raise_flag(a.status, CSA_FLAG_TOPK_OOB);
+        } else {
+          const int p = __ldg(a.page_table + (size_t)b * a.max_pages + e / PAGE);
+          if (p < 0 || p >= a.num_pages) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
+          else { pg = p; slot = e % PAGE; }
+        }
+      }
+    }
+    sm.ent_pg[j] = pg;
+    sm.ent_slot[j] = (uint8_t)slot;
   }
   if (tid < H) {
     sm.m_run[tid] = -INFINITY;
@@ -147,63 +233,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const uint32_t tS = tmem, tO = tmem + 64;      // S^T: H cols; O^T chunk c at 64 + 64c
   const float scale_log2 = a.softmax_scale * kLog2e;
 
-  const int key = tid & (kTileKeys - 1), khalf = tid >> 7;   // gather role
-  const int q4 = warp & 3, hsel = warp >> 2;                  // TMEM role: lane quarter, head half
+  const int key = tid & (kTileKeys - 1), part = tid >> 7;    // gather role: dims 128*part..+128
+  const int q4 = warp & 3, hsel = warp >> 2;                  // TMEM role: lane quarter, head quarter
   const int mykey = 32 * q4 + lane;
   bool ok = true;
 
+  Raw cur, nxt;
+  cur.valid = 0;
+  if (t_beg < t_end) gather(a, sm, r, b, pos, t_beg, has_win && t_beg == ntiles - 1, key, part, cur);
+
   for (int t = t_beg; t < t_end && ok; ++t) {
     const int it = t - t_beg;
-    if (it > 0 && !mbar_wait(&sm.pv_bar, (it - 1) & 1)) { raise_flag(a.status, CSA_FLAG_TIMEOUT); ok = false; break; }
-    // ---------------- gather + dequantise this tile into sm.k ----------------
     const bool is_win = has_win && (t == ntiles - 1);
+    nxt.valid = 0;
+    if (t + 1 < t_end) gather(a, sm, r, b, pos, t + 1, has_win && t + 1 == ntiles - 1, key, part, nxt);
+    if (it > 0 && !mbar_wait(&sm.pv_bar, (it - 1) & 1)) { raise_flag(a.status, CSA_FLAG_TIMEOUT); ok = false; break; }
+    // ---------------- dequantise this tile into sm.k ----------------
     uint8_t* krow_base = sm.k + (key >> 3) * 1024;
     if (!is_win) {
-      const int j = t * kTileKeys + key;
-      int e = (j < nsel) ? __ldg(a.topk + (size_t)r * TOPK + j) : -1;
-      const uint8_t* src = nullptr;
-      if (e >= 0) {
-        if (e >= n || e / PAGE >= a.max_pages) {
-          raise_flag(a.status, CSA_FLAG_TOPK_OOB);
-        } else {
-          const int pg = __ldg(a.page_table + (size_t)b * a.max_pages + e / PAGE);
-          if (pg < 0 || pg >= a.num_pages) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
-          else src = a.kv_pool + (size_t)pg * KV_PAGE;
-        }
-      }
-      if (khalf == 0) sm.mu[key] = src ? 1.0f : 0.0f;
-      uint4 data[8], sc;
-      if (src) {
-        const uint4* dp = reinterpret_cast<const uint4*>(src + (e % PAGE) * 256 + khalf * 128);
+      if (part == 0) sm.mu[key] = cur.valid ? 1.0f : 0.0f;
+      const uint32_t sw[2] = {cur.valid ? cur.sc.x : 0u, cur.valid ? cur.sc.y : 0u};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) data[i] = __ldg(dp + i);
-        sc = __ldg(reinterpret_cast<const uint4*>(src + KV_SCALE_OFF + (e % PAGE) * 32 + khalf * 16));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) data[i] = make_uint4(0u, 0u, 0u, 0u);
-        sc = make_uint4(0u, 0u, 0u, 0u);
-      }
-      const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
-      // 128 data bytes = 256 dims = 4 atom columns of 64 dims; 16 B of data = 32 dims = 2 scale blocks
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t w4[4] = {data[i].x, data[i].y, data[i].z, data[i].w};
-        // data[i] covers dims 256*khalf + 32*i .. +32, scale blocks 2i, 2i+1
-        const uint32_t s0 = (scw[(2 * i) >> 2] >> (8 * ((2 * i) & 3))) & 0xFFu;
-        const uint32_t s1 = (scw[(2 * i + 1) >> 2] >> (8 * ((2 * i + 1) & 3))) & 0xFFu;
-        const __half2 hs0 = __float2half2_rn(sm.e4m3_tab[s0]);
-        const __half2 hs1 = __float2half2_rn(sm.e4m3_tab[s1]);
+      for (int i = 0; i < 4; ++i) {                  // 32 dims, scale blocks 2i and 2i+1
+        const uint4 dv = cur.valid ? cur.d[i] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w4[4] = {dv.x, dv.y, dv.z, dv.w};
+        uint32_t s2[2];
+        e4m3x4_to_f16(sw[i >> 1], s2);
+        const uint32_t sp = s2[i & 1];
+        const __half2 hs0 = __low2half2(*reinterpret_cast<const __half2*>(&sp));
+        const __half2 hs1 = __high2half2(*reinterpret_cast<const __half2*>(&sp));
         uint32_t o[16];
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {
-          const __half2 hs = (wd < 2) ? hs0 : hs1;
+          uint32_t f[4];
+          e2m1x8_to_f16(w4[wd], f);
 #pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const __half2 v = __hmul2(sm.e2m1_pair[(w4[wd] >> (8 * bb)) & 0xFFu], hs);
-            o[wd * 4 + bb] = *reinterpret_cast<const uint32_t*>(&v);
-          }
+          for (int bb = 0; bb < 4; ++bb) o[wd * 4 + bb] = hmul2_u32(f[bb], wd < 2 ? hs0 : hs1);
         }
-        const int dim0 = 256 * khalf + 32 * i;          // 32 dims = 4 chunks of 8
+        const int dim0 = 128 * part + 32 * i;          // 32 dims = 4 chunks of 8
         const int kc = dim0 >> 6, ch0 = (dim0 & 63) >> 3;
         uint8_t* dst = krow_base + kc * 16384;
 #pragma unroll
@@ -212,42 +279,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
               make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
       }
     } else {
-      const int lo_pos = max(0, pos - (WIN - 1));
-      const int p = lo_pos + key;
-      const bool valid = p <= pos;
-      uint4 data[16];
-      float s = 0.0f;
-      if (valid) {
-        const size_t slot = (size_t)b * a.win_cap + (size_t)(p % a.win_cap);
-        const uint4* dp = reinterpret_cast<const uint4*>(a.win_codes + slot * D + khalf * 256);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) data[i] = __ldg(dp + i);
-        s = __ldg(a.win_scale + slot);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) data[i] = make_uint4(0u, 0u, 0u, 0u);
-      }
       // s = 2^e * mu, mu in [1, 2): the codes are scaled by 2^e (exact in fp16)
       float pow2 = 0.0f, mu = 0.0f;
-      if (s > 0.0f) {
-        pow2 = __uint_as_float(__float_as_uint(s) & 0x7F800000u);
-        mu = s / pow2;
+      if (cur.valid && cur.ws > 0.0f) {
+        int ex;
+        const float m = frexpf(cur.ws, &ex);           // ws = m * 2^ex, m in [0.5, 1)
+        mu = 2.0f * m;
+        pow2 = ldexpf(1.0f, ex - 1);
       }
-      if (khalf == 0) sm.mu[key] = valid ? mu : 0.0f;
+      if (part == 0) sm.mu[key] = cur.valid ? mu : 0.0f;
+      const bool fast = pow2 >= 6.103515625e-05f && pow2 <= 32768.0f;   // 2^e is a normal fp16
+      const __half2 hp = __float2half2_rn(pow2);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {       // 16 codes = 16 dims = 2 chunks
-        const uint32_t w4[4] = {data[i].x, data[i].y, data[i].z, data[i].w};
+      for (int i = 0; i < 8; ++i) {                  // 16 codes = 16 dims = 2 chunks
+        const uint4 dv = cur.valid ? cur.d[i] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w4[4] = {dv.x, dv.y, dv.z, dv.w};
         uint32_t o[8];
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {
+          uint32_t f[2];
+          e4m3x4_to_f16(w4[wd], f);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t c0 = (w4[wd] >> (16 * hh)) & 0xFFu, c1 = (w4[wd] >> (16 * hh + 8)) & 0xFFu;
-            const __half2 v = __floats2half2_rn(sm.e4m3_tab[c0] * pow2, sm.e4m3_tab[c1] * pow2);
-            o[wd * 2 + hh] = *reinterpret_cast<const uint32_t*>(&v);
+            if (fast) {
+              o[wd * 2 + hh] = hmul2_u32(f[hh], hp);
+            } else {
+              const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&f[hh]));
+              const __half2 v = __floats2half2_rn(x.x * pow2, x.y * pow2);
+              o[wd * 2 + hh] = *reinterpret_cast<const uint32_t*>(&v);
+            }
           }
         }
-        const int dim0 = 256 * khalf + 16 * i;
+        const int dim0 = 128 * part + 16 * i;
         const int kc = dim0 >> 6, ch0 = (dim0 & 63) >> 3;
         uint8_t* dst = krow_base + kc * 16384;
         *reinterpret_cast<uint4*>(dst + swz128(key & 7, ch0)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -276,23 +339,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     float lg[HH];
     {
       const uint32_t base = tS + ((uint32_t)(32 * q4) << 16) + hsel * HH;
+      if constexpr (HH % 16 == 0) {
 #pragma unroll
-      for (int c = 0; c < HH; c += 16) {
-        uint32_t v[16];
-        if constexpr (HH >= 16) {
+        for (int c = 0; c < HH; c += 16) {
+          uint32_t v[16];
           tmem_ld16(base + c, v);
-        } else {
-          uint32_t v4[4];
-          tmem_ld4(base + c, v4);
-          uint32_t v4b[4];
-          tmem_ld4(base + c + 4, v4b);
+          tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) { v[i] = v4[i]; v[4 + i] = v4b[i]; }
+          for (int i = 0; i < 16; ++i) lg[c + i] = __uint_as_float(v[i]);
         }
-        tmem_ld_wait();
+      } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (c + i < HH) lg[c + i] = __uint_as_float(v[i]);
+        for (int c = 0; c < HH; c += 4) {
+          uint32_t v[4];
+          tmem_ld4(base + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) lg[c + i] = __uint_as_float(v[i]);
+        }
       }
     }
     // a global key is valid when it was gathered (mu = 1); a window key when
@@ -305,9 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     float tmp[HH];
 #pragma unroll
     for (int i = 0; i < HH; ++i) tmp[i] = lg[i];
+    constexpr int kShift = RedShift<HH>::v;
     {
       const float mx = warp_reduce_many<HH, true>(tmp, lane);
-      constexpr int kShift = (HH == 32) ? 0 : (HH == 16 ? 1 : 2);
       if ((lane & ((1 << kShift) - 1)) == 0) sm.red[q4][hsel * HH + (lane >> kShift)] = mx;
     }
     __syncthreads();
@@ -336,16 +400,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
         packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hv);
       }
       uint8_t* prow = sm.p + (mykey >> 3) * 1024;
+      if constexpr (HH >= 8) {
 #pragma unroll
-      for (int c = 0; c < HH / 8; ++c) {
-        const int chunk = (hsel * HH) / 8 + c;
-        *reinterpret_cast<uint4*>(prow + swz128(mykey & 7, chunk)) =
-            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        for (int c = 0; c < HH / 8; ++c) {
+          const int chunk = (hsel * HH) / 8 + c;
+          *reinterpret_cast<uint4*>(prow + swz128(mykey & 7, chunk)) =
+              make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        }
+      } else {                                        // 4 heads = half a 16-byte chunk
+        const int chunk = (hsel * HH) / 8;
+        *reinterpret_cast<uint2*>(prow + swz128(mykey & 7, chunk) + 8 * (hsel & 1)) =
+            make_uint2(packed[0], packed[1]);
       }
     }
     {
       const float sum = warp_reduce_many<HH, false>(tmp, lane);
-      constexpr int kShift = (HH == 32) ? 0 : (HH == 16 ? 1 : 2);
       __syncthreads();   // everyone is done reading sm.red (max) above
       if ((lane & ((1 << kShift) - 1)) == 0) sm.red[q4][hsel * HH + (lane >> kShift)] = sum;
     }
@@ -357,10 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     // rescale the O^T accumulators of heads whose running max grew
     if (sm.rescale) {
       tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int chunk = 2 * hsel + cc;
-        const uint32_t base = tO + ((uint32_t)(32 * q4) << 16) + chunk * 64;
+      const uint32_t base = tO + ((uint32_t)(32 * q4) << 16) + hsel * 64;
+      if constexpr (H % 16 == 0) {
+#pragma unroll 1
         for (int h0 = 0; h0 < H; h0 += 16) {
           uint32_t v[16];
           tmem_ld16(base + h0, v);
@@ -390,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
       tc_commit(&sm.pv_bar);
     }
     __syncwarp();
+    cur = nxt;
   }
   const int done = t_end - t_beg;
   if (ok && done > 0) {
@@ -401,27 +470,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   tc_fence_after();
   __syncthreads();
   // ---------------- epilogue ----------------
-  // thread: dims d = chunk*128 + 32*q4 + lane for chunks 2*hsel, 2*hsel+1
+  // thread: dims d = 128*hsel + 32*q4 + lane (O^T chunk hsel, TMEM lane quarter q4)
   const bool have = ok && done > 0;
+  const int d = 128 * hsel + 32 * q4 + lane;
+  const uint32_t obase = tO + ((uint32_t)(32 * q4) << 16) + hsel * 64;
   if (a.splits == 1) {
-    for (int cc = 0; cc < 2; ++cc) {
-      const int chunk = 2 * hsel + cc;
-      const int d = chunk * 128 + 32 * q4 + lane;
-      const uint32_t base = tO + ((uint32_t)(32 * q4) << 16) + chunk * 64;
-      for (int h0 = 0; h0 < H; h0 += 16) {
-        uint32_t v[16];
-        if (have) {
-          tmem_ld16(base + h0, v);
-          tmem_ld_wait();
-        }
+    for (int h0 = 0; h0 < H; h0 += 16) {
+      uint32_t v[16];
+      if (have) {
+        tmem_ld16(obase + h0, v);
+        tmem_ld_wait();
+      }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int h = h0 + i;
-          const float l = sm.l_run[h];
-          const float o = (have && l > 0.0f) ? __uint_as_float(v[i]) / l : 0.0f;
-          const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-          a.out[((size_t)r * H + h) * D + d] = *reinterpret_cast<const uint16_t*>(&ob);
-        }
+      for (int i = 0; i < 16; ++i) {
+        const int h = h0 + i;
+        const float l = sm.l_run[h];
+        const float o = (have && l > 0.0f) ? __uint_as_float(v[i]) / l : 0.0f;
+        const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+        a.out[((size_t)r * H + h) * D + d] = *reinterpret_cast<const uint16_t*>(&ob);
       }
     }
     if (a.lse && tid < H) {
@@ -430,24 +496,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     }
   } else {
     // partial: O [H][512] unnormalised, then m (log2) [H], l [H]
-    float* part = a.part + ((size_t)r * a.splits + split) * (size_t)H * (D + 2);
-    for (int cc = 0; cc < 2; ++cc) {
-      const int chunk = 2 * hsel + cc;
-      const int d = chunk * 128 + 32 * q4 + lane;
-      const uint32_t base = tO + ((uint32_t)(32 * q4) << 16) + chunk * 64;
-      for (int h0 = 0; h0 < H; h0 += 16) {
-        uint32_t v[16];
-        if (have) {
-          tmem_ld16(base + h0, v);
-          tmem_ld_wait();
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) part[(size_t)(h0 + i) * D + d] = have ? __uint_as_float(v[i]) : 0.0f;
+    float* part_out = a.part + ((size_t)r * a.splits + split) * (size_t)H * (D + 2);
+    for (int h0 = 0; h0 < H; h0 += 16) {
+      uint32_t v[16];
+      if (have) {
+        tmem_ld16(obase + h0, v);
+        tmem_ld_wait();
       }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) part_out[(size_t)(h0 + i) * D + d] = have ? __uint_as_float(v[i]) : 0.0f;
     }
     if (tid < H) {
-      part[(size_t)H * D + tid] = have ? sm.m_run[tid] : -INFINITY;
-      part[(size_t)H * D + H + tid] = have ? sm.l_run[tid] : 0.0f;
+      part_out[(size_t)H * D + tid] = have ? sm.m_run[tid] : -INFINITY;
+      part_out[(size_t)H * D + H + tid] = have ? sm.l_run[tid] : 0.0f;
     }
   }
   tc_fence_before();
