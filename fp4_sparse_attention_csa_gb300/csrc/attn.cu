@@ -12,8 +12,8 @@
 //   route besides one that rounds Q and P to MXFP8; here every MMA operand is
 //   fp16 and exact except P (rounded once to fp16).
 //
-// Per CTA: one row and a contiguous run of its 128-key tiles (tiles 0..3 =
-// the selected entries in ascending order, the last tile = the window).  Each
+// Per CTA: one row and a contiguous run of its 128-key tiles (the window
+// first, then the selected entries' tiles in ascending order).  Each
 // tile is gathered and dequantised to fp16 into one shared-memory buffer
 // [128 keys x 512 dims] (128-byte swizzle), which serves as
 //   the K-major A operand of  S^T = K Q^T        (M = 128 keys, N = H heads)
@@ -29,7 +29,10 @@
 // threads together; the raw FP4/FP8 bytes of tile t+1 are loaded into
 // registers while tile t is dequantised and multiplied, so the HBM gather of
 // one tile overlaps the tensor-core and softmax work of the previous one.
-// Dequantisation uses the packed e2m1x2 / e4m3x2 -> f16x2 conversions.
+// Dequantisation uses the packed e2m1x2 / e4m3x2 -> f16x2 conversions.  MMA
+// descriptors are formed once and advanced by constant offsets, so the
+// issuing thread keeps the tensor pipe busy.  The output is normalised by a
+// per-head reciprocal and leaves through shared memory in 16-byte stores.
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
@@ -41,8 +44,13 @@ constexpr int kThreads = 512;
 constexpr int kTileKeys = 128;
 constexpr int kMainTiles = TOPK / kTileKeys;      // 4
 constexpr int kMaxTiles = kMainTiles + 1;         // 4 global + 1 window
+static_assert(TOPK == kThreads, "one selected entry per thread in the set-up lookup");
 constexpr int kMaxH = CSA_MAX_HEADS;             // 64
 constexpr float kLog2e = 1.4426950408889634f;
+// The running max used for exp2 moves only when a tile's max exceeds it by
+// more than this (log2 units): p <= 2^8, so P stays far inside fp16 range and
+// the O^T accumulators are rarely rescaled.
+constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnSmem {
   uint8_t k[kTileKeys * D * 2];        // 131072, 1024-aligned: kc*16384 + (key/8)*1024 + (key%8)*128
@@ -51,11 +59,13 @@ struct AttnSmem {
   int32_t ent_pg[TOPK];                // page of each selected entry, -1 when none
   uint8_t ent_slot[TOPK];
   float mu[kTileKeys];
-  float red[4][kMaxH];                 // per-quarter partial max / sum
-  float m_run[kMaxH], l_run[kMaxH], alpha[kMaxH];
+  float red_max[4][kMaxH];             // per key-quarter partial max / sum of a tile
+  float red_sum[4][kMaxH];
+  float m_buf[2][kMaxH];               // running max (log2), by tile parity
+  float l_run[kMaxH];
+  float inv_l[kMaxH];
   uint64_t s_bar, pv_bar;
   uint32_t tmem_base;
-  int32_t rescale;
 };
 
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
@@ -125,41 +135,202 @@ __device__ __forceinline__ float warp_reduce_many(float (&v)[NV], int lane) {
   return x;
 }
 
-// Raw bytes of one key's quarter (128 dims) of a tile, in registers.
-struct Raw {
-  uint4 d[8];      // main entry: d[0..3] = 64 FP4 bytes; window: 128 E4M3 codes
-  uint2 sc;        // main entry: the 8 E4M3 block scales of these 128 dims
-  float ws;        // window token: fp32 scale
+// Gather role of a thread: warp w holds keys 8w..8w+7, lane = 8q + (key & 7).
+// A thread takes the 16-byte chunks c16 = 4i + q of its key's row, so one
+// warp-wide load covers 8 keys x 64 contiguous bytes (8 cache lines), and the
+// eight lanes of a quarter-warp, which differ in key & 7, store to distinct
+// swizzled banks.
+struct RawMain {
+  uint4 d[4];      // chunks c16 = q, 4+q, 8+q, 12+q of the 256 FP4 data bytes
+  uint16_t sc[4];  // E4M3 scales of blocks 2*c16, 2*c16+1 for each chunk
+  int valid;
+};
+struct RawWin {
+  uint4 d[8];      // chunks c16 = 4i + q (i = 0..7) of the 512 E4M3 codes
+  float ws;        // the token's fp32 scale
   int valid;
 };
 
-__device__ __forceinline__ void gather(const AttnArgs& a, const AttnSmem& sm, int r, int b, int pos,
-                                       int t, bool is_win, int key, int part, Raw& g) {
-  if (!is_win) {
-    const int j = t * kTileKeys + key;
-    const int pg = sm.ent_pg[j];
-    g.valid = pg >= 0;
-    if (pg >= 0) {
-      const uint8_t* src = a.kv_pool + (size_t)pg * KV_PAGE;
-      const int slot = sm.ent_slot[j];
-      const uint4* dp = reinterpret_cast<const uint4*>(src + slot * 256 + 64 * part);
+// Loads written as volatile asm stay where the program issues them, so the
+// prefetch of the next tile is in flight while this one is processed.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint16_t ldg_nc_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ldg_nc_f32(const void* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void gather_main(const AttnArgs& a, const AttnSmem& sm, int m, int key, int q,
+                                            RawMain& g) {
+  const int j = m * kTileKeys + key;
+  const int pg = sm.ent_pg[j];
+  g.valid = pg >= 0;
+  if (pg >= 0) {
+    const uint8_t* src = a.kv_pool + (size_t)pg * KV_PAGE;
+    const int slot = sm.ent_slot[j];
+    const uint8_t* dp = src + slot * 256 + 16 * q;
+    const uint8_t* sp = src + KV_SCALE_OFF + slot * 32 + 2 * q;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) g.d[i] = __ldg(dp + i);
-      g.sc = __ldg(reinterpret_cast<const uint2*>(src + KV_SCALE_OFF + slot * 32 + 8 * part));
+    for (int i = 0; i < 4; ++i) g.d[i] = ldg_nc_v4(dp + 64 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) g.sc[i] = ldg_nc_u16(sp + 8 * i);
+  }
+}
+
+__device__ __forceinline__ void gather_win(const AttnArgs& a, int b, int pos, int key, int q, RawWin& g) {
+  const int p = max(0, pos - (WIN - 1)) + key;
+  g.valid = p <= pos;
+  if (p <= pos) {
+    const size_t slot = (size_t)b * a.win_cap + (size_t)(p % a.win_cap);
+    const uint8_t* dp = a.win_codes + slot * D + 16 * q;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g.d[i] = ldg_nc_v4(dp + 64 * i);
+    g.ws = ldg_nc_f32(a.win_scale + slot);
+  }
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16(uint16_t v) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+  return d;
+}
+
+// NVFP4 entry chunks -> fp16 K rows (e2m1 * E4M3 scale is exact in fp16).
+__device__ __forceinline__ void dequant_main(const RawMain& g, AttnSmem& sm, int key, int q) {
+  uint8_t* krow_base = sm.k + (key >> 3) * 1024;
+  if (q == 0) sm.mu[key] = g.valid ? 1.0f : 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {                  // chunk c16 = 4i + q: dims 32*c16 .. +32
+    const uint4 dv = g.valid ? g.d[i] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w4[4] = {dv.x, dv.y, dv.z, dv.w};
+    const uint32_t sp = e4m3x2_to_f16(g.valid ? g.sc[i] : (uint16_t)0);
+    const __half2 hs0 = __low2half2(*reinterpret_cast<const __half2*>(&sp));
+    const __half2 hs1 = __high2half2(*reinterpret_cast<const __half2*>(&sp));
+    uint32_t o[16];
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+      uint32_t f[4];
+      e2m1x8_to_f16(w4[wd], f);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) o[wd * 4 + bb] = hmul2_u32(f[bb], wd < 2 ? hs0 : hs1);
+    }
+    const int c16 = 4 * i + q;
+    const int kc = c16 >> 1, ch0 = (c16 & 1) * 4;    // 64-dim atom, first 8-dim chunk
+    uint8_t* dst = krow_base + kc * 16384;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(dst + swz128(key & 7, ch0 + c)) =
+          make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+  }
+}
+
+// Window token chunks: s = 2^e * mu, mu in [1, 2); codes * 2^e go to the
+// fp16 K rows (exact), mu scales the logit and p.
+__device__ __forceinline__ void dequant_win(const RawWin& g, AttnSmem& sm, int key, int q) {
+  uint8_t* krow_base = sm.k + (key >> 3) * 1024;
+  float pow2 = 0.0f, mu = 0.0f;
+  if (g.valid && g.ws > 0.0f) {
+    int ex;
+    const float m = frexpf(g.ws, &ex);             // ws = m * 2^ex, m in [0.5, 1)
+    mu = 2.0f * m;
+    pow2 = ldexpf(1.0f, ex - 1);
+  }
+  if (q == 0) sm.mu[key] = g.valid ? mu : 0.0f;
+  const bool fast = pow2 >= 6.103515625e-05f && pow2 <= 32768.0f;   // 2^e is a normal fp16
+  const __half2 hp = __float2half2_rn(pow2);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {                  // chunk c16 = 4i + q: 16 codes = dims 16*c16 .. +16
+    const uint4 dv = g.valid ? g.d[i] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w4[4] = {dv.x, dv.y, dv.z, dv.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+      uint32_t f[2];
+      e4m3x4_to_f16(w4[wd], f);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (fast) {
+          o[wd * 2 + hh] = hmul2_u32(f[hh], hp);
+        } else {
+          const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&f[hh]));
+          const __half2 v = __floats2half2_rn(x.x * pow2, x.y * pow2);
+          o[wd * 2 + hh] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+      }
+    }
+    const int c16 = 4 * i + q;
+    const int kc = c16 >> 2, ch0 = (c16 & 3) * 2;
+    uint8_t* dst = krow_base + kc * 16384;
+    *reinterpret_cast<uint4*>(dst + swz128(key & 7, ch0)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(dst + swz128(key & 7, ch0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+// Barrier over the four warps that share one head group (ids 1..8).
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N % 16 == 0) {
+#pragma unroll
+    for (int c = 0; c < N; c += 16) {
+      uint32_t u[16];
+      tmem_ld16(taddr + c, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[c + i] = __uint_as_float(u[i]);
     }
   } else {
-    const int p = max(0, pos - (WIN - 1)) + key;
-    g.valid = p <= pos;
-    if (p <= pos) {
-      const size_t slot = (size_t)b * a.win_cap + (size_t)(p % a.win_cap);
-      const uint4* dp = reinterpret_cast<const uint4*>(a.win_codes + slot * D + 128 * part);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) g.d[i] = __ldg(dp + i);
-      g.ws = __ldg(a.win_scale + slot);
+    for (int c = 0; c < N; c += 4) {
+      uint32_t u[4];
+      tmem_ld4(taddr + c, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[c + i] = __uint_as_float(u[i]);
     }
   }
 }
 
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float (&v)[N]) {
+  if constexpr (N % 16 == 0) {
+#pragma unroll
+    for (int c = 0; c < N; c += 16) {
+      uint32_t u[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[c + i]);
+      tmem_st16(taddr + c, u);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < N; c += 4) {
+      uint32_t u[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) u[i] = __float_as_uint(v[c + i]);
+      tmem_st4(taddr + c, u);
+    }
+  }
+}
+
+// Tile order within a row: the window first (when present), then the
+// selected entries' tiles in ascending order.  A CTA takes the contiguous
+// tile range [t_beg, t_end) of its split.
 template <int H>
 __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   constexpr int HH = H / 4;                       // heads per thread in the softmax
@@ -175,32 +346,70 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const int n = row_ok ? (pos + 1) / a.P : 0;
   const int nsel = min(n, TOPK);
   const int gtiles = (nsel + kTileKeys - 1) / kTileKeys;
-  const bool has_win = (a.win_codes != nullptr) && row_ok;
-  const int ntiles = gtiles + (has_win ? 1 : 0);
+  const int hw = ((a.win_codes != nullptr) && row_ok) ? 1 : 0;   // window tile present
+  const int ntiles = gtiles + hw;
   const int tper = (ntiles + a.splits - 1) / a.splits;
   const int t_beg = min(ntiles, split * tper), t_end = min(ntiles, t_beg + tper);
+  const bool win_here = hw && t_beg == 0 && t_end > 0;
+  const int m_beg = max(t_beg - hw, 0), m_end = max(t_end - hw, 0);   // main tiles [m_beg, m_end)
 
-  // ---- setup: entry pages, barriers, TMEM, Q (bf16 -> fp16, K-major 128B swizzle)
+  // ---- setup.  The window tile's loads go out first (they need no lookup);
+  // the selected entries are looked up (index, then page) while Q is loaded,
+  // and every entry's bytes are prefetched into L2 at once, so the per-tile
+  // gathers below hit L2.
+  const int key = 8 * warp + (lane & 7), gq = lane >> 3;      // gather role (see RawMain)
+  RawWin wraw;
+  RawMain cur, nxt;
+  wraw.valid = 0;
+  cur.valid = 0;
+  if (win_here) gather_win(a, b, pos, key, gq, wraw);
+  const int j = tid;                              // TOPK == kThreads: one selected entry per thread
+  const bool jin = j < nsel && j >= m_beg * kTileKeys && j < m_end * kTileKeys;
+  int e = jin ? __ldg(a.topk + (size_t)r * TOPK + j) : -1;
+  constexpr int kQChunks = H * 64 / kThreads;     // 16-byte chunks of Q per thread
+  uint4 qv[kQChunks];
+  const uint16_t* qr = a.q + (size_t)r * H * D;
+#pragma unroll
+  for (int i = 0; i < kQChunks; ++i) {
+    const int c = tid + i * kThreads, h = c >> 6, ch = c & 63;
+    qv[i] = __ldg(reinterpret_cast<const uint4*>(qr + (size_t)h * D + ch * 8));
+  }
   {
-    const int j = tid;                            // TOPK == kThreads
     int pg = -1, slot = 0;
-    if (j < nsel && j >= t_beg * kTileKeys && j < min(t_end, gtiles) * kTileKeys) {
-      const int e = __ldg(a.topk + (size_t)r * TOPK + j);
-      if (e >= 0) {
-        if (e >= n || e / PAGE >= a.max_pages) {
-          raise_flag(a.status, CSA_FLAG_TOPK_OOB);
-        } else {
-          const int p = __ldg(a.page_table + (size_t)b * a.max_pages + e / PAGE);
-          if (p < 0 || p >= a.num_pages) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
-          else { pg = p; slot = e % PAGE; }
-        }
+    if (e >= 0) {
+      if (e >= n || e / PAGE >= a.max_pages) {
+        raise_flag(a.status, CSA_FLAG_TOPK_OOB);
+      } else {
+        const int p = __ldg(a.page_table + (size_t)b * a.max_pages + e / PAGE);
+        if (p < 0 || p >= a.num_pages) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
+        else { pg = p; slot = e % PAGE; }
       }
+    }
+    if (pg >= 0) {
+      const uint8_t* src = a.kv_pool + (size_t)pg * KV_PAGE;
+      prefetch_l2(src + slot * 256, 256);
+      prefetch_l2(src + KV_SCALE_OFF + slot * 32, 32);
     }
     sm.ent_pg[j] = pg;
     sm.ent_slot[j] = (uint8_t)slot;
   }
+  // Q: bf16 -> fp16, K-major 128B swizzle
+#pragma unroll
+  for (int i = 0; i < kQChunks; ++i) {
+    const int c = tid + i * kThreads, h = c >> 6, ch = c & 63, kc = ch >> 3;
+    const uint32_t w[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 hv = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+      o[k] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    *reinterpret_cast<uint4*>(sm.q + kc * (H * 128) + (h >> 3) * 1024 + swz128(h & 7, ch & 7)) =
+        make_uint4(o[0], o[1], o[2], o[3]);
+  }
   if (tid < H) {
-    sm.m_run[tid] = -INFINITY;
+    sm.m_buf[0][tid] = -INFINITY;
+    sm.m_buf[1][tid] = -INFINITY;
     sm.l_run[tid] = 0.0f;
   }
   if (tid == 0) {
@@ -209,22 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     fence_barrier_init();
   }
   if (warp == 0) tmem_alloc(&sm.tmem_base, 512);
-  {
-    const uint16_t* qr = a.q + (size_t)r * H * D;
-    for (int c = tid; c < H * 64; c += kThreads) {     // 16-byte chunks of 8 dims
-      const int h = c >> 6, ch = c & 63, kc = ch >> 3;
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(qr + (size_t)h * D + ch * 8));
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half2 hv = __floats2half2_rn(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-        o[i] = *reinterpret_cast<const uint32_t*>(&hv);
-      }
-      *reinterpret_cast<uint4*>(sm.q + kc * (H * 128) + (h >> 3) * 1024 + swz128(h & 7, ch & 7)) =
-          make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
+  __syncthreads();                                // entry table visible
+  if (!win_here && m_beg < m_end) gather_main(a, sm, m_beg, key, gq, cur);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -233,170 +428,81 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const uint32_t tS = tmem, tO = tmem + 64;      // S^T: H cols; O^T chunk c at 64 + 64c
   const float scale_log2 = a.softmax_scale * kLog2e;
 
-  const int key = tid & (kTileKeys - 1), part = tid >> 7;    // gather role: dims 128*part..+128
-  const int q4 = warp & 3, hsel = warp >> 2;                  // TMEM role: lane quarter, head quarter
+  const int q4 = warp & 3, hsel = warp >> 2;                  // TMEM role: lane quarter, head group
   const int mykey = 32 * q4 + lane;
+  const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+  const int myh = hsel * HH + (lane < HH ? lane : 0);         // head owned by this lane (lane < HH)
   bool ok = true;
+  // base descriptors; each MMA adds a constant (byte offset >> 4) to the address field
+  const uint64_t dK = smem_desc(smem_u32(sm.k), 16, 1024, kSwizzle128B);
+  const uint64_t dQ = smem_desc(smem_u32(sm.q), 16, 1024, kSwizzle128B);
+  const uint64_t dV = smem_desc(smem_u32(sm.k), 16384, 1024, kSwizzle128B);
+  const uint64_t dP = smem_desc(smem_u32(sm.p), 8192, 1024, kSwizzle128B);
 
-  Raw cur, nxt;
-  cur.valid = 0;
-  if (t_beg < t_end) gather(a, sm, r, b, pos, t_beg, has_win && t_beg == ntiles - 1, key, part, cur);
-
-  for (int t = t_beg; t < t_end && ok; ++t) {
-    const int it = t - t_beg;
-    const bool is_win = has_win && (t == ntiles - 1);
-    nxt.valid = 0;
-    if (t + 1 < t_end) gather(a, sm, r, b, pos, t + 1, has_win && t + 1 == ntiles - 1, key, part, nxt);
-    if (it > 0 && !mbar_wait(&sm.pv_bar, (it - 1) & 1)) { raise_flag(a.status, CSA_FLAG_TIMEOUT); ok = false; break; }
-    // ---------------- dequantise this tile into sm.k ----------------
-    uint8_t* krow_base = sm.k + (key >> 3) * 1024;
-    if (!is_win) {
-      if (part == 0) sm.mu[key] = cur.valid ? 1.0f : 0.0f;
-      const uint32_t sw[2] = {cur.valid ? cur.sc.x : 0u, cur.valid ? cur.sc.y : 0u};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {                  // 32 dims, scale blocks 2i and 2i+1
-        const uint4 dv = cur.valid ? cur.d[i] : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t w4[4] = {dv.x, dv.y, dv.z, dv.w};
-        uint32_t s2[2];
-        e4m3x4_to_f16(sw[i >> 1], s2);
-        const uint32_t sp = s2[i & 1];
-        const __half2 hs0 = __low2half2(*reinterpret_cast<const __half2*>(&sp));
-        const __half2 hs1 = __high2half2(*reinterpret_cast<const __half2*>(&sp));
-        uint32_t o[16];
-#pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
-          uint32_t f[4];
-          e2m1x8_to_f16(w4[wd], f);
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) o[wd * 4 + bb] = hmul2_u32(f[bb], wd < 2 ? hs0 : hs1);
-        }
-        const int dim0 = 128 * part + 32 * i;          // 32 dims = 4 chunks of 8
-        const int kc = dim0 >> 6, ch0 = (dim0 & 63) >> 3;
-        uint8_t* dst = krow_base + kc * 16384;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(dst + swz128(key & 7, ch0 + c)) =
-              make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-      }
-    } else {
-      // s = 2^e * mu, mu in [1, 2): the codes are scaled by 2^e (exact in fp16)
-      float pow2 = 0.0f, mu = 0.0f;
-      if (cur.valid && cur.ws > 0.0f) {
-        int ex;
-        const float m = frexpf(cur.ws, &ex);           // ws = m * 2^ex, m in [0.5, 1)
-        mu = 2.0f * m;
-        pow2 = ldexpf(1.0f, ex - 1);
-      }
-      if (part == 0) sm.mu[key] = cur.valid ? mu : 0.0f;
-      const bool fast = pow2 >= 6.103515625e-05f && pow2 <= 32768.0f;   // 2^e is a normal fp16
-      const __half2 hp = __float2half2_rn(pow2);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {                  // 16 codes = 16 dims = 2 chunks
-        const uint4 dv = cur.valid ? cur.d[i] : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t w4[4] = {dv.x, dv.y, dv.z, dv.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
-          uint32_t f[2];
-          e4m3x4_to_f16(w4[wd], f);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            if (fast) {
-              o[wd * 2 + hh] = hmul2_u32(f[hh], hp);
-            } else {
-              const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&f[hh]));
-              const __half2 v = __floats2half2_rn(x.x * pow2, x.y * pow2);
-              o[wd * 2 + hh] = *reinterpret_cast<const uint32_t*>(&v);
-            }
-          }
-        }
-        const int dim0 = 128 * part + 16 * i;
-        const int kc = dim0 >> 6, ch0 = (dim0 & 63) >> 3;
-        uint8_t* dst = krow_base + kc * 16384;
-        *reinterpret_cast<uint4*>(dst + swz128(key & 7, ch0)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(dst + swz128(key & 7, ch0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
-      }
-    }
+  // S^T, softmax, P, rescale, PV for the tile now in sm.k.
+  auto compute = [&](int it, bool is_win) -> bool {
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // ---------------- S^T = K Q^T ----------------
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t kb = smem_u32(sm.k), qb = smem_u32(sm.q);
-#pragma unroll 4
+      constexpr uint32_t id = idesc_f16(128, H, 0, 0);
+#pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        mma_f16(tS, smem_desc(kb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128B),
-                smem_desc(qb + (ks >> 2) * (H * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128B),
-                idesc_f16(128, H, 0, 0), ks > 0 ? 1u : 0u);
+        mma_f16(tS, dK + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                dQ + (uint64_t)((ks >> 2) * (H * 8) + (ks & 3) * 2), id, ks > 0 ? 1u : 0u);
       }
       tc_commit(&sm.s_bar);
     }
     __syncwarp();
-    if (!mbar_wait(&sm.s_bar, it & 1)) { raise_flag(a.status, CSA_FLAG_TIMEOUT); ok = false; break; }
-    tc_fence_after();
-    // ---------------- softmax over this tile (log2 domain) ----------------
-    float lg[HH];
-    {
-      const uint32_t base = tS + ((uint32_t)(32 * q4) << 16) + hsel * HH;
-      if constexpr (HH % 16 == 0) {
-#pragma unroll
-        for (int c = 0; c < HH; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(base + c, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) lg[c + i] = __uint_as_float(v[i]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < HH; c += 4) {
-          uint32_t v[4];
-          tmem_ld4(base + c, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) lg[c + i] = __uint_as_float(v[i]);
-        }
-      }
+    // every thread takes the same branch, so no barrier below is left short
+    if (__syncthreads_or(!mbar_wait(&sm.s_bar, it & 1))) {
+      if (tid == 0) raise_flag(a.status, CSA_FLAG_TIMEOUT);
+      return false;
     }
+    tc_fence_after();
+    // ---- softmax over this tile (log2 domain) ----
+    float lg[HH];
+    tmem_ld_n<HH>(tS + lane_off + hsel * HH, lg);
     // a global key is valid when it was gathered (mu = 1); a window key when
     // its position is inside the window (an all-zero token has mu = 0 and
     // contributes logit 0 and value 0, as its dequantised vector is zero)
     const float mu_k = sm.mu[mykey];
     const bool key_ok = is_win ? (max(0, pos - (WIN - 1)) + mykey) <= pos : mu_k != 0.0f;
+    const float f = scale_log2 * (is_win ? mu_k : 1.0f);
 #pragma unroll
-    for (int i = 0; i < HH; ++i) lg[i] = key_ok ? lg[i] * (scale_log2 * (is_win ? mu_k : 1.0f)) : -INFINITY;
+    for (int i = 0; i < HH; ++i) lg[i] = key_ok ? lg[i] * f : -INFINITY;
     float tmp[HH];
 #pragma unroll
     for (int i = 0; i < HH; ++i) tmp[i] = lg[i];
     constexpr int kShift = RedShift<HH>::v;
     {
       const float mx = warp_reduce_many<HH, true>(tmp, lane);
-      if ((lane & ((1 << kShift) - 1)) == 0) sm.red[q4][hsel * HH + (lane >> kShift)] = mx;
+      if ((lane & ((1 << kShift) - 1)) == 0) sm.red_max[q4][hsel * HH + (lane >> kShift)] = mx;
     }
-    __syncthreads();
-    if (tid < H) {
-      const float tmax = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
-      const float mold = sm.m_run[tid];
-      const float mnew = fmaxf(mold, tmax);
-      sm.alpha[tid] = (mold == -INFINITY) ? 0.0f : exp2f(mold - mnew);
-      sm.m_run[tid] = mnew;
+    group_sync(1 + hsel);
+    // lane i < HH owns head hsel*HH + i: its new running max and correction
+    float mnew = 0.0f, alpha = 1.0f;
+    {
+      const float tmax = fmaxf(fmaxf(sm.red_max[0][myh], sm.red_max[1][myh]),
+                               fmaxf(sm.red_max[2][myh], sm.red_max[3][myh]));
+      const float mold = sm.m_buf[(it + 1) & 1][myh];
+      mnew = (mold == -INFINITY || tmax > mold + kRescaleLog2) ? tmax : mold;
+      alpha = (mold == -INFINITY) ? 0.0f : (mnew == mold ? 1.0f : exp2f(mold - mnew));
+      if (q4 == 0 && lane < HH) sm.m_buf[it & 1][myh] = mnew;
     }
-    if (tid == 0) sm.rescale = 0;
-    __syncthreads();
-    if (tid < H && it > 0 && sm.alpha[tid] != 1.0f) sm.rescale = 1;
     // p = exp2(l - m); P'^T = p * mu (window) as fp16, heads along the 128-byte row
     {
+      const float fm = is_win ? mu_k : 1.0f;
       uint32_t packed[HH / 2];
 #pragma unroll
       for (int i = 0; i < HH; i += 2) {
-        const float m0 = sm.m_run[hsel * HH + i], m1 = sm.m_run[hsel * HH + i + 1];
+        const float m0 = __shfl_sync(0xFFFFFFFFu, mnew, i), m1 = __shfl_sync(0xFFFFFFFFu, mnew, i + 1);
         const float p0 = (lg[i] == -INFINITY) ? 0.0f : exp2f(lg[i] - m0);
         const float p1 = (lg[i + 1] == -INFINITY) ? 0.0f : exp2f(lg[i + 1] - m1);
         tmp[i] = p0;
         tmp[i + 1] = p1;
-        const float f = is_win ? mu_k : 1.0f;
-        const __half2 hv = __floats2half2_rn(p0 * f, p1 * f);
+        const __half2 hv = __floats2half2_rn(p0 * fm, p1 * fm);
         packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hv);
       }
       uint8_t* prow = sm.p + (mykey >> 3) * 1024;
@@ -415,52 +521,74 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     }
     {
       const float sum = warp_reduce_many<HH, false>(tmp, lane);
-      __syncthreads();   // everyone is done reading sm.red (max) above
-      if ((lane & ((1 << kShift) - 1)) == 0) sm.red[q4][hsel * HH + (lane >> kShift)] = sum;
+      if ((lane & ((1 << kShift) - 1)) == 0) sm.red_sum[q4][hsel * HH + (lane >> kShift)] = sum;
     }
-    __syncthreads();
-    if (tid < H) {
-      const float ts = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
-      sm.l_run[tid] = sm.alpha[tid] * sm.l_run[tid] + ts;
-    }
-    // rescale the O^T accumulators of heads whose running max grew
-    if (sm.rescale) {
-      tc_fence_after();
-      const uint32_t base = tO + ((uint32_t)(32 * q4) << 16) + hsel * 64;
-      if constexpr (H % 16 == 0) {
-#pragma unroll 1
-        for (int h0 = 0; h0 < H; h0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(base + h0, v);
-          tmem_ld_wait();
+    // rescale this warp's lanes of the O^T columns of its heads whose max moved
+    const bool resc = __any_sync(0xFFFFFFFFu, it > 0 && lane < HH && alpha != 1.0f);
+    if (resc) {
+      float al[HH];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * sm.alpha[h0 + i]);
-          tmem_st16(base + h0, v);
-        }
+      for (int i = 0; i < HH; ++i) al[i] = __shfl_sync(0xFFFFFFFFu, alpha, i);
+#pragma unroll 1
+      for (int dc = 0; dc < D / 128; ++dc) {
+        float v[HH];
+        const uint32_t ta = tO + lane_off + dc * 64 + hsel * HH;
+        tmem_ld_n<HH>(ta, v);
+#pragma unroll
+        for (int i = 0; i < HH; ++i) v[i] *= al[i];
+        tmem_st_n<HH>(ta, v);
       }
       tmem_st_wait();
+    }
+    group_sync(5 + hsel);
+    if (q4 == 0 && lane < HH) {
+      const float ts = (sm.red_sum[0][myh] + sm.red_sum[1][myh]) + (sm.red_sum[2][myh] + sm.red_sum[3][myh]);
+      sm.l_run[myh] = alpha * sm.l_run[myh] + ts;
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // ---------------- O^T += V^T P^T ----------------
+    // ---- O^T += V^T P^T ----
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t kb = smem_u32(sm.k), pb = smem_u32(sm.p);
+      constexpr uint32_t id = idesc_f16(128, H, 1, 1);
+      const uint32_t acc0 = it > 0 ? 1u : 0u;
+#pragma unroll
       for (int dc = 0; dc < D / 128; ++dc) {
 #pragma unroll
         for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-          mma_f16(tO + dc * 64, smem_desc(kb + dc * 32768 + ks * 2048, 16384, 1024, kSwizzle128B),
-                  smem_desc(pb + ks * 2048, 8192, 1024, kSwizzle128B), idesc_f16(128, H, 1, 1),
-                  (it > 0 || ks > 0) ? 1u : 0u);
+          mma_f16(tO + dc * 64, dV + (uint64_t)(dc * 2048 + ks * 128), dP + (uint64_t)(ks * 128), id,
+                  ks > 0 ? 1u : acc0);
         }
       }
       tc_commit(&sm.pv_bar);
     }
     __syncwarp();
+    return true;
+  };
+
+  int it = 0;
+  if (win_here) {
+    if (m_beg < m_end) gather_main(a, sm, m_beg, key, gq, cur);
+    // ---------------- the window tile ----------------
+    dequant_win(wraw, sm, key, gq);
+    ok = compute(0, true);
+    it = 1;
+  }
+  for (int m = m_beg; m < m_end && ok; ++m, ++it) {
+    nxt.valid = 0;
+    if (m + 1 < m_end) gather_main(a, sm, m + 1, key, gq, nxt);
+    if (__syncthreads_or(it > 0 && !mbar_wait(&sm.pv_bar, (it - 1) & 1))) {
+      if (tid == 0) raise_flag(a.status, CSA_FLAG_TIMEOUT);
+      ok = false;
+      break;
+    }
+    // ---------------- dequantise this tile into sm.k ----------------
+    dequant_main(cur, sm, key, gq);
+    ok = compute(it, false);
     cur = nxt;
   }
-  const int done = t_end - t_beg;
+  const int done = it;
   if (ok && done > 0) {
     if (!mbar_wait(&sm.pv_bar, (done - 1) & 1)) {
       raise_flag(a.status, CSA_FLAG_TIMEOUT);
@@ -472,27 +600,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   // ---------------- epilogue ----------------
   // thread: dims d = 128*hsel + 32*q4 + lane (O^T chunk hsel, TMEM lane quarter q4)
   const bool have = ok && done > 0;
+  const float* m_fin = sm.m_buf[(done + 1) & 1];     // written by the last tile (it = done - 1)
   const int d = 128 * hsel + 32 * q4 + lane;
-  const uint32_t obase = tO + ((uint32_t)(32 * q4) << 16) + hsel * 64;
+  const uint32_t obase = tO + lane_off + hsel * 64;
   if (a.splits == 1) {
+    // O[h][d] = O^T[d][h] / l[h] as bf16, staged in sm.k (free after the last PV)
+    if (tid < H) {
+      const float l = sm.l_run[tid];
+      sm.inv_l[tid] = (have && l > 0.0f) ? 1.0f / l : 0.0f;
+    }
+    __syncthreads();
+    __nv_bfloat16* ostage = reinterpret_cast<__nv_bfloat16*>(sm.k);
     for (int h0 = 0; h0 < H; h0 += 16) {
       uint32_t v[16];
       if (have) {
         tmem_ld16(obase + h0, v);
         tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0u;
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int h = h0 + i;
-        const float l = sm.l_run[h];
-        const float o = (have && l > 0.0f) ? __uint_as_float(v[i]) / l : 0.0f;
-        const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-        a.out[((size_t)r * H + h) * D + d] = *reinterpret_cast<const uint16_t*>(&ob);
-      }
+      for (int i = 0; i < 16; ++i)
+        ostage[(h0 + i) * D + d] = __float2bfloat16_rn(__uint_as_float(v[i]) * sm.inv_l[h0 + i]);
+    }
+    __syncthreads();
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(ostage);
+      uint4* dst = reinterpret_cast<uint4*>(a.out + (size_t)r * H * D);
+      for (int i = tid; i < H * D / 8; i += kThreads) dst[i] = src[i];
     }
     if (a.lse && tid < H) {
       const float l = sm.l_run[tid];
-      a.lse[(size_t)r * H + tid] = (have && l > 0.0f) ? (sm.m_run[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      a.lse[(size_t)r * H + tid] = (have && l > 0.0f) ? (m_fin[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
   } else {
     // partial: O [H][512] unnormalised, then m (log2) [H], l [H]
@@ -507,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
       for (int i = 0; i < 16; ++i) part_out[(size_t)(h0 + i) * D + d] = have ? __uint_as_float(v[i]) : 0.0f;
     }
     if (tid < H) {
-      part_out[(size_t)H * D + tid] = have ? sm.m_run[tid] : -INFINITY;
+      part_out[(size_t)H * D + tid] = have ? m_fin[tid] : -INFINITY;
       part_out[(size_t)H * D + H + tid] = have ? sm.l_run[tid] : 0.0f;
     }
   }
