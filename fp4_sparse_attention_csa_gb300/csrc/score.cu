@@ -21,15 +21,19 @@
 //                        pages = one 128-entry tile per stage, 12 stages; the
 //                        copy engine is fed by several warps because one
 //                        warp's copy issue rate caps its bandwidth.
-//                scale warp  gathers the tile's E8M0 bytes into the tcgen05
-//                        scale-factor atom (and the q scales per segment).
-//                MMA thread  tcgen05.cp of the scales, two kind::mxf4 MMAs
-//                        (K = 64 each) per 128-column N chunk; A = 128 entries
-//                        x 128 dims, B = rows*heads x 128 dims, D = fp32 [entry
-//                        lane, row*head column] in TMEM.
-//                4 epilogue warp groups on 4 TMEM accumulator buffers: per
-//                        entry lane, sum_h w*relu(D) in head order, coalesced
-//                        fp32 score stores.
+//                4 MMA warps, one per TMEM accumulator buffer (tile t goes
+//                        to buffer t mod 4): the warp gathers the tile's E8M0
+//                        bytes into the tcgen05 scale-factor atom, and one
+//                        lane issues tcgen05.cp of the scales and two
+//                        kind::mxf4 MMAs (K = 64 each) per 128-column N chunk;
+//                        A = 128 entries x 128 dims, B = rows*heads x 128
+//                        dims, D = fp32 [entry lane, row*head column].  A
+//                        single issuing thread spends hundreds of cycles per
+//                        tile on tcgen05 issue, so four run side by side.
+//                4 epilogue warp groups on the 4 buffers: per entry lane,
+//                        sum_h w*relu(D) with packed fp32x2 fused multiply-adds
+//                        (even and odd heads in the two halves, added at the
+//                        end), coalesced fp32 score stores.
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
@@ -42,11 +46,13 @@ struct Seg {
 };
 
 constexpr int kStages = 12;
-constexpr int kMaxBuf = 4;                     // TMEM accumulator buffers = epilogue groups
-constexpr int kProducers = 4;                  // producer warps: 0, 3 and the last two
-constexpr int kWarps = 4 + 4 * kMaxBuf + 2;
-constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxBuf = 4;                     // TMEM accumulator buffers = MMA warps = epilogue groups
+constexpr int kProducers = 4;                  // warps 0..3
+constexpr int kMmaWarp0 = kProducers;          // warps 4..7
+constexpr int kEpiWarp0 = kMmaWarp0 + kMaxBuf; // warps 8..23 (group g = warps 8+4g .. 8+4g+3)
 constexpr int kEpiWarps = 4 * kMaxBuf;
+constexpr int kWarps = kEpiWarp0 + kEpiWarps;
+constexpr int kThreads = 32 * kWarps;
 constexpr int kTileEntries = 128;
 constexpr int kStageA = 2 * IDX_PAGE;          // two whole pages = 16 groups of 544 B
 constexpr int kStageSF = 512;                  // scale-factor atom of 128 rows
@@ -55,7 +61,9 @@ constexpr int kQData = kMaxN * 64;   // 24576
 constexpr int kQSF = kMaxN * 4;      // 1536
 constexpr int kItemCap = 512;        // work items per table chunk
 constexpr int kMaxGroupRows = 64;    // rows per segment (kMaxN / 8 heads at least)
-constexpr int kTmemSFA = 0, kTmemSFB = 16, kTmemD = 48;
+// TMEM columns: A scale factors 4 per buffer; q scale factors 2 parities x
+// 3 atoms x 4; then the accumulator buffers.
+constexpr int kTmemSFA = 0, kTmemSFB = 16, kTmemD = kTmemSFB + 24;
 
 struct Item {
   int32_t seg, tile, pg0, pg1;       // local segment index, tile in segment, pages (-1: none)
@@ -70,9 +78,9 @@ struct ScoreSmem {
   Item items[kItemCap];
   Seg segs[kItemCap];
   int32_t pref[kItemCap + 1];
-  float wseg[kEpiWarps][kMaxN];
+  alignas(16) float wseg[kEpiWarps][kMaxN];    // row kr's w at kr * Hp (16-byte aligned rows)
   int32_t rown[kEpiWarps][kMaxGroupRows];
-  uint64_t full[kStages], empty[kStages], sfready[kStages];
+  uint64_t full[kStages], empty[kStages];
   uint64_t tfull[kMaxBuf], tempty[kMaxBuf];
   uint64_t qfull[2], qempty[2], qready[2];
   uint32_t tmem_base;
@@ -278,6 +286,21 @@ __device__ __forceinline__ void sf_to_atom(const uint8_t* raw, uint8_t* atom, in
   reinterpret_cast<uint4*>(atom)[lane] = v;
 }
 
+__device__ __forceinline__ float relu(uint32_t bits) { return fmaxf(__uint_as_float(bits), 0.0f); }
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+// d = a * b + c on both fp32 halves, each rounded once
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ScoreSmem& sm, uint32_t* status) {
   if (mbar_wait(bar, parity)) return true;
   raise_flag(status, CSA_FLAG_TIMEOUT);
@@ -285,8 +308,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sc
   return false;
 }
 
-__device__ __forceinline__ int producer_index(int warp) {
-  return warp == 0 ? 0 : (warp == 3 ? 1 : (warp >= kWarps - 2 ? warp - (kWarps - 2) + 2 : -1));
+// Whole-warp wait: lane 0 waits, the warp then agrees on the outcome, so a
+// time-out never leaves some lanes of a warp inside the loop and others out.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, ScoreSmem& sm, uint32_t* status) {
+  int ok = 1;
+  if (lane_id() == 0) ok = wait_or_abort(bar, parity, sm, status) ? 1 : 0;
+  __syncwarp();
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_t* ws) {
@@ -311,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
-      mbar_init(&sm.sfready[s], 1);
     }
     for (int d = 0; d < kMaxBuf; ++d) {
       mbar_init(&sm.tfull[d], 1);
@@ -319,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(&sm.qfull[d], 1);
-      mbar_init(&sm.qempty[d], 1);
+      mbar_init(&sm.qempty[d], nbuf);            // every active MMA warp leaves each segment once
       mbar_init(&sm.qready[d], 1);
     }
     sm.abort_flag = 0;
@@ -333,10 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
 
   // Role state kept across work chunks.  A segment's ordinal within this CTA
   // (ord) picks its q buffer (ord & 1) and the phases of the q barriers.
-  const int prod = producer_index(warp);
-  int f_s = 0, f_use = 0, f_ord = -1;                        // scale-factor warp
-  int m_ord = -1, m_par = 0, m_N = 0;                        // MMA issuer
-  int m_s = 0, m_use = 0, m_d = 0, m_round = 0;
+  const int prod = warp < kProducers ? warp : -1;
+  const int iss = warp - kMmaWarp0;                          // MMA warp index (buffer) when in [0, nbuf)
+  int m_ord = -1, m_par = 0, m_N = 0;                        // MMA warp state
+  uint64_t m_bdesc = 0;
+  uint32_t m_idesc0 = 0, m_idesc1 = 0;
+  int m_nchunks = 0;
   int e_gseg = -1, e_round = 0;                              // epilogue
   int last_ord = -1;                                         // ordinal of the previous chunk's last item
   int ord_base = 0;                                          // ordinal of this chunk's first segment
@@ -412,99 +441,94 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
         if (e.pg0 >= 0) bulk_load(sm.a[s], ipool + (size_t)e.pg0 * IDX_PAGE, IDX_PAGE, &sm.full[s]);
         if (e.pg1 >= 0) bulk_load(sm.a[s] + IDX_PAGE, ipool + (size_t)e.pg1 * IDX_PAGE, IDX_PAGE, &sm.full[s]);
       }
-    } else if (warp == 2) {
-      // ================= scale-factor warp =================
-      for (int i = 0; i < m; ++i) {
-        if (sm.abort_flag) break;
-        const Item e = sm.items[i];
-        const int ord = ord_base + e.seg;
-        if (ord != f_ord) {
-          const int par = ord & 1;
-          if (!wait_or_abort(&sm.qfull[par], (ord >> 1) & 1, sm, a.status)) break;
-          const int natoms = (sm.segs[e.seg].nrows * Hp + 127) / 128;
-          // rows past N inside the last atom hold stale bytes; their D columns are never read
-          for (int c = 0; c < natoms; ++c)
-            sf_to_atom(sm.sfb_raw[par] + 512 * c, sm.sfb_atom[par] + 512 * c, lane);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.qready[par]);
-          f_ord = ord;
-        }
-        if (!wait_or_abort(&sm.full[f_s], f_use & 1, sm, a.status)) break;
-        // entry row r of the tile: page r / 64, group (r % 64) / 8, scale word (r % 8)
-        const uint8_t* st = sm.a[f_s];
-        uint32_t wv[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = lane + 32 * j;
-          wv[j] = *reinterpret_cast<const uint32_t*>(st + (r >> 6) * IDX_PAGE + idx_scale_off(r & 63, 0));
-        }
-        reinterpret_cast<uint4*>(sm.sfa_atom[f_s])[lane] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.sfready[f_s]);
-        if (++f_s == kStages) {
-          f_s = 0;
-          ++f_use;
-        }
-      }
-    } else if (warp == 1 && lane == 0) {
-      // ================= MMA issuer (one thread) =================
+    } else if (iss >= 0 && iss < nbuf) {
+      // ================= MMA warp iss: items it with it % nbuf == iss =================
+      const uint64_t adesc0 = smem_desc(smem_u32(sm.a[0]), 128, IDX_GROUP, kSwizzleNone);
+      const uint32_t sfb_t = tmem + kTmemSFB;
       for (int i = 0; i < m; ++i) {
         if (sm.abort_flag) break;
         const Item e = sm.items[i];
         const int ord = ord_base + e.seg;
         if (ord != m_ord) {
-          // the previous segment's q buffer is free once its MMAs complete
-          if (m_ord >= 0) tc_commit(&sm.qempty[m_ord & 1]);
+          // leaving a segment: its q buffer is free once this warp's MMAs complete
+          if (m_ord >= 0 && lane == 0) tc_commit(&sm.qempty[m_ord & 1]);
           m_par = ord & 1;
-          if (!wait_or_abort(&sm.qready[m_par], (ord >> 1) & 1, sm, a.status)) break;
+          if (!warp_wait(&sm.qfull[m_par], (ord >> 1) & 1, sm, a.status)) break;
           m_N = sm.segs[e.seg].nrows * Hp;
           const int natoms = (m_N + 127) / 128;
-          tc_fence_after();
-          for (int c = 0; c < natoms; ++c)
-            tmem_cp_32x128b_x4(tmem + kTmemSFB + 12 * m_par + 4 * c,
-                               smem_desc(smem_u32(sm.sfb_atom[m_par] + 512 * c), 16, 128, kSwizzleNone));
+          if (ord % nbuf == iss) {
+            // one warp per segment lays the q scales out as atoms and copies them
+            // to TMEM; the commit tells the other MMA warps the copy has landed.
+            // Rows past N inside the last atom hold stale bytes; their D columns
+            // are never read.
+            for (int c = 0; c < natoms; ++c)
+              sf_to_atom(sm.sfb_raw[m_par] + 512 * c, sm.sfb_atom[m_par] + 512 * c, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tc_fence_after();
+              for (int c = 0; c < natoms; ++c)
+                tmem_cp_32x128b_x4(sfb_t + 12 * m_par + 4 * c,
+                                   smem_desc(smem_u32(sm.sfb_atom[m_par] + 512 * c), 16, 128, kSwizzleNone));
+              tc_commit(&sm.qready[m_par]);
+            }
+            __syncwarp();
+          }
+          if (!warp_wait(&sm.qready[m_par], (ord >> 1) & 1, sm, a.status)) break;
+          const int Nm = mma_n(m_N);
+          m_nchunks = (Nm + 127) / 128;
+          m_bdesc = smem_desc(smem_u32(sm.qdata[m_par]), 16, 512, kSwizzle64B);
+          const uint32_t n_last = (uint32_t)(Nm - 128 * (m_nchunks - 1));   // N of the last chunk
+          m_idesc0 = idesc_mxf4(128, n_last, 0, 0);
+          m_idesc1 = idesc_mxf4(128, n_last, 2, 2);
           m_ord = ord;
         }
-        if (!wait_or_abort(&sm.sfready[m_s], m_use & 1, sm, a.status)) break;
-        if (m_round > 0 && !wait_or_abort(&sm.tempty[m_d], (m_round - 1) & 1, sm, a.status)) break;
-        tc_fence_after();
-        const uint32_t sfa = tmem + kTmemSFA + 4 * m_d;
-        tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[m_s]), 16, 128, kSwizzleNone));
-        // A: the two pages as they landed: 8-entry groups IDX_GROUP apart, 16-byte
-        // core matrices 128 B apart along K (no swizzle); second K half at +256 B
-        const uint32_t abase = smem_u32(sm.a[m_s]);
-        const uint32_t bbase = smem_u32(sm.qdata[m_par]);
-        const uint32_t dcol = tmem + kTmemD + m_d * dstride;
-        const int Nm = mma_n(m_N);
-        for (int c = 0; c * 128 < Nm; ++c) {
-          const uint32_t Nc = (uint32_t)min(128, Nm - c * 128);
-          const uint32_t sfb = tmem + kTmemSFB + 12 * m_par + 4 * c;
-          const uint32_t bchunk = bbase + c * 128 * 64;
-          mma_mxf4(dcol + c * 128, smem_desc(abase, 128, IDX_GROUP, kSwizzleNone),
-                   smem_desc(bchunk, 16, 512, kSwizzle64B), idesc_mxf4(128, Nc, 0, 0), sfa, sfb, 0u);
-          mma_mxf4(dcol + c * 128, smem_desc(abase + 256, 128, IDX_GROUP, kSwizzleNone),
-                   smem_desc(bchunk + 32, 16, 512, kSwizzle64B), idesc_mxf4(128, Nc, 2, 2), sfa, sfb, 1u);
+        const int it = it_base + i;
+        if (it % nbuf != iss) continue;
+        const int s = it % kStages, use = it / kStages, round = it / nbuf;
+        if (!warp_wait(&sm.full[s], use & 1, sm, a.status)) break;
+        // entry row r of the tile: page r / 64, group (r % 64) / 8, scale word (r % 8)
+        {
+          const uint8_t* st = sm.a[s];
+          uint32_t wv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = lane + 32 * j;
+            wv[j] = *reinterpret_cast<const uint32_t*>(st + (r >> 6) * IDX_PAGE + idx_scale_off(r & 63, 0));
+          }
+          reinterpret_cast<uint4*>(sm.sfa_atom[s])[lane] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
-        tc_commit(&sm.empty[m_s]);
-        tc_commit(&sm.tfull[m_d]);
-        if (++m_s == kStages) {
-          m_s = 0;
-          ++m_use;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (round > 0 && !warp_wait(&sm.tempty[iss], (round - 1) & 1, sm, a.status)) break;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sfa = tmem + kTmemSFA + 4 * iss;
+          tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[s]), 16, 128, kSwizzleNone));
+          // A: the two pages as they landed: 8-entry groups IDX_GROUP apart, 16-byte
+          // core matrices 128 B apart along K (no swizzle); second K half at +256 B
+          const uint64_t ad = adesc0 + (uint64_t)(s * (kStageA >> 4));
+          const uint32_t dcol = tmem + kTmemD + iss * dstride;
+          for (int c = 0; c < m_nchunks; ++c) {
+            const uint32_t sfb = sfb_t + 12 * m_par + 4 * c;
+            const uint64_t bd = m_bdesc + (uint64_t)(c * (128 * 64 >> 4));
+            const uint32_t id0 = (c + 1 < m_nchunks) ? idesc_mxf4(128, 128, 0, 0) : m_idesc0;
+            const uint32_t id1 = (c + 1 < m_nchunks) ? idesc_mxf4(128, 128, 2, 2) : m_idesc1;
+            mma_mxf4(dcol + c * 128, ad, bd, id0, sfa, sfb, 0u);
+            mma_mxf4(dcol + c * 128, ad + 16, bd + 2, id1, sfa, sfb, 1u);
+          }
+          tc_commit(&sm.empty[s]);
+          tc_commit(&sm.tfull[iss]);
         }
-        if (++m_d == nbuf) {
-          m_d = 0;
-          ++m_round;
-        }
+        __syncwarp();
       }
-    } else if (warp >= 4 && warp < 4 + kEpiWarps && ((warp - 4) >> 2) < nbuf) {
+    } else if (warp >= kEpiWarp0 && ((warp - kEpiWarp0) >> 2) < nbuf) {
       // ================= epilogue group grp =================
-      const int grp = (warp - 4) >> 2;
+      const int grp = (warp - kEpiWarp0) >> 2;
       const int q = warp & 3;                       // TMEM lane quarter of this warp
       const int mrow = 32 * q + lane;               // entry within the tile
-      float* ew = sm.wseg[warp - 4];                // this warp's copy of the segment's w
-      int32_t* en = sm.rown[warp - 4];              // and of its rows' visible lengths
+      float* ew = sm.wseg[warp - kEpiWarp0];        // this warp's copy of the segment's w
+      int32_t* en = sm.rown[warp - kEpiWarp0];      // and of its rows' visible lengths
       int i = grp - (it_base % nbuf);
       if (i < 0) i += nbuf;
       for (; i < m; i += nbuf) {
@@ -514,28 +538,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
         const int gseg = seg0 + e.seg;
         if (gseg != e_gseg) {                       // stage this segment's weights and row lengths
           __syncwarp();                             // (per warp: no cross-warp barrier here)
-          for (int x = lane; x < sg.nrows * Hi; x += 32) ew[x] = __ldg(a.w + (size_t)sg.r0 * Hi + x);
+          for (int x = lane; x < sg.nrows * Hi; x += 32) ew[(x / Hi) * Hp + x % Hi] = __ldg(a.w + (size_t)sg.r0 * Hi + x);
           for (int x = lane; x < sg.nrows; x += 32) en[x] = (__ldg(a.row_pos + sg.r0 + x) + 1) / a.P;
           __syncwarp();
           e_gseg = gseg;
         }
-        if (!wait_or_abort(&sm.tfull[grp], e_round & 1, sm, a.status)) break;
+        if (!warp_wait(&sm.tfull[grp], e_round & 1, sm, a.status)) break;
         tc_fence_after();
         const int ient = e.tile * kTileEntries + mrow;
         const bool page_ok = (mrow < 64) ? (e.pg0 >= 0) : (e.pg1 >= 0);
         const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + kTmemD + grp * dstride;
         for (int kr = 0; kr < sg.nrows; ++kr) {
-          const float* wr = ew + kr * Hi;
-          float acc = 0.0f;
+          const float* wr = ew + kr * Hp;
+          uint64_t acc2 = 0ull;                     // (even heads, odd heads) partial sums, +0.0f each
+          float acc1 = 0.0f;                        // heads past the last full group of 32
           int h0 = 0;
           for (; h0 + 32 <= Hi; h0 += 32) {
             uint32_t v[32];
             tmem_ld32(dbase + kr * Hp + h0, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float dot = __uint_as_float(v[j]);
-              acc = __fadd_rn(acc, __fmul_rn(wr[h0 + j], dot > 0.0f ? dot : 0.0f));
+            for (int j = 0; j < 32; j += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wr + h0 + j);
+              acc2 = ffma2(pack2(w4.x, w4.y), pack2(relu(v[j]), relu(v[j + 1])), acc2);
+              acc2 = ffma2(pack2(w4.z, w4.w), pack2(relu(v[j + 2]), relu(v[j + 3])), acc2);
             }
           }
           for (; h0 < Hi; h0 += 16) {
@@ -543,13 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
             tmem_ld16(dbase + kr * Hp + h0, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (h0 + j < Hi) {
-                const float dot = __uint_as_float(v[j]);
-                acc = __fadd_rn(acc, __fmul_rn(wr[h0 + j], dot > 0.0f ? dot : 0.0f));
-              }
-            }
+            for (int j = 0; j < 16; ++j)
+              if (h0 + j < Hi) acc1 = fmaf(wr[h0 + j], relu(v[j]), acc1);
           }
+          const float acc = (lo_f32(acc2) + hi_f32(acc2)) + acc1;
           if (ient < en[kr] && ient < sg.n)
             a.scores[(size_t)(sg.r0 + kr) * a.ld + ient] = page_ok ? acc : -INFINITY;
         }

@@ -104,16 +104,23 @@ def test_index_score_matches_oracle(Hi, rows):
     ref = oracle.build_cache(wl)
     q_idx, w, _ = wl.step_queries()
     ref_sc = oracle.index_score(ref, wl.row_req, wl.row_pos, q_idx, w, ld)
+    # sum_h |w_h| relu(q_h . k): the scale of the fp32 rounding in either sum
+    mag = oracle.index_score(ref, wl.row_req, wl.row_pos, q_idx, np.abs(w), ld)
+    # The score is sum_h w_h * relu(q_h . k) (the pages fix no summation order
+    # or fusing); the oracle adds products in head order, the kernel uses fused
+    # multiply-adds on even/odd head pairs.  Each fp32 sum of Hi terms is within
+    # gamma_(Hi+1) * mag of the exact value, so the two are within twice that.
+    u = 2.0 ** -24
+    tol_f = 2.0 * (Hi + 1) * u / (1.0 - (Hi + 1) * u)
     got = scores.cpu().numpy()
     n = wl.row_entries()
-    exact = total = 0
     for r in range(wl.R):
-        g, o = got[r, :n[r]], ref_sc[r, :n[r]]
-        np.testing.assert_allclose(g, o, rtol=1e-6, atol=0)
-        exact += int((g == o).sum())
-        total += int(n[r])
+        g, o, m = got[r, :n[r]], ref_sc[r, :n[r]], mag[r, :n[r]]
+        fin = np.isfinite(o)
+        assert np.array_equal(np.isfinite(g), fin) and np.array_equal(g[~fin], o[~fin]), r
+        err = np.abs(g[fin].astype(np.float64) - o[fin].astype(np.float64))
+        assert (err <= tol_f * m[fin].astype(np.float64)).all(), (r, float((err / np.maximum(m[fin], 1e-30)).max()))
         assert np.isnan(got[r, n[r]:]).all(), "scores past the visible range must be untouched"
-    assert exact >= 0.99 * total, (exact, total)
 
 
 def test_identical_entries_score_identically():
