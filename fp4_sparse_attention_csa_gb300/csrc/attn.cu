@@ -353,6 +353,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const bool win_here = hw && t_beg == 0 && t_end > 0;
   const int m_beg = max(t_beg - hw, 0), m_end = max(t_end - hw, 0);   // main tiles [m_beg, m_end)
 
+  // ---- prologue, overlapping the previous kernel's tail: barriers, TMEM;
+  // then wait for it (the selected indices, and transitively the cache
+  // append of this step, are ready from there on)
+  pdl_trigger();
+  if (tid == 0) {
+    mbar_init(&sm.s_bar, 1);
+    mbar_init(&sm.pv_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(&sm.tmem_base, 512);
+  pdl_wait();
+
   // ---- setup.  The window tile's loads go out first (they need no lookup);
   // the selected entries are looked up (index, then page) while Q is loaded,
   // and every entry's bytes are prefetched into L2 at once, so the per-tile
@@ -412,12 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     sm.m_buf[1][tid] = -INFINITY;
     sm.l_run[tid] = 0.0f;
   }
-  if (tid == 0) {
-    mbar_init(&sm.s_bar, 1);
-    mbar_init(&sm.pv_bar, 1);
-    fence_barrier_init();
-  }
-  if (warp == 0) tmem_alloc(&sm.tmem_base, 512);
   __syncthreads();                                // entry table visible
   if (!win_here && m_beg < m_end) gather_main(a, sm, m_beg, key, gq, cur);
   fence_proxy_async_smem();
@@ -661,6 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
 
 // Log-sum-exp merge of the split partials: one block per (row, head).
 __global__ void __launch_bounds__(128) k_attn_merge(AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();                    // the partials come from the previous kernel
   const int r = blockIdx.x / a.H, h = blockIdx.x % a.H;
   const int H = a.H, S = a.splits;
   const float* base = a.part + (size_t)r * S * H * (D + 2);
@@ -690,11 +698,9 @@ cudaError_t launch_h(const AttnArgs& a, cudaStream_t stream) {
   const size_t smem = sizeof(AttnSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(k_sparse_attn<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_sparse_attn<H><<<a.num_rows * a.splits, kThreads, smem, stream>>>(a);
-  e = cudaGetLastError();
+  e = launch_dependent(k_sparse_attn<H>, dim3(a.num_rows * a.splits), dim3(kThreads), smem, stream, a);
   if (e != cudaSuccess || a.splits == 1) return e;
-  k_attn_merge<<<a.num_rows * a.H, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(k_attn_merge, dim3(a.num_rows * a.H), dim3(128), 0, stream, a);
 }
 
 }  // namespace

@@ -137,6 +137,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// Programmatic dependent launch.  pdl_wait: block until the previous kernel
+// in the stream has completed and its writes are visible (a no-op when the
+// kernel was launched without the attribute).  pdl_trigger: let the next
+// kernel in the stream start its prologue now; it still waits for this
+// kernel's completion before it reads what this kernel writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // The suspend-time hint lets a waiting thread sleep until the phase completes
 // (or the hint, in ns, runs out) instead of spinning: spinning warps would take
 // issue slots from the warps doing the work.

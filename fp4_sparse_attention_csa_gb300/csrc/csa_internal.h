@@ -8,6 +8,26 @@
 
 namespace csa {
 
+// Launch with programmatic dependent launch: the kernel may start while the
+// previous kernel in the stream is still running; it runs its prologue, then
+// griddepcontrol.wait (pdl_wait) blocks until that kernel has completed and
+// its memory is visible, before anything it produced is read.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 struct AppendArgs {
   uint8_t* kv_pool;
   uint8_t* idx_pool;

@@ -153,7 +153,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* sm_w
   return off + x - v;
 }
 
+// Reads only the step's inputs, so it may run beside the cache append; it
+// waits for the previous kernel before it exits, so that everything after it
+// also sees that kernel's writes.
 __global__ void __launch_bounds__(128) k_score_prep(ScoreArgs a, uint8_t* ws) {
+  pdl_trigger();
   const int R = a.num_rows, Hi = a.Hi, Hp = hi_pad(Hi);
   ScoreWs W = carve_score_ws(ws, R, Hi);
   if (blockIdx.x == 0) {
@@ -230,6 +234,7 @@ __global__ void __launch_bounds__(128) k_score_prep(ScoreArgs a, uint8_t* ws) {
       }
       W.cta_seg[g] = seg;
     }
+    pdl_wait();
     return;
   }
   // ---- MXFP4 quantisation of row r's indexer queries into the MMA B image.
@@ -271,6 +276,7 @@ __global__ void __launch_bounds__(128) k_score_prep(ScoreArgs a, uint8_t* ws) {
     *reinterpret_cast<uint4*>(W.qimg + n * 64 + sw * 16) = out;
     W.qsf[n * 4 + kb] = (uint8_t)E8;
   }
+  pdl_wait();
 }
 
 // Rearrange 4-byte scale words of up to 128 rows into the tcgen05 scale-factor
@@ -324,10 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
   ScoreWs W = carve_score_ws(ws, a.num_rows, Hi);
   const int warp = warp_id(), lane = lane_id(), tid = threadIdx.x;
   const uint8_t* ipool = static_cast<const uint8_t*>(a.idx_pool);
-
-  const int S = W.nseg[0], total = W.nseg[1];
-  const int per = (total + gridDim.x - 1) / gridDim.x;
-  const int beg = min(total, (int)blockIdx.x * per), end = min(total, beg + per);
+  pdl_trigger();
 
   // TMEM: scale factors in columns [0, 48), accumulator buffer d at
   // kTmemD + d * dstride; one epilogue warp group per buffer.
@@ -357,6 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  pdl_wait();                    // the segment table, q image and pages are ready from here on
+
+  const int S = W.nseg[0], total = W.nseg[1];
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  const int beg = min(total, (int)blockIdx.x * per), end = min(total, beg + per);
 
   // Role state kept across work chunks.  A segment's ordinal within this CTA
   // (ord) picks its q buffer (ord & 1) and the phases of the q barriers.
@@ -615,14 +623,12 @@ cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, cudaStream_t str
   uint8_t* ws = reinterpret_cast<uint8_t*>(a.status);
   ScoreArgs ap = a;
   ap.grid = num_sms < kMaxGrid ? num_sms : kMaxGrid;
-  k_score_prep<<<1 + a.num_rows, 128, 0, stream>>>(ap, ws);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(k_score_prep, dim3(1 + a.num_rows), dim3(128), 0, stream, ap, ws);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(ScoreSmem) + 1024;
   e = cudaFuncSetAttribute(k_index_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_index_score<<<ap.grid, kThreads, smem, stream>>>(ap, ws);
-  return cudaGetLastError();
+  return launch_dependent(k_index_score, dim3(ap.grid), dim3(kThreads), smem, stream, ap, ws);
 }
 
 }  // namespace csa

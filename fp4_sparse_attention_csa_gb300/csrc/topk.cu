@@ -120,6 +120,8 @@ __device__ void radix_select_block(const uint32_t* keys, int m, uint32_t need, T
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int slice_cap, int staged) {
+  pdl_trigger();
+  pdl_wait();                    // the scores come from the previous kernel
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) uint8_t smem[];
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem);
@@ -438,6 +440,8 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, RowS
 }
 
 __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
+  pdl_trigger();
+  pdl_wait();                    // the scores come from the previous kernel
   extern __shared__ __align__(16) uint8_t smem[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
   const int r = blockIdx.x;
@@ -711,8 +715,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
     const size_t smem = sizeof(RowSmem);
     cudaError_t e = cudaFuncSetAttribute(k_topk_row, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_topk_row<<<a.num_rows, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(k_topk_row, dim3(a.num_rows), dim3(kThreads), smem, stream, a);
   }
   int C = (a.max_n + kStageMax - 1) / kStageMax;
   C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
@@ -729,13 +732,15 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_topk, a, C, slice_cap, staged);
 }
 
