@@ -7,20 +7,23 @@
 //   invalid-position filtering is fused with the selection (rows with n <= 512
 //   return every visible index, the rest of the row is -1).
 //
-// One thread-block cluster of C CTAs per row; CTA k owns a contiguous slice of
-// the row, staged in shared memory as order-preserving uint32 keys (-0 folded
-// onto +0).  The 512th-largest key T is found in two steps:
-//   1. a 4096-bin histogram in *value* space between the row's min and max
-//      (binning is monotone, so every key in a higher bin is larger); the
-//      cluster sums the C histograms through distributed shared memory and
-//      finds the bin holding rank 512;
-//   2. that bin's keys (usually a handful) are gathered into CTA 0, which runs
-//      a radix select over them for the exact key T.
-// If the bin holds more than kCandCap keys, or the value range is not finite,
-// a three-pass radix select over all keys (11/11/10 bits) is used instead.
-// A final index-ordered ballot compaction writes every key > T and the
-// lowest-index keys == T until 512 are taken.  Cluster barriers are hardware
-// barriers, so there is no spin-wait here.
+// Two kernels, both one thread-block cluster per row:
+//  k_topk_row  rows up to 128K entries (every decode shape but the unpooled
+//              long context): C <= 8 CTAs per row stream slices of the
+//              L2-resident row; value range and value histogram are combined
+//              over distributed shared memory, the entries in or above the
+//              bin of rank 512 are compacted in row order into CTA 0, which
+//              finds the exact 512th key and the ties' cut on that list.
+//  k_topk      longer rows: C CTAs per row with each slice staged in shared
+//              memory as order-preserving uint32 keys (-0 folded onto +0); a
+//              4096-bin value-space histogram summed over the cluster finds
+//              the bin of rank 512, whose keys are gathered into CTA 0 for a
+//              radix select of the exact key T.
+// In both, a candidate list that overflows (many ties at the cut) or a
+// non-finite value range falls back to a three-pass radix select over all
+// keys (11/11/10 bits), and an index-ordered compaction writes every key > T
+// and the lowest-index keys == T until 512 are taken.  Cluster barriers are
+// hardware barriers, so there is no spin-wait here.
 #include <cooperative_groups.h>
 
 #include "csa_device.cuh"
@@ -372,21 +375,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int sli
 }
 
 // ---------------------------------------------------------------------------
-// One CTA per row (rows up to kRowMax entries): the row is streamed from L2
-// with 16-byte loads -- value range, a kRowBins-bin value histogram, then every
-// entry at or above the threshold bin is compacted, in index order, into a
-// candidate list in shared memory, where the exact 512th key and the output
-// are resolved.  Shared memory stays small, so several rows run per SM.
-constexpr int kRowMax = 65536;
+// Rows up to kRowMax entries: a cluster of C CTAs per row (C set at launch),
+// CTA k streaming the contiguous slice [k*S, min(n, (k+1)*S)) of the
+// L2-resident row with 16-byte loads (S a multiple of 4).  The cluster
+//   1. reduces the slices' value ranges through distributed shared memory,
+//   2. sums the CTAs' kRowBins-bin value histograms (read remotely) and finds
+//      the bin holding rank 512; every CTA derives the same bin and each
+//      CTA's count of entries in or above it, hence its offset,
+//   3. each CTA compacts its slice's entries in or above that bin, in index
+//      order, straight into CTA 0's candidate list at its offset, so the list
+//      is in row order,
+// and CTA 0 resolves the exact 512th key and the ties' cut on the list.  A
+// list longer than kRowCap (many ties at the cut) or a non-finite range falls
+// back to a whole-row radix select in CTA 0.  A CTA leaves only after a
+// cluster barrier that follows every remote read of its shared memory.
+constexpr int kRowMax = 131072;
 constexpr int kRowBins = 2048;
 constexpr int kRowCap = 4096;
+constexpr int kRowCluster = 8;
 
 struct alignas(16) RowSmem {
-  uint32_t hist[kBins];            // kRowBins used by the value pass; radix passes use 2048
-  uint32_t cand_key[kRowCap];
+  uint32_t hist[kRowBins];         // value histogram; the radix passes reuse it
+  uint32_t cand_key[kRowCap];      // CTA 0: the row's candidates, row order
   int32_t cand_idx[kRowCap];
   uint32_t warp_a[kWarps], warp_b[kWarps];
-  uint32_t cnt, sel_bin, sel_need, T, take, fallback;
+  uint32_t part[kWarps][kRowCluster];
+  uint32_t cnt[kRowCluster];       // entries in or above the cut bin, per CTA
+  uint32_t sel_bin, sel_need;
   float fmin, fmax;
 };
 
@@ -412,8 +427,6 @@ __device__ __forceinline__ void block_minmax(float& vmin, float& vmax, RowSmem& 
     sm.fmax = b0;
   }
   __syncthreads();
-  vmin = sm.fmin;
-  vmax = sm.fmax;
 }
 
 // Block-wide exclusive scan of one count per thread; returns the thread's
@@ -442,34 +455,41 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, RowS
 __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
   pdl_trigger();
   pdl_wait();                    // the scores come from the previous kernel
+  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) uint8_t smem[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
-  const int r = blockIdx.x;
+  const int C = (int)cluster.num_blocks();
+  const int kq = (int)cluster.block_rank();
+  const int r = blockIdx.x / C;
   const int tid = threadIdx.x;
   const float* row = a.scores + (size_t)r * a.ld;
   int32_t* out = a.out + (size_t)r * TOPK;
 
   int n = a.n_valid ? __ldg(a.n_valid + r) : (__ldg(a.row_pos + r) + 1) / a.P;
   if (n < 0 || n > a.max_n) {
-    if (tid == 0) raise_flag(a.status, CSA_FLAG_ROW_INVALID);
+    if (tid == 0 && kq == 0) raise_flag(a.status, CSA_FLAG_ROW_INVALID);
     n = n < 0 ? 0 : a.max_n;
   }
-  if (n <= TOPK) {
-    for (int i = tid; i < TOPK; i += kThreads) out[i] = i < n ? i : -1;
+  if (n <= TOPK) {                 // the same branch in every CTA of the cluster
+    if (kq == 0)
+      for (int i = tid; i < TOPK; i += kThreads) out[i] = i < n ? i : -1;
     return;
   }
-  const float4* row4 = reinterpret_cast<const float4*>(row);
-  const int n4 = n >> 2;
+  const int S = (((n + C - 1) / C) + 3) & ~3;
+  const int lo = min(n, kq * S), len = min(n, lo + S) - lo;
+  const float* sl = row + lo;
+  const float4* sl4 = reinterpret_cast<const float4*>(sl);   // lo is a multiple of 4
+  const int n4 = len >> 2;
   auto fold = [](float v) { return v == 0.0f ? 0.0f : v; };   // -0 onto +0
 
-  // ---- pass 1: value range (four 16-byte loads in flight per thread) ---------------
+  // ---- pass 1: value range of the slice, then of the row ----------------------------
   float vmin = INFINITY, vmax = -INFINITY;
   for (int b0 = tid; b0 < n4; b0 += 4 * kThreads) {
     float4 v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = b0 + j * kThreads;
-      v[j] = i < n4 ? __ldg(row4 + i) : make_float4(vmax, vmax, vmax, vmax);
+      v[j] = i < n4 ? __ldg(sl4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -479,21 +499,25 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
       }
     }
   }
-  for (int i = 4 * n4 + tid; i < n; i += kThreads) {
-    const float v = __ldg(row + i);
+  for (int i = 4 * n4 + tid; i < len; i += kThreads) {
+    const float v = __ldg(sl + i);
     vmin = fminf(vmin, v);
     vmax = fmaxf(vmax, v);
   }
   for (int i = tid; i < kRowBins; i += kThreads) sm.hist[i] = 0u;
   block_minmax(vmin, vmax, sm);
+  cluster.sync();                                  // every slice's range is published
+  vmin = INFINITY;
+  vmax = -INFINITY;
+  for (int q = 0; q < C; ++q) {
+    const RowSmem* rs = cluster.map_shared_rank(&sm, q);
+    vmin = fminf(vmin, rs->fmin);
+    vmax = fmaxf(vmax, rs->fmax);
+  }
   vmin = fold(vmin);
   vmax = fold(vmax);
   const float range = vmax - vmin;
-  if (range == 0.0f) {             // all equal: the lowest 512 indices
-    for (int i = tid; i < TOPK; i += kThreads) out[i] = i;
-    return;
-  }
-  const bool binning = isfinite(range) && isfinite((float)kRowBins / range);
+  const bool binning = range != 0.0f && isfinite(range) && isfinite((float)kRowBins / range);
   const float scale = binning ? (float)kRowBins / range : 0.0f;
   auto bin_of = [&](float v) -> int {
     const int b = (int)((fold(v) - vmin) * scale);
@@ -503,13 +527,13 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
   uint32_t T = 0, take = 0;
   bool done = false;
   if (binning) {
-    // ---- pass 2: histogram --------------------------------------------------------
+    // ---- pass 2: histogram of the slice ---------------------------------------------
     for (int b0 = tid; b0 < n4; b0 += 4 * kThreads) {
       float4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int i = b0 + j * kThreads;
-        v[j] = i < n4 ? __ldg(row4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        v[j] = i < n4 ? __ldg(sl4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -521,74 +545,112 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
         }
       }
     }
-    for (int i = 4 * n4 + tid; i < n; i += kThreads) atomicAdd(&sm.hist[bin_of(__ldg(row + i))], 1u);
-    __syncthreads();
-    // find the bin of rank 512 (uses the cluster kernel's helper on a one-CTA view)
-    {
-      const int lane = lane_id(), warp = warp_id();
-      constexpr int per = kRowBins / kThreads;
-      uint32_t c[per], mine = 0;
-#pragma unroll
-      for (int j = 0; j < per; ++j) {
-        c[j] = sm.hist[per * tid + j];
-        mine += c[j];
-      }
-      uint32_t incl = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
-        if (lane + o < 32) incl += y;
-      }
-      if (lane == 0) sm.warp_a[warp] = incl;
-      __syncthreads();
-      uint32_t acc = incl - mine;
-      for (int w2 = warp + 1; w2 < kWarps; ++w2) acc += sm.warp_a[w2];
-#pragma unroll
-      for (int j = per - 1; j >= 0; --j) {
-        if (acc < (uint32_t)TOPK && acc + c[j] >= (uint32_t)TOPK) sm.sel_bin = (uint32_t)(per * tid + j);
-        acc += c[j];
-      }
-      __syncthreads();
+    for (int i = 4 * n4 + tid; i < len; i += kThreads) atomicAdd(&sm.hist[bin_of(__ldg(sl + i))], 1u);
+  }
+  cluster.sync();                                  // histograms complete; range reads done
+  if (!binning) {
+    if (kq != 0) return;           // CTA 0 alone: all equal, or the whole-row radix below
+    if (range == 0.0f) {           // all equal: the lowest 512 indices
+      for (int i = tid; i < TOPK; i += kThreads) out[i] = i;
+      return;
     }
+  } else {
+    // ---- the bin of rank 512 in the summed histogram --------------------------------
+    const int lane = lane_id(), warp = warp_id();
+    constexpr int per = kRowBins / kThreads;
+    uint32_t c[per], mine = 0;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      uint32_t t = 0;
+      for (int q = 0; q < C; ++q) t += cluster.map_shared_rank(sm.hist, q)[per * tid + j];
+      c[j] = t;
+      mine += t;
+    }
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    if (lane == 0) sm.warp_a[warp] = incl;
+    __syncthreads();
+    uint32_t acc = incl - mine;
+    for (int w2 = warp + 1; w2 < kWarps; ++w2) acc += sm.warp_a[w2];
+#pragma unroll
+    for (int j = per - 1; j >= 0; --j) {
+      if (acc < (uint32_t)TOPK && acc + c[j] >= (uint32_t)TOPK) sm.sel_bin = (uint32_t)(per * tid + j);
+      acc += c[j];
+    }
+    __syncthreads();
     const int tb = (int)sm.sel_bin;
-    uint32_t above = 0;            // entries in bins >= tb: the candidate list
-    for (int b = tid; b < kRowBins; b += kThreads) above += (b >= tb) ? sm.hist[b] : 0u;
-    uint32_t m_total;
-    (void)block_scan(above, &m_total, sm);
-    if (m_total <= (uint32_t)kRowCap) {
-      // ---- pass 3: compact entries with bin >= tb, in index order; each thread
-      // takes a run of 16 consecutive entries per chunk -------------------------------
-      uint32_t base = 0;
-      for (int c0 = 0; c0 < n; c0 += 16 * kThreads) {
+    // each CTA's count of entries in bins >= tb, from its own histogram
+    uint32_t pc[kRowCluster];
+#pragma unroll
+    for (int q = 0; q < kRowCluster; ++q) pc[q] = 0u;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      const int bb = per * tid + j;
+      if (bb >= tb)
+        for (int q = 0; q < C; ++q) pc[q] += cluster.map_shared_rank(sm.hist, q)[bb];
+    }
+#pragma unroll
+    for (int q = 0; q < kRowCluster; ++q) {
+      uint32_t x = pc[q];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+      if (lane == 0) sm.part[warp][q] = x;
+    }
+    __syncthreads();
+    if (tid < C) {
+      uint32_t t = 0;
+      for (int w2 = 0; w2 < kWarps; ++w2) t += sm.part[w2][tid];
+      sm.cnt[tid] = t;
+    }
+    __syncthreads();
+    uint32_t m_total = 0, pre = 0;
+    for (int q = 0; q < C; ++q) {
+      if (q < kq) pre += sm.cnt[q];
+      m_total += sm.cnt[q];
+    }
+    cluster.sync();                                // every remote histogram read is done
+    if (m_total > (uint32_t)kRowCap) {
+      if (kq != 0) return;         // CTA 0 alone: the whole-row radix below
+    } else {
+      // ---- pass 3: compact entries with bin >= tb, in index order, into CTA 0 -------
+      uint32_t* dkey = cluster.map_shared_rank(sm.cand_key, 0);
+      int32_t* didx = cluster.map_shared_rank(sm.cand_idx, 0);
+      uint32_t base = pre;
+      for (int c0 = 0; c0 < len; c0 += 16 * kThreads) {
         const int i0 = c0 + 16 * tid;
         float v[16];
-        if (i0 + 15 < n) {
+        if (i0 + 15 < len) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float4 x = __ldg(row4 + (i0 >> 2) + q);
+            const float4 x = __ldg(sl4 + (i0 >> 2) + q);
             v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = i0 + j < n ? __ldg(row + i0 + j) : vmin;
+          for (int j = 0; j < 16; ++j) v[j] = i0 + j < len ? __ldg(sl + i0 + j) : vmin;
         }
         uint32_t bits = 0;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (i0 + j < n && bin_of(v[j]) >= tb) bits |= 1u << j;
+          if (i0 + j < len && bin_of(v[j]) >= tb) bits |= 1u << j;
         uint32_t tot;
         uint32_t off = base + block_scan((uint32_t)__popc(bits), &tot, sm);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           if (bits & (1u << j)) {
-            sm.cand_key[off] = score_key(fold(v[j]));
-            sm.cand_idx[off] = i0 + j;
+            dkey[off] = score_key(fold(v[j]));
+            didx[off] = lo + i0 + j;
             ++off;
           }
         }
         base += tot;
       }
-      __syncthreads();
+      cluster.sync();                              // the row's list is complete in CTA 0
+      if (kq != 0) return;
       // ---- exact 512th key among the candidates ----------------------------------
       const int m = (int)m_total;
       {
@@ -712,10 +774,36 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;
   if (a.max_n <= kRowMax && (a.ld % 4) == 0 && ((uintptr_t)a.scores & 15u) == 0) {
-    const size_t smem = sizeof(RowSmem);
-    cudaError_t e = cudaFuncSetAttribute(k_topk_row, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // CTAs per row: about one per 8K entries, up to 8, and at most two CTAs
+    // per SM over the grid (measured on the serving batch: 2 per row 29 us,
+    // 1 per row 34 us, 4 per row 48 us)
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    return launch_dependent(k_topk_row, dim3(a.num_rows), dim3(kThreads), smem, stream, a);
+    int C = (a.max_n + 8191) / 8192;
+    C = C < 1 ? 1 : (C > kRowCluster ? kRowCluster : C);
+    while (C > 1 && (long long)a.num_rows * C > 2LL * sms) --C;
+    const size_t smem = sizeof(RowSmem);
+    e = cudaFuncSetAttribute(k_topk_row, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_topk_row, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_rows * C, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_topk_row, a);
   }
   int C = (a.max_n + kStageMax - 1) / kStageMax;
   C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
