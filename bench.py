@@ -166,6 +166,17 @@ def run_reference(args, wl, cfg):
     print(json.dumps(line), flush=True)
 
 
+def job_throughput(total_ms, rows_per_step, steps, world, dist=None, device="cpu"):
+    """Whole-job rows/s with replicas: every rank's rows over the slowest rank's
+    time (max over ranks of the timed region)."""
+    if dist is not None:
+        import torch
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, rows_per_step * steps * world / (total_ms / 1e3)
+
+
 def cpu_baseline(wl, rows_cap, budget_s=20.0):
     import oracle
     oracle.build()
@@ -256,13 +267,7 @@ def main():
         dist.barrier()
     clocks = sampler.stop()
     step_ms = np.array([a.elapsed_time(b) for a, b in zip(starts, ends)])
-    total_ms = float(step_ms.sum())
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    rows_total = wl.R * args.steps * world
-    value = rows_total / (total_ms / 1e3)
+    total_ms, value = job_throughput(float(step_ms.sum()), wl.R, args.steps, world, dist, "cuda")
 
     # ---- dominant kernel: index score (prep + k_index_score), same inputs, L2 flushed
     ld = ((wl.max_entries + 63) // 64) * 64

@@ -1,0 +1,49 @@
+"""The N > 1 host logic of bench.py, on CPU: replicas over gloo (world size
+2, 127.0.0.1), the whole-job throughput takes the slowest rank's time and
+every rank's rows; the reference arm runs on rank 0 alone."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        total_ms, value = bench.job_throughput(10.0 + 5.0 * rank, 128, 20, world, dist, "cpu")
+        out[rank] = (total_ms, value)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_job_throughput_max_over_ranks():
+    world = 2
+    out = mp.Manager().dict()
+    mp.start_processes(_rank, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
+    for r in range(world):
+        total_ms, value = out[r]
+        assert total_ms == 15.0                       # the slowest rank's timed region
+        assert value == pytest.approx(128 * 20 * world / 0.015)
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr
+    assert p.stdout.strip() == ""
