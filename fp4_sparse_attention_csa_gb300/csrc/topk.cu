@@ -452,13 +452,13 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, RowS
   return off + x - v;
 }
 
+template <int C>                   // CTAs per row: 1, 2, 4 or 8
 __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
   pdl_trigger();
   pdl_wait();                    // the scores come from the previous kernel
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) uint8_t smem[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
-  const int C = (int)cluster.num_blocks();
   const int kq = (int)cluster.block_rank();
   const int r = blockIdx.x / C;
   const int tid = threadIdx.x;
@@ -558,11 +558,20 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
     // ---- the bin of rank 512 in the summed histogram --------------------------------
     const int lane = lane_id(), warp = warp_id();
     constexpr int per = kRowBins / kThreads;
+    // every CTA's bins of this thread, read once from distributed shared memory
+    uint32_t hv[C][per];
+#pragma unroll
+    for (int q = 0; q < C; ++q) {
+      const uint32_t* h = cluster.map_shared_rank(sm.hist, q);
+#pragma unroll
+      for (int j = 0; j < per; ++j) hv[q][j] = h[per * tid + j];
+    }
     uint32_t c[per], mine = 0;
 #pragma unroll
     for (int j = 0; j < per; ++j) {
       uint32_t t = 0;
-      for (int q = 0; q < C; ++q) t += cluster.map_shared_rank(sm.hist, q)[per * tid + j];
+#pragma unroll
+      for (int q = 0; q < C; ++q) t += hv[q][j];
       c[j] = t;
       mine += t;
     }
@@ -583,19 +592,12 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
     }
     __syncthreads();
     const int tb = (int)sm.sel_bin;
-    // each CTA's count of entries in bins >= tb, from its own histogram
-    uint32_t pc[kRowCluster];
+    // each CTA's count of entries in bins >= tb
 #pragma unroll
-    for (int q = 0; q < kRowCluster; ++q) pc[q] = 0u;
+    for (int q = 0; q < C; ++q) {
+      uint32_t x = 0;
 #pragma unroll
-    for (int j = 0; j < per; ++j) {
-      const int bb = per * tid + j;
-      if (bb >= tb)
-        for (int q = 0; q < C; ++q) pc[q] += cluster.map_shared_rank(sm.hist, q)[bb];
-    }
-#pragma unroll
-    for (int q = 0; q < kRowCluster; ++q) {
-      uint32_t x = pc[q];
+      for (int j = 0; j < per; ++j) x += (per * tid + j >= tb) ? hv[q][j] : 0u;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
       if (lane == 0) sm.part[warp][q] = x;
@@ -774,9 +776,10 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;
   if (a.max_n <= kRowMax && (a.ld % 4) == 0 && ((uintptr_t)a.scores & 15u) == 0) {
-    // CTAs per row: about one per 8K entries, up to 8, and at most two CTAs
-    // per SM over the grid (measured on the serving batch: 2 per row 29 us,
-    // 1 per row 34 us, 4 per row 48 us)
+    // CTAs per row: about one per 8K entries, up to 8, at most two CTAs per
+    // SM over the grid, rounded down to a power of two (measured on the
+    // serving batch, 128 rows of up to 60K entries: 1 per row 34 us, 2 per
+    // row 26 us, 4 per row 37 us, 8 per row 83 us)
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -784,10 +787,10 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
     int C = (a.max_n + 8191) / 8192;
     C = C < 1 ? 1 : (C > kRowCluster ? kRowCluster : C);
     while (C > 1 && (long long)a.num_rows * C > 2LL * sms) --C;
+    C = C >= 8 ? 8 : (C >= 4 ? 4 : (C >= 2 ? 2 : 1));             // a power of two
+    void (*kern)(TopkArgs) = C == 8 ? k_topk_row<8> : (C == 4 ? k_topk_row<4> : (C == 2 ? k_topk_row<2> : k_topk_row<1>));
     const size_t smem = sizeof(RowSmem);
-    e = cudaFuncSetAttribute(k_topk_row, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_topk_row, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_rows * C, 1, 1);
@@ -803,7 +806,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_topk_row, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
   }
   int C = (a.max_n + kStageMax - 1) / kStageMax;
   C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
