@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 from fp4_sparse_attention_csa_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode query rows/s (csa_append + csa_decode step)"
-CFG_OF = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5}
+CFG_OF = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5, "cfg6": 6}
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one index-score

@@ -213,11 +213,13 @@ CONFIG_NAMES = {
     3: "speculative verify: 32 requests x 6 rows, 64 heads, 3072-5120 (+0-1024) tokens, append of 6",
     4: "serving batch: 128 requests x 1 row, 64 heads, 4k-128k log-uniform tokens, shuffled pages",
     5: "unpooled long context: 4 requests x 1 row, 64 heads, 262144 entries, ties at rank 512",
+    6: "chunked prefill / extend: 4 requests x 128 rows, 64 heads, 8192-16384 history + 128-token chunk",
 }
 
 
 def config(cfg: int) -> Workload:
-    """The five step shapes, seeded with cfg - 1."""
+    """The five decode step shapes and the chunked-prefill / extend shape (6),
+    seeded with cfg - 1."""
     seed = cfg - 1
     if cfg == 1:
         return custom("cfg1", seed, [4096], [1], H=16, Hi=16)
@@ -234,4 +236,12 @@ def config(cfg: int) -> Workload:
     if cfg == 5:
         tie = {"group": 1024, "group_scale": 8.0, "salient": 300, "salient_scale": 16.0}
         return custom("cfg5", seed, [262144] * 4, [1] * 4, H=64, Hi=64, P=1, tie=tie)
+    if cfg == 6:
+        # an extend step: each request appends a 128-token chunk and every chunk
+        # position is a query row; the 256-slot window ring holds the 127
+        # positions before the chunk and the chunk itself, so every row sees its
+        # full 128-position window
+        g = _rng(seed, _TAG_LEN)
+        hist = g.integers(8192, 16385, size=4)
+        return custom("cfg6", seed, hist + 128, [128] * 4, H=64, Hi=64, shuffle=True, win_cap=256)
     raise ValueError(f"unknown config {cfg}")

@@ -30,7 +30,7 @@ def _built():
     torch.cuda.set_device(0)
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6])
 def test_config_parity(cfg):
     wl = W.config(cfg)
     st = DeviceState(wl)
