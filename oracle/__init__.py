@@ -58,6 +58,10 @@ def lib():
                 getattr(L, fn).argtypes = [vp, vp, vp]
                 getattr(L, fn).restype = None
             L.or_append.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+            L.or_append_compress.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+            L.or_append_compress.restype = C.c_int
+            L.or_compress_vec.argtypes = [vp, C.c_int, vp, f32, vp, vp]
+            L.or_compress_vec.restype = None
             L.or_append.restype = C.c_int
             L.or_index_score.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, i64]
             L.or_index_score.restype = None
@@ -133,6 +137,22 @@ class _CacheStruct(C.Structure):
                 ("win_codes", C.c_void_p), ("win_scale", C.c_void_p), ("win_cap", C.c_int32)]
 
 
+class _CompressStruct(C.Structure):
+    _fields_ = [("kv_gamma", C.c_void_p), ("idx_gamma", C.c_void_p), ("eps", C.c_float),
+                ("rope_cos", C.c_void_p), ("rope_sin", C.c_void_p), ("rope_rows", C.c_int32)]
+
+
+def compress_vec(v, gamma=None, eps=1e-6, cos32=None, sin32=None):
+    """RMSNorm + rotate-half RoPE of one pooled vector (512 or 128 values),
+    as the compressor applies it before quantisation; returns a new array."""
+    v = np.array(v, dtype=np.float32, copy=True)
+    g = None if gamma is None else _c(gamma, np.float32)
+    cs = None if cos32 is None else _c(cos32, np.float32)
+    sn = None if sin32 is None else _c(sin32, np.float32)
+    lib().or_compress_vec(_p(v), int(v.size), _p(g), float(eps), _p(cs), _p(sn))
+    return v
+
+
 class Cache:
     """The oracle's own copy of the paged FP4 cache, FP8 window and pending tokens."""
 
@@ -155,14 +175,23 @@ class Cache:
                             self.P, self.win_codes.ctypes.data if w else None,
                             self.win_scale.ctypes.data if w else None, self.win_cap)
 
-    def append(self, pos0, tok_off, kv_in, idx_in, window=True):
-        """Append tokens (bf16 bits) for all requests; pending is updated in place."""
+    def append(self, pos0, tok_off, kv_in, idx_in, window=True, compress=None):
+        """Append tokens (bf16 bits) for all requests; pending is updated in place.
+        compress: None, or a dict with any of kv_gamma [512], idx_gamma [128],
+        eps, rope_cos / rope_sin [rows, 32] (fp32) for the compressor steps."""
         pos0, tok_off = _c(pos0, np.int32), _c(tok_off, np.int32)
         kv_in, idx_in = _c(kv_in, np.uint16), _c(idx_in, np.uint16)
         s = self.struct(window)
-        rc = lib().or_append(C.byref(s), _p(pos0), _p(tok_off), _p(kv_in), _p(idx_in),
-                             _p(self.pending), _p(self.pending))
-        return rc
+        if compress is None:
+            return lib().or_append(C.byref(s), _p(pos0), _p(tok_off), _p(kv_in), _p(idx_in),
+                                   _p(self.pending), _p(self.pending))
+        keep = {k: (None if compress.get(k) is None else _c(compress[k], np.float32))
+                for k in ("kv_gamma", "idx_gamma", "rope_cos", "rope_sin")}
+        rows = 0 if keep["rope_cos"] is None else int(keep["rope_cos"].shape[0])
+        cs = _CompressStruct(_p(keep["kv_gamma"]), _p(keep["idx_gamma"]), float(compress.get("eps", 1e-6)),
+                             _p(keep["rope_cos"]), _p(keep["rope_sin"]), rows)
+        return lib().or_append_compress(C.byref(s), _p(pos0), _p(tok_off), _p(kv_in), _p(idx_in),
+                                        _p(self.pending), _p(self.pending), C.byref(cs))
 
     def main_entry(self, b, e):
         page = int(self.page_table[b, e // 64])

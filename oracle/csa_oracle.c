@@ -220,9 +220,67 @@ static void load_token(const uint16_t* kv_in, const uint16_t* idx_in, int64_t t,
   for (int d = 0; d < OR_DI; ++d) y128[d] = or_bf16_to_f32(idx_in[t * OR_DI + d]);
 }
 
+/* ======================================================================
+ * Compressor steps on a pooled entry ([SGL] "DSpark adaptation and
+ * optimization": pooling, RMSNorm, RoPE and quantisation fused in one step,
+ * reused for the indexer key).  The pages name the steps but give neither the
+ * weights nor a rotary convention; the readings used here:
+ *   RMSNorm   v_i = (v_i * r) * gamma_i, r = 1 / sqrt(ms + eps), ms = ss / dim,
+ *             every product, sum, square root and quotient rounded to fp32
+ *             once (IEEE, no fused multiply-add).  ss, the sum of squares, is
+ *             taken in one fixed order: the vector is cut into 32 contiguous
+ *             parts of dim/32 values, each part summed left to right, then the
+ *             32 part sums are combined pairwise at distance 16, 8, 4, 2, 1
+ *             (s_l <- s_l + s_(l xor d)).  Every sum of this tree is the same
+ *             in all 32 positions, so the tree defines one value.
+ *   RoPE      rotate-half on the last 64 dims: for j < 32, with a = v[dim-64+j],
+ *             b = v[dim-32+j], c = cos[j], s = sin[j]:
+ *             a' = a*c - b*s,  b' = b*c + a*s  (products rounded, then the sum).
+ * ====================================================================== */
+void or_compress_vec(float* v, int dim, const float* gamma, float eps, const float* cos32,
+                     const float* sin32) {
+  if (gamma != NULL) {
+    const int k = dim / 32;
+    float part[32], next[32];
+    for (int l = 0; l < 32; ++l) {
+      float p = 0.0f;
+      for (int i = 0; i < k; ++i) {
+        const float sq = v[l * k + i] * v[l * k + i];
+        p = p + sq;
+      }
+      part[l] = p;
+    }
+    for (int d = 16; d >= 1; d >>= 1) {
+      for (int l = 0; l < 32; ++l) next[l] = part[l] + part[l ^ d];
+      memcpy(part, next, sizeof(part));
+    }
+    const float ms = part[0] * (1.0f / (float)dim);      /* dim is a power of two: exact */
+    const float den = sqrtf(ms + eps);
+    const float r = 1.0f / den;
+    for (int i = 0; i < dim; ++i) {
+      const float t = v[i] * r;
+      v[i] = t * gamma[i];
+    }
+  }
+  if (cos32 != NULL && sin32 != NULL) {
+    for (int j = 0; j < 32; ++j) {
+      const float a = v[dim - 64 + j], b = v[dim - 32 + j];
+      const float ac = a * cos32[j], bs = b * sin32[j], bc = b * cos32[j], as = a * sin32[j];
+      v[dim - 64 + j] = ac - bs;
+      v[dim - 32 + j] = bc + as;
+    }
+  }
+}
+
 int or_append(const or_cache_t* c, const int32_t* pos0, const int32_t* tok_off,
               const uint16_t* kv_in, const uint16_t* idx_in,
               const uint16_t* pending_in, uint16_t* pending_out) {
+  return or_append_compress(c, pos0, tok_off, kv_in, idx_in, pending_in, pending_out, NULL);
+}
+
+int or_append_compress(const or_cache_t* c, const int32_t* pos0, const int32_t* tok_off,
+                       const uint16_t* kv_in, const uint16_t* idx_in,
+                       const uint16_t* pending_in, uint16_t* pending_out, const or_compress_t* cmp) {
   int status = 0;
   const int P = c->pool_ratio;
   float x[OR_D], y[OR_DI], xp[OR_D], yp[OR_DI];
@@ -258,6 +316,18 @@ int or_append(const or_cache_t* c, const int32_t* pos0, const int32_t* tok_off,
       if (lp >= c->max_pages_per_req) { status = -1; continue; }
       int32_t page = c->page_table[(int64_t)b * c->max_pages_per_req + lp];
       if (page < 0 || page >= c->num_pages) { status = -1; continue; }
+      if (cmp != NULL) {
+        const int64_t rp = e * P + (P - 1);          /* position of the entry's last token */
+        const float* cs = NULL;
+        const float* sn = NULL;
+        if (cmp->rope_cos != NULL && cmp->rope_sin != NULL) {
+          if (rp >= cmp->rope_rows) { status = -3; continue; }
+          cs = cmp->rope_cos + rp * 32;
+          sn = cmp->rope_sin + rp * 32;
+        }
+        or_compress_vec(x, OR_D, cmp->kv_gamma, cmp->eps, cs, sn);
+        or_compress_vec(y, OR_DI, cmp->idx_gamma, cmp->eps, cs, sn);
+      }
       uint8_t* kvp = c->kv_pool + (int64_t)page * OR_KV_PAGE;
       uint8_t* ixp = c->idx_pool + (int64_t)page * OR_IDX_PAGE;
       or_quant_main_entry(x, kvp + slot * 256, kvp + OR_KV_SCALE_OFF + slot * 32);

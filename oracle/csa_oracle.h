@@ -81,6 +81,32 @@ int or_append(const or_cache_t* c, const int32_t* pos0, const int32_t* tok_off,
               const uint16_t* kv_in, const uint16_t* idx_in,
               const uint16_t* pending_in, uint16_t* pending_out);
 
+/* The compressor's normalisation and rotary steps, applied to each pooled
+ * entry before quantisation ([SGL] "DSpark adaptation and optimization":
+ * pair pooling, RMSNorm, RoPE, quantisation and the cache write are one fused
+ * step, reused for the indexer key).  Any pointer may be NULL (step skipped).
+ * rope_cos / rope_sin: [rope_rows, 32] for the 32 frequency pairs of the last
+ * 64 dims of each vector, indexed by the position of the entry's last token. */
+typedef struct {
+  const float* kv_gamma;    /* [512] */
+  const float* idx_gamma;   /* [128] */
+  float        eps;
+  const float* rope_cos;
+  const float* rope_sin;
+  int32_t      rope_rows;
+} or_compress_t;
+
+/* RMSNorm (sum of squares in the fixed order documented in csa_oracle.c),
+ * then rotate-half RoPE on the last 64 dims, in place.  dim: 512 or 128. */
+void or_compress_vec(float* v, int dim, const float* gamma, float eps, const float* cos32,
+                     const float* sin32);
+
+/* or_append with the compressor steps (cmp may be NULL: plain or_append).
+ * Returns -3 when an entry's position is beyond the rotary tables. */
+int or_append_compress(const or_cache_t* c, const int32_t* pos0, const int32_t* tok_off,
+                       const uint16_t* kv_in, const uint16_t* idx_in,
+                       const uint16_t* pending_in, uint16_t* pending_out, const or_compress_t* cmp);
+
 /* Indexer scores for rows: scores[r*ld + i] for i < n(r) = (pos+1)/P. */
 void or_index_score(const or_cache_t* c, int32_t num_rows, const int32_t* row_req,
                     const int32_t* row_pos, int32_t n_idx_heads,

@@ -383,3 +383,98 @@ def test_indexer_page_byte_layout():
         assert cache.idx_pool[page + 544 * 3 + 128 * (k // 16) + 16 * 5 + k % 16] == data[k]
     for j in range(4):
         assert cache.idx_pool[page + 544 * 3 + 512 + 4 * 5 + j] == sc[j]
+
+
+# ---------------------------------------------------------------- compressor
+# The fused compressor ([SGL] "DSpark adaptation and optimization": pooling,
+# RMSNorm, RoPE and quantisation in one step) on a pooled vector: RMSNorm with
+# a gamma input, then rotate-half RoPE on the last 64 dims.
+
+def _ulp32(x):
+    return np.spacing(np.abs(np.float32(x))).astype(np.float64)
+
+
+@pytest.mark.parametrize("dim", [512, 128])
+def test_rmsnorm_closed_form(dim):
+    """Against the fp64 definition x * gamma / sqrt(mean(x^2) + eps): a few
+    fp32 roundings apart, for random vectors and gammas."""
+    g = np.random.default_rng(dim)
+    for _ in range(20):
+        x = (g.standard_normal(dim) * np.exp(g.uniform(-3, 3))).astype(np.float32)
+        gam = g.uniform(0.5, 1.5, dim).astype(np.float32)
+        got = oracle.compress_vec(x, gamma=gam, eps=1e-6).astype(np.float64)
+        x64 = x.astype(np.float64)
+        ref = x64 * gam / np.sqrt(np.mean(x64 * x64) + 1e-6)
+        assert (np.abs(got - ref) <= 8 * _ulp32(ref) + 1e-30).all()
+
+
+def test_rmsnorm_constant_vector_and_unit_rms():
+    """A constant vector c maps to c / sqrt(c^2 + eps) in every element (the
+    sum of squares is exact for c a power of two); with gamma = 1 and eps
+    small the output has unit RMS."""
+    for c in (0.25, 2.0, 64.0):
+        x = np.full(512, c, np.float32)
+        got = oracle.compress_vec(x, gamma=np.ones(512, np.float32), eps=1e-6)
+        ref = c / np.sqrt(c * c + 1e-6)
+        assert np.abs(got.astype(np.float64) - ref).max() <= 2 * _ulp32(ref)
+    x = np.random.default_rng(7).standard_normal(128).astype(np.float32)
+    got = oracle.compress_vec(x, gamma=np.ones(128, np.float32), eps=1e-12).astype(np.float64)
+    assert abs(np.sqrt(np.mean(got * got)) - 1.0) < 1e-6
+
+
+def test_rope_special_angles():
+    """cos = 1, sin = 0 leaves the vector unchanged; cos = 0, sin = 1 maps each
+    pair (a, b) of the last 64 dims to (-b, a) exactly; the first dims never
+    move."""
+    x = np.random.default_rng(3).standard_normal(512).astype(np.float32)
+    one, zero = np.ones(32, np.float32), np.zeros(32, np.float32)
+    assert np.array_equal(oracle.compress_vec(x, cos32=one, sin32=zero), x)
+    got = oracle.compress_vec(x, cos32=zero, sin32=one)
+    assert np.array_equal(got[:448], x[:448])
+    assert np.array_equal(got[448:480], -x[480:512])
+    assert np.array_equal(got[480:512], x[448:480])
+
+
+def test_rope_is_a_rotation():
+    """Each pair keeps its length, and rotating by theta then by -theta
+    returns the input, up to fp32 rounding."""
+    g = np.random.default_rng(11)
+    x = g.standard_normal(128).astype(np.float32)
+    th = g.uniform(0, 2 * np.pi, 32)
+    c, s = np.cos(th).astype(np.float32), np.sin(th).astype(np.float32)
+    y = oracle.compress_vec(x, cos32=c, sin32=s)
+    n0 = np.hypot(x[64:96].astype(np.float64), x[96:128].astype(np.float64))
+    n1 = np.hypot(y[64:96].astype(np.float64), y[96:128].astype(np.float64))
+    assert np.allclose(n0, n1, rtol=1e-6, atol=1e-7)
+    z = oracle.compress_vec(y, cos32=c, sin32=-s)
+    assert np.allclose(z, x, rtol=0, atol=1e-6)
+    assert np.array_equal(y[:64], x[:64])
+
+
+@pytest.mark.parametrize("P", [2, 1])
+def test_compressed_append_token_by_token_equals_one_call(P):
+    """With the compressor on, appending a request's tokens one at a time
+    writes the same bytes as appending them in one call (pooling partners,
+    pending token and rotary positions line up)."""
+    g = np.random.default_rng(40 + P)
+    B, L = 2, 150
+    pages_per_req = (L // P + 63) // 64 + 1
+    pt = np.arange(B * pages_per_req, dtype=np.int32).reshape(B, pages_per_req)
+    kv = (g.standard_normal((B, L, 512)) * 2).astype(np.float32)
+    ix = g.standard_normal((B, L, 128)).astype(np.float32)
+    to_bits = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)
+    kvb, ixb = to_bits(kv), to_bits(ix)
+    th = g.uniform(0, 2 * np.pi, (L, 32))
+    cmp = {"kv_gamma": g.uniform(0.5, 1.5, 512), "idx_gamma": g.uniform(0.5, 1.5, 128), "eps": 1e-6,
+           "rope_cos": np.cos(th), "rope_sin": np.sin(th)}
+    one = oracle.Cache(B * pages_per_req, pt, P)
+    assert one.append(np.zeros(B, np.int32), np.array([0, L, 2 * L], np.int32),
+                      kvb.reshape(-1, 512), ixb.reshape(-1, 128), compress=cmp) == 0
+    step = oracle.Cache(B * pages_per_req, pt, P)
+    for p in range(L):
+        assert step.append(np.full(B, p, np.int32), np.array([0, 1, 2], np.int32),
+                           kvb[:, p].reshape(-1, 512), ixb[:, p].reshape(-1, 128), compress=cmp) == 0
+    assert np.array_equal(one.kv_pool, step.kv_pool) and np.array_equal(one.idx_pool, step.idx_pool)
+    plain = oracle.Cache(B * pages_per_req, pt, P)
+    plain.append(np.zeros(B, np.int32), np.array([0, L, 2 * L], np.int32), kvb.reshape(-1, 512), ixb.reshape(-1, 128))
+    assert not np.array_equal(plain.kv_pool, one.kv_pool)     # the steps did change the entries
