@@ -208,6 +208,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--compress", action="store_true",
+                    help="append through csa_append_compress (RMSNorm + RoPE before quantisation)")
     args = ap.parse_args()
     cfg = CFG_OF[args.workload]
     wl = W.config(cfg)
@@ -232,6 +234,8 @@ def main():
 
     st = DeviceState(wl)
     st.build_history()
+    if args.compress:
+        st.set_compress(W.compress_inputs(cfg, int(wl.ctx_len.max())))
     s = st.step_inputs()
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
@@ -384,7 +388,8 @@ def main():
                    "step_ms_p90": float(np.percentile(step_ms, 90)),
                    "path_unique_bytes": ab["total"], "path_gbs": path_gbs,
                    "path_frac_of_hbm": path_gbs / peak, "path_frac_of_8tbs": path_gbs / 8000.0,
-                   "bytes": ab, "parallelism": f"replicas x{world}"},
+                   "bytes": ab, "parallelism": f"replicas x{world}",
+                   "append": "csa_append_compress (RMSNorm + RoPE)" if args.compress else "csa_append"},
         "roofline": {"bound": "hbm", "kernel": "index score (k_score_prep + k_index_score)",
                      "achieved": score_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": score_gbs / peak, "traffic": traffic,

@@ -43,6 +43,11 @@ class CsaWindow(C.Structure):
     _fields_ = [("e4m3", C.c_void_p), ("scale", C.c_void_p), ("capacity", C.c_int32)]
 
 
+class CsaCompress(C.Structure):
+    _fields_ = [("kv_gamma", C.c_void_p), ("idx_gamma", C.c_void_p), ("eps", C.c_float),
+                ("rope_cos", C.c_void_p), ("rope_sin", C.c_void_p), ("rope_rows", C.c_int32)]
+
+
 class CsaRows(C.Structure):
     _fields_ = [("num_rows", C.c_int32), ("row_req", C.c_void_p), ("row_pos", C.c_void_p),
                 ("max_entries", C.c_int32), ("max_rows_per_req", C.c_int32)]
@@ -64,6 +69,7 @@ def lib():
             L.csa_workspace_size.argtypes = [i32, i32, i32, i32]
             L.csa_workspace_size.restype = sz
             L.csa_append.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+            L.csa_append_compress.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
             L.csa_index_score.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp, sz, vp]
             L.csa_topk.argtypes = [i32, vp, i32, vp, i32, i32, vp, vp, sz, vp]
             L.csa_sparse_attn.argtypes = [vp, vp, vp, vp, i32, vp, f32, vp, vp, vp, sz, vp]
@@ -120,6 +126,21 @@ def make_rows(row_req, row_pos, max_entries, max_rows_per_req):
 # ---- entry points (same names as the C ABI) ----------------------------------------
 def csa_workspace_size(op, num_rows, max_entries, n_heads):
     return int(lib().csa_workspace_size(op, num_rows, max_entries, n_heads))
+
+
+def make_compress(kv_gamma=None, idx_gamma=None, eps=1e-6, rope_cos=None, rope_sin=None):
+    """Compressor-step arguments of csa_append_compress (fp32 device tensors;
+    rope tables [rows, 32])."""
+    rows = 0 if rope_cos is None else int(rope_cos.shape[0])
+    return CsaCompress(_ptr(kv_gamma), _ptr(idx_gamma), float(eps), _ptr(rope_cos), _ptr(rope_sin), rows)
+
+
+def csa_append_compress(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, compress, ws=None,
+                        stream=None):
+    rc = lib().csa_append_compress(C.byref(cache), C.byref(window) if window is not None else None, _ptr(pos0),
+                                   _ptr(tok_off), int(total_tokens), _ptr(kv_in), _ptr(idx_in), _ptr(pending),
+                                   C.byref(compress), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "csa_append_compress")
 
 
 def csa_append(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, ws=None, stream=None):

@@ -153,6 +153,14 @@ size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int
 csa_status_t csa_append(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
                         const int32_t* tok_off, int32_t total_tokens, const void* kv_in, const void* idx_in,
                         void* pending, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return csa_append_compress(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, nullptr, ws,
+                             ws_bytes, stream);
+}
+
+csa_status_t csa_append_compress(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
+                                 const int32_t* tok_off, int32_t total_tokens, const void* kv_in,
+                                 const void* idx_in, void* pending, const csa_compress_t* compress, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
   csa_status_t s = check_cache(cache);
   if (s != CSA_OK) return s;
   if ((s = check_window(window, 1)) != CSA_OK) return s;
@@ -179,6 +187,19 @@ csa_status_t csa_append(const csa_cache_t* cache, const csa_window_t* window, co
   a.idx_in = static_cast<const uint16_t*>(idx_in);
   a.pending = static_cast<uint16_t*>(pending);
   a.status = static_cast<uint32_t*>(ws);
+  a.kv_gamma = compress ? compress->kv_gamma : nullptr;
+  a.idx_gamma = compress ? compress->idx_gamma : nullptr;
+  a.eps = compress ? compress->eps : 0.0f;
+  const bool rope = compress && compress->rope_cos && compress->rope_sin;
+  a.rope_cos = rope ? compress->rope_cos : nullptr;
+  a.rope_sin = rope ? compress->rope_sin : nullptr;
+  a.rope_rows = rope ? compress->rope_rows : 0;
+  if (compress) {
+    if (!aligned(compress->kv_gamma, 4) || !aligned(compress->idx_gamma, 4)) return CSA_ERR_INVALID_ARGUMENT;
+    if (rope && (compress->rope_rows < 0 || !aligned(compress->rope_cos, 4) || !aligned(compress->rope_sin, 4)))
+      return CSA_ERR_INVALID_ARGUMENT;
+    if (!(compress->eps >= 0.0f)) return CSA_ERR_INVALID_ARGUMENT;
+  }
   return from_cuda(launch_append(a, stream));
 }
 

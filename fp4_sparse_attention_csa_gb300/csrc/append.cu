@@ -54,6 +54,46 @@ __device__ __forceinline__ float warp_max(float v) {
 
 constexpr int kOffStage = 4096;      // token offsets staged in shared memory
 
+// RMSNorm of a vector spread over the warp, K values per lane (lane l holds
+// elements K*l .. K*l+K-1): each lane sums its squares left to right, the 32
+// partial sums are combined at lane distance 16, 8, 4, 2, 1 (every lane ends
+// with the same sum), then v = (v * r) * gamma with r = 1 / sqrt(ss/dim + eps),
+// each step rounded to fp32.
+template <int K>
+__device__ __forceinline__ void rms_norm(float (&v)[K], const float* gamma, float eps, float inv_dim) {
+  float p = 0.0f;
+#pragma unroll
+  for (int i = 0; i < K; ++i) p = __fadd_rn(p, __fmul_rn(v[i], v[i]));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xFFFFFFFFu, p, o));
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(p, inv_dim), eps)));
+#pragma unroll
+  for (int i = 0; i < K; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], r), __ldg(gamma + i));
+}
+
+// Rotate-half RoPE on the last 64 elements of a warp-spread vector, K values
+// per lane: the first half (a) sits in lanes [lo, lo + 32/K), the second half
+// (b) in the next 32/K lanes, partner = lane xor (32/K).  a' = a*c - b*s,
+// b' = b*c + a*s for pair j (products rounded, then the sum).
+template <int K>
+__device__ __forceinline__ void rope_last64(float (&v)[K], const float* cs, const float* sn, int lane) {
+  constexpr int kHalfLanes = 32 / K;              // lanes holding one 32-element half
+  constexpr int kLo = 32 - 2 * kHalfLanes;        // first lane of the rotary part
+  float other[K];
+#pragma unroll
+  for (int i = 0; i < K; ++i) other[i] = __shfl_xor_sync(0xFFFFFFFFu, v[i], kHalfLanes);
+  if (lane >= kLo) {
+    const int jb = K * ((lane - kLo) % kHalfLanes);
+    const bool first = lane < kLo + kHalfLanes;
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      const float c = __ldg(cs + jb + i), s = __ldg(sn + jb + i);
+      v[i] = first ? __fsub_rn(__fmul_rn(v[i], c), __fmul_rn(other[i], s))
+                   : __fadd_rn(__fmul_rn(v[i], c), __fmul_rn(other[i], s));
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
   pdl_trigger();                 // the score step's prep reads nothing this kernel writes
   // request lookup table: tok_off staged once per block (one coalesced read
@@ -135,12 +175,27 @@ __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) y[i] = (yp[i] + y[i]) * 0.5f;
     }
+    // ---- compressor steps on the pooled entry (csa_append_compress)
+    bool write_entry = true;
+    if (a.kv_gamma) rms_norm<16>(x, a.kv_gamma + lane * 16, a.eps, 1.0f / 512.0f);
+    if (a.idx_gamma) rms_norm<4>(y, a.idx_gamma + lane * 4, a.eps, 1.0f / 128.0f);
+    if (a.rope_cos) {
+      if (p >= a.rope_rows) {      // p: the position of the entry's last token
+        if (lane == 0) raise_flag(a.status, CSA_FLAG_APPEND);
+        write_entry = false;
+      } else {
+        const float* cs = a.rope_cos + (size_t)p * 32;
+        const float* sn = a.rope_sin + (size_t)p * 32;
+        rope_last64<16>(x, cs, sn, lane);
+        rope_last64<4>(y, cs, sn, lane);
+      }
+    }
     const int lp = e / PAGE, slot = e % PAGE;
     int page = -1;
     if (lp < a.max_pages) page = __ldg(a.page_table + (size_t)b * a.max_pages + lp);
     if (page < 0 || page >= a.num_pages) {
       if (lane == 0) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
-    } else {
+    } else if (write_entry) {
       // NVFP4 block (this lane's 16 values): S = E4M3(amax/6), codes = e2m1(x/s)
       float amax = 0.0f;
 #pragma unroll

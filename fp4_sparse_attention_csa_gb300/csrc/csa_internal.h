@@ -43,6 +43,13 @@ struct AppendArgs {
   const uint16_t* idx_in;
   uint16_t* pending;
   uint32_t* status;
+  // compressor steps (NULL: skipped); see csa_append_compress
+  const float* kv_gamma;
+  const float* idx_gamma;
+  float eps;
+  const float* rope_cos;
+  const float* rope_sin;
+  int32_t rope_rows;
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 

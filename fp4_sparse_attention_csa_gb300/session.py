@@ -8,7 +8,8 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 import torch
 
-from . import (KV_PAGE_BYTES, IDX_PAGE_BYTES, OP_APPEND, OP_DECODE, csa_append, csa_decode,
+from . import (KV_PAGE_BYTES, IDX_PAGE_BYTES, OP_APPEND, OP_DECODE, csa_append, csa_append_compress,
+               make_compress, csa_decode,
                csa_workspace_size, make_cache, make_rows, make_window)
 
 
@@ -118,7 +119,23 @@ class DeviceState:
                               device=self.device)
         return s
 
+    def set_compress(self, inputs):
+        """Run the step's append with the compressor steps (csa_append_compress);
+        inputs: dict of fp32 numpy arrays kv_gamma, idx_gamma, rope_cos, rope_sin
+        and eps (see workloads.compress_inputs), or None to switch them off."""
+        if inputs is None:
+            self.compress = None
+            return
+        self._compress_dev = {k: (torch.from_numpy(v).to(self.device) if isinstance(v, np.ndarray) else v)
+                              for k, v in inputs.items()}
+        d = self._compress_dev
+        self.compress = make_compress(d["kv_gamma"], d["idx_gamma"], d["eps"], d["rope_cos"], d["rope_sin"])
+
     def step_append(self, s, stream=None):
+        if getattr(self, "compress", None) is not None:
+            csa_append_compress(self.cache, self.window, s["pos0"], s["tok_off"], self.wl.R, s["kv_new"],
+                                s["idx_new"], self.pending, self.compress, self.ws_append, stream)
+            return
         csa_append(self.cache, self.window, s["pos0"], s["tok_off"], self.wl.R, s["kv_new"], s["idx_new"],
                    self.pending, self.ws_append, stream)
 

@@ -207,6 +207,18 @@ def custom(name: str, seed: int, ctx_len, new_tok, H: int, Hi: int, P: int = 2,
                     salient_frac=salient_frac, tie=tie or {})
 
 
+def compress_inputs(seed: int, rows: int) -> dict:
+    """Seeded inputs of the compressor steps: RMSNorm weights U(0.5, 1.5) for
+    the latent (512) and the indexer key (128), eps, and rotary tables
+    cos/sin [rows, 32] of seeded uniform angles (fp32).  No method arithmetic:
+    these are the weights and tables a caller supplies."""
+    g = _rng(seed, 0x434D50)
+    th = g.uniform(0.0, 2.0 * math.pi, (rows, 32))
+    return {"kv_gamma": g.uniform(0.5, 1.5, 512).astype(np.float32),
+            "idx_gamma": g.uniform(0.5, 1.5, 128).astype(np.float32), "eps": 1e-6,
+            "rope_cos": np.cos(th).astype(np.float32), "rope_sin": np.sin(th).astype(np.float32)}
+
+
 CONFIG_NAMES = {
     1: "tiny decode: 1 row, 16 heads, 4096 tokens -> 2048 entries",
     2: "single-request long decode: 1 row, 64 heads, 32768 tokens -> 16384 entries, 5% salient x4",

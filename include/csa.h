@@ -232,6 +232,41 @@ CSA_API csa_status_t csa_index_score_noalloc(const csa_cache_t* cache, const csa
                                              int32_t n_idx_heads, const void* q_idx, const float* w,
                                              float* scores, int32_t ld, cudaStream_t stream);
 
+/* csa_append_compress -- csa_append with the compressor's normalisation and
+ * rotary steps applied to every new pooled entry (main latent and indexer
+ * key) after pooling and before quantisation ([SGL] "DSpark adaptation and
+ * optimization": pair pooling, RMSNorm, RoPE, quantisation and the main-KV
+ * write fused in one kernel, reused for index-K).  The pages give neither the
+ * weights nor a rotary convention; this library's reading:
+ *  - RMSNorm: v_i = (v_i * r) * gamma_i, r = 1 / sqrt(ss / dim + eps), every
+ *    step rounded to fp32 (no fused multiply-add); ss = sum of squares taken
+ *    as 32 contiguous parts of dim/32 values summed left to right, the part
+ *    sums then combined pairwise at distance 16, 8, 4, 2, 1.
+ *  - RoPE: rotate-half on the last 64 dims of each vector: for j < 32,
+ *    a = v[dim-64+j], b = v[dim-32+j]: a' = a*c_j - b*s_j, b' = b*c_j + a*s_j,
+ *    with (c, s) = rope_cos/rope_sin row p, p = the position of the entry's
+ *    last token (p = P*e + P - 1 for entry e).
+ *  - The FP8 window tokens and the pending token stay raw (unnormalised).
+ * compress (host pointer, required): any of its device pointers may be NULL
+ * to skip that step.  kv_gamma fp32 [512], idx_gamma fp32 [128]; rope_cos /
+ * rope_sin fp32 [rope_rows, 32], 4-byte aligned.  An entry whose position is
+ * >= rope_rows is not written and raises CSA_FLAG_APPEND.  Other arguments,
+ * layouts and errors as csa_append. */
+typedef struct {
+  const float* kv_gamma;
+  const float* idx_gamma;
+  float        eps;
+  const float* rope_cos;
+  const float* rope_sin;
+  int32_t      rope_rows;
+} csa_compress_t;
+
+CSA_API csa_status_t csa_append_compress(const csa_cache_t* cache, const csa_window_t* window,
+                                         const int32_t* pos0, const int32_t* tok_off, int32_t total_tokens,
+                                         const void* kv_in, const void* idx_in, void* pending,
+                                         const csa_compress_t* compress, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream);
+
 /* Synchronises `stream`, returns the status word's flags in *flags_out (host)
  * and clears it.  Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_FAULT. */
 CSA_API csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out);

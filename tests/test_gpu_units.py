@@ -274,3 +274,64 @@ def test_decode_is_deterministic():
     o1, t1 = s["out"].clone(), s["topk"].clone()
     st.step_decode(s)
     assert torch.equal(o1, s["out"]) and torch.equal(t1, s["topk"])
+
+
+# ------------------------------------------------ compressed append (NEXT f-3)
+def _compress_dev(c):
+    return {k: (torch.from_numpy(c[k]).cuda() if isinstance(c[k], np.ndarray) else c[k]) for k in c}
+
+
+@pytest.mark.parametrize("P", [2, 1])
+def test_append_compress_bit_exact(P):
+    """csa_append_compress (RMSNorm with gamma, rotate-half RoPE, then the
+    quantisers) writes the same bytes as the oracle, over two calls per
+    request (whole history, then a few tokens with odd and even starts, so
+    pooling crosses the pending token)."""
+    ctx = [1, 2, 3, 63, 64, 65, 129, 300, 1025]
+    new = [1, 2, 1, 6, 3, 1, 6, 2, 5]
+    wl = W.custom("cmp", 14 + P, ctx, new, H=16, Hi=16, P=P, shuffle=True)
+    cmp = W.compress_inputs(14 + P, int(wl.ctx_len.max()))
+    dcmp = _compress_dev(cmp)
+    st = DeviceState(wl)
+    ref = oracle.Cache(wl.num_pages, wl.page_table, wl.P, wl.win_cap)
+    comp = csa.make_compress(dcmp["kv_gamma"], dcmp["idx_gamma"], dcmp["eps"], dcmp["rope_cos"], dcmp["rope_sin"])
+    for lo_of, hi_of in ((lambda b: 0, lambda b: int(wl.hist_len[b])),
+                         (lambda b: int(wl.hist_len[b]), lambda b: int(wl.ctx_len[b]))):
+        xs, ys, cnt = [], [], []
+        pos0 = np.zeros(wl.B, np.int32)
+        for b in range(wl.B):
+            lo, hi = lo_of(b), hi_of(b)
+            x, y = wl.tokens(b, lo, hi)
+            xs.append(x)
+            ys.append(y)
+            pos0[b] = lo
+            cnt.append(hi - lo)
+        tok_off = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+        X, Y = np.concatenate(xs), np.concatenate(ys)
+        csa.csa_append_compress(st.cache, st.window, torch.from_numpy(pos0).cuda(), torch.from_numpy(tok_off).cuda(),
+                                int(tok_off[-1]), torch.from_numpy(X.view(np.int16)).cuda(),
+                                torch.from_numpy(Y.view(np.int16)).cuda(), st.pending, comp, st.ws_append)
+        assert ref.append(pos0, tok_off, X, Y, compress=cmp) == 0
+    rc, flags = csa.csa_check_device_status(st.ws_append)
+    assert rc == 0 and flags == 0, flags
+    _pools_equal(st, ref)
+    plain = oracle.build_cache(wl)                       # the steps changed the entries
+    assert not np.array_equal(plain.kv_pool, ref.kv_pool)
+
+
+def test_append_compress_flags_positions_beyond_the_tables():
+    wl = W.custom("cmpf", 16, [200], [1], H=16, Hi=16)
+    cmp = W.compress_inputs(16, 100)                      # rows for positions 0..99 only
+    dcmp = _compress_dev(cmp)
+    st = DeviceState(wl)
+    comp = csa.make_compress(dcmp["kv_gamma"], dcmp["idx_gamma"], dcmp["eps"], dcmp["rope_cos"], dcmp["rope_sin"])
+    x, y = wl.tokens(0, 0, 200)
+    csa.csa_append_compress(st.cache, st.window, torch.zeros(1, dtype=torch.int32).cuda(),
+                            torch.tensor([0, 200], dtype=torch.int32).cuda(), 200,
+                            torch.from_numpy(x.view(np.int16)).cuda(), torch.from_numpy(y.view(np.int16)).cuda(),
+                            st.pending, comp, st.ws_append)
+    rc, flags = csa.csa_check_device_status(st.ws_append)
+    assert rc == 5 and (flags & csa.FLAG_APPEND)
+    ref = oracle.Cache(wl.num_pages, wl.page_table, wl.P, wl.win_cap)
+    assert ref.append(np.zeros(1, np.int32), np.array([0, 200], np.int32), x, y, compress=cmp) == -3
+    _pools_equal(st, ref)                                 # entries 0..49 written, the rest untouched
