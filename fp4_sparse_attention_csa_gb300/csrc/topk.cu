@@ -8,8 +8,8 @@
 //   return every visible index, the rest of the row is -1).
 //
 // Two kernels, both one thread-block cluster per row:
-//  k_topk_row  rows up to 128K entries (every decode shape but the unpooled
-//              long context): C <= 8 CTAs per row stream slices of the
+//  k_topk_row  rows up to 256K entries (every decode shape here): C <= 8
+//              CTAs per row stream slices of the
 //              L2-resident row; value range and value histogram are combined
 //              over distributed shared memory, the entries in or above the
 //              bin of rank 512 are compacted in row order into CTA 0, which
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int sli
 // list longer than kRowCap (many ties at the cut) or a non-finite range falls
 // back to a whole-row radix select in CTA 0.  A CTA leaves only after a
 // cluster barrier that follows every remote read of its shared memory.
-constexpr int kRowMax = 131072;
+constexpr int kRowMax = 262144;
 constexpr int kRowBins = 2048;
 constexpr int kRowCap = 4096;
 constexpr int kRowCluster = 8;

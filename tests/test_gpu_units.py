@@ -141,7 +141,7 @@ def test_identical_entries_score_identically():
 
 
 # ------------------------------------------------------------------- top-k
-@pytest.mark.parametrize("n", [0, 1, 300, 511, 512, 513, 1000, 5000, 70000, 262144])
+@pytest.mark.parametrize("n", [0, 1, 300, 511, 512, 513, 1000, 5000, 70000, 262144, 300000])
 def test_topk_exact_with_ties(n):
     g = np.random.default_rng(n)
     R = 3
