@@ -7,14 +7,14 @@ the step's tokens appended, then one csa_decode.
   J-2  every row's top-512 set is right outside the 1e-4 tie band; for the
        unpooled workload, whose rank-512 tie group is bitwise identical
        entries, the selection must equal the oracle's exactly.
-  J-3  every row's attention output and lse are within tolerance, judged
+  J-3  every row's attention output and lse are within tolerance, checked
        against the oracle run on the indices the GPU chose.
 """
 import numpy as np
 import pytest
 import torch
 
-import judge
+import parity
 import oracle
 import fp4_sparse_attention_csa_gb300 as csa
 from fp4_sparse_attention_csa_gb300 import workloads as W
@@ -63,12 +63,12 @@ def test_config_parity(cfg):
     # ---- J-2
     differ = 0
     for r in range(wl.R):
-        differ += judge.check_topk_row(gt[r], scores[r], int(n[r]))
+        differ += parity.check_topk_row(gt[r], scores[r], int(n[r]))
     if wl.tie:
         assert np.array_equal(gt, topk), "tie group must resolve to the lowest indices"
     # ---- J-3 (re-run the oracle's attention where the GPU picked differently in the band)
     for r in range(wl.R):
         if not np.array_equal(gt[r], topk[r]):
             out[r], lse[r] = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], gt[r], q[r], wl.softmax_scale)
-    norm, l2 = judge.check_attention(go, out, gl, lse)
+    norm, l2 = parity.check_attention(go, out, gl, lse)
     print(f"cfg{cfg}: rows={wl.R} band-picks={differ} attn max-norm-err={norm:.2e} rel-L2={l2:.2e}")

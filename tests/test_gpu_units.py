@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-import judge
+import parity
 import oracle
 import fp4_sparse_attention_csa_gb300 as csa
 from fp4_sparse_attention_csa_gb300 import workloads as W
@@ -214,7 +214,7 @@ def test_sparse_attention_matches_oracle(H, ctx, rows):
     for r in range(wl.R):
         o_ref[r], l_ref[r] = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], topk[r], q[r],
                                                   wl.softmax_scale)
-    norm, l2 = judge.check_attention(out.float().cpu().numpy(), o_ref, lse.cpu().numpy(), l_ref)
+    norm, l2 = parity.check_attention(out.float().cpu().numpy(), o_ref, lse.cpu().numpy(), l_ref)
     print(f"attention H={H}: max normalised err {norm:.2e}, rel L2 {l2:.2e}")
 
 
@@ -235,8 +235,8 @@ def test_attention_many_rows_single_split():
     gt = s["topk"].cpu().numpy()
     n = wl.row_entries()
     for r in range(wl.R):
-        judge.check_topk_row(gt[r], scores[r], int(n[r]))
-    judge.check_attention(s["out"].float().cpu().numpy(), out, s["lse"].cpu().numpy(), lse)
+        parity.check_topk_row(gt[r], scores[r], int(n[r]))
+    parity.check_attention(s["out"].float().cpu().numpy(), out, s["lse"].cpu().numpy(), lse)
 
 
 # ------------------------------------------------------------------ decode
@@ -259,9 +259,9 @@ def test_decode_end_to_end(H, Hi, rows):
     o_ref = np.zeros((wl.R, H, 512), np.float32)
     l_ref = np.zeros((wl.R, H), np.float32)
     for r in range(wl.R):
-        judge.check_topk_row(gt[r], scores[r], int(n[r]))
+        parity.check_topk_row(gt[r], scores[r], int(n[r]))
         o_ref[r], l_ref[r] = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], gt[r], q[r], wl.softmax_scale)
-    judge.check_attention(s["out"].float().cpu().numpy(), o_ref, s["lse"].cpu().numpy(), l_ref)
+    parity.check_attention(s["out"].float().cpu().numpy(), o_ref, s["lse"].cpu().numpy(), l_ref)
 
 
 def test_decode_is_deterministic():
