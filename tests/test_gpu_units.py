@@ -264,6 +264,38 @@ def test_decode_end_to_end(H, Hi, rows):
     parity.check_attention(s["out"].float().cpu().numpy(), o_ref, s["lse"].cpu().numpy(), l_ref)
 
 
+def test_plan_reused_across_layers():
+    """Cross-layer reuse: layers that read the same cache share one top-512
+    plan (csa_decode's topk_out); each further layer runs only the sparse
+    attention with its own q, and matches a full csa_decode for that layer
+    bit for bit."""
+    ctx = [700, 2500, 5003, 9000]
+    wl = W.custom("plan", 61, ctx, [1] * len(ctx), H=64, Hi=64, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    st.step_decode(s)                                    # layer 0: score + top-512 + attention
+    plan = s["topk"].clone()
+    g = np.random.default_rng(7)
+    ws_a = torch.zeros(csa.csa_workspace_size(csa.OP_SPARSE_ATTN, wl.R, wl.max_entries, wl.H), dtype=torch.uint8,
+                       device="cuda")
+    for layer in (1, 2):
+        q_l = torch.from_numpy(W.f32_to_bf16_bits(g.standard_normal((wl.R, wl.H, 512)).astype(np.float32))
+                               .view(np.int16)).cuda().view(torch.bfloat16)
+        out_p = torch.empty_like(s["out"])
+        lse_p = torch.empty_like(s["lse"])
+        csa.csa_sparse_attn(st.cache, st.window, s["rows"], plan, wl.H, q_l, wl.softmax_scale, out_p, lse_p, ws_a)
+        s_full = dict(s)
+        s_full["q"] = q_l
+        s_full["out"], s_full["lse"] = torch.empty_like(s["out"]), torch.empty_like(s["lse"])
+        s_full["topk"] = torch.empty_like(s["topk"])
+        st.step_decode(s_full)
+        torch.cuda.synchronize()
+        assert torch.equal(s_full["topk"], plan)           # the same cache and indexer query: the same plan
+        assert torch.equal(out_p, s_full["out"]) and torch.equal(lse_p, s_full["lse"])
+
+
 def test_decode_is_deterministic():
     wl = W.custom("det", 61, [3000, 5000], [2, 1], H=64, Hi=64)
     st = DeviceState(wl)
