@@ -368,9 +368,7 @@ def main():
                "l2": "not flushed inside the pipeline (the cache pools exceed L2)",
                "serial_value": wl.R * args.steps * world / (serial_ms / 1e3)}
 
-    sms = torch.cuda.get_device_properties(local).multi_processor_count
-    attn_splits = max(1, min(5, sms // max(wl.R, 1)))          # the library's split rule
-    launches_per_step = 1 + 4 + (1 if attn_splits > 1 else 0)  # append, prep, score, top-k, attention, merge
+    launches_per_step = 5          # append, score prep, index score, top-k, attention (splits merge in-cluster)
     if rank != 0:
         return
     cpu = None

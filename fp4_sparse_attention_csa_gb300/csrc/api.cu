@@ -55,14 +55,13 @@ csa_status_t check_rows(const csa_rows_t* r, const csa_cache_t* c) {
 size_t scores_ld(int32_t max_entries) { return align_up((size_t)(max_entries > 0 ? max_entries : 1), 64); }
 
 struct DecodeLayout {
-  size_t scores, topk, attn, end;
+  size_t scores, topk, end;
 };
-DecodeLayout decode_layout(int32_t R, int32_t max_entries, int32_t H) {
+DecodeLayout decode_layout(int32_t R, int32_t max_entries) {
   DecodeLayout L;
   L.scores = align_up(score_ws_bytes(R, CSA_MAX_IDX_HEADS));
   L.topk = align_up(L.scores + sizeof(float) * (size_t)R * scores_ld(max_entries));
-  L.attn = align_up(L.topk + sizeof(int32_t) * (size_t)R * CSA_TOPK);
-  L.end = align_up(L.attn + attn_partial_bytes(R, H, attn_choose_splits(R, num_sms())));
+  L.end = align_up(L.topk + sizeof(int32_t) * (size_t)R * CSA_TOPK);
   return L;
 }
 
@@ -102,7 +101,7 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
 
 csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                       const int32_t* topk, int32_t H, const void* q, float softmax_scale, void* out, float* lse,
-                      void* ws, size_t part_off, cudaStream_t stream) {
+                      void* ws, cudaStream_t stream) {
   AttnArgs a;
   a.kv_pool = static_cast<const uint8_t*>(cache->kv_pool);
   a.page_table = cache->page_table;
@@ -123,7 +122,6 @@ csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, cons
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.splits = attn_choose_splits(rows->num_rows, num_sms());
-  a.part = a.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + part_off) : nullptr;
   a.status = static_cast<uint32_t*>(ws);
   return from_cuda(launch_sparse_attn(a, stream));
 }
@@ -134,7 +132,7 @@ extern "C" {
 
 size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int32_t n_heads) {
   if (num_rows < 0 || max_entries < 0) return 0;
-  const int32_t H = n_heads > 0 ? n_heads : CSA_MAX_HEADS;
+  (void)n_heads;                     // no size depends on the head count
   switch (op) {
     case CSA_OP_APPEND:
     case CSA_OP_TOPK:
@@ -142,9 +140,9 @@ size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int
     case CSA_OP_INDEX_SCORE:
       return align_up(score_ws_bytes(num_rows, CSA_MAX_IDX_HEADS));
     case CSA_OP_SPARSE_ATTN:
-      return align_up(kStatusBytes + attn_partial_bytes(num_rows, H, attn_choose_splits(num_rows, num_sms())));
+      return kStatusBytes;
     case CSA_OP_DECODE:
-      return decode_layout(num_rows, max_entries, H).end;
+      return decode_layout(num_rows, max_entries).end;
     default:
       return 0;
   }
@@ -249,10 +247,8 @@ csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* windo
   if (n_heads < 1 || n_heads > CSA_MAX_HEADS) return CSA_ERR_UNSUPPORTED;
   if (rows->num_rows == 0) return CSA_OK;
   if (!topk_idx || !q || !out || !aligned(q, 16) || !aligned(out, 16)) return CSA_ERR_INVALID_ARGUMENT;
-  const size_t need = kStatusBytes + attn_partial_bytes(rows->num_rows, n_heads,
-                                                        attn_choose_splits(rows->num_rows, num_sms()));
-  if (!ws || ws_bytes < need || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
-  return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, ws, kStatusBytes, stream);
+  if (!ws || ws_bytes < kStatusBytes || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, ws, stream);
 }
 
 csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
@@ -268,7 +264,7 @@ csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window, co
   if (rows->num_rows == 0) return CSA_OK;
   if (!q_idx || !w || !q || !out || !aligned(q_idx, 16) || !aligned(q, 16) || !aligned(out, 16))
     return CSA_ERR_INVALID_ARGUMENT;
-  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries, n_heads);
+  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries);
   if (!ws || ws_bytes < L.end || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* base = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(base + L.scores);
@@ -286,7 +282,7 @@ csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window, co
   t.out = topk;
   t.status = static_cast<uint32_t*>(ws);
   if ((s = from_cuda(launch_topk(t, stream))) != CSA_OK) return s;
-  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, ws, L.attn, stream);
+  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, ws, stream);
 }
 
 csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out) {

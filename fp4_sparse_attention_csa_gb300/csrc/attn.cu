@@ -22,8 +22,10 @@
 // (exact in fp16) with the rest of their fp32 scale, mu in [1, 2), applied to
 // the logit and to p.  Online softmax across tiles in the log2 domain; the
 // O^T accumulators live in TMEM and are rescaled when a head's max grows.
-// With several CTAs per row, partial (O, m, l) go to the workspace and a merge
-// kernel combines them by log-sum-exp.
+// With several CTAs per row (few rows), the row's CTAs form a thread-block
+// cluster: each stages its unnormalised O and (m, l) in shared memory and the
+// CTAs merge them by log-sum-exp over distributed shared memory, each taking
+// every splits-th head.
 //
 // Latency: every selected entry's page is resolved once, up front, by all
 // threads together; the raw FP4/FP8 bytes of tile t+1 are loaded into
@@ -33,8 +35,14 @@
 // descriptors are formed once and advanced by constant offsets, so the
 // issuing thread keeps the tensor pipe busy.  The output is normalised by a
 // per-head reciprocal and leaves through shared memory in 16-byte stores.
+#include <cooperative_groups.h>
+
+#include <atomic>
+
 #include "csa_device.cuh"
 #include "csa_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace csa {
 
@@ -63,6 +71,7 @@ struct AttnSmem {
   float red_sum[4][kMaxH];
   float m_buf[2][kMaxH];               // running max (log2), by tile parity
   float l_run[kMaxH];
+  float m_out[kMaxH], l_out[kMaxH];    // a split's final (m, l), read by the cluster's merge
   float inv_l[kMaxH];
   uint64_t s_bar, pv_bar;
   uint32_t tmem_base;
@@ -641,8 +650,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
       a.lse[(size_t)r * H + tid] = (have && l > 0.0f) ? (m_fin[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
   } else {
-    // partial: O [H][512] unnormalised, then m (log2) [H], l [H]
-    float* part_out = a.part + ((size_t)r * a.splits + split) * (size_t)H * (D + 2);
+    // split partials, merged inside the row's cluster: O [H][512] unnormalised
+    // (fp32, in the key tile's buffer, free after the last PV) and (m, l)
+    cg::cluster_group cluster = cg::this_cluster();
+    float* ostage = reinterpret_cast<float*>(sm.k);
     for (int h0 = 0; h0 < H; h0 += 16) {
       uint32_t v[16];
       if (have) {
@@ -650,12 +661,72 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
         tmem_ld_wait();
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) part_out[(size_t)(h0 + i) * D + d] = have ? __uint_as_float(v[i]) : 0.0f;
+      for (int i = 0; i < 16; ++i) ostage[(h0 + i) * D + d] = have ? __uint_as_float(v[i]) : 0.0f;
     }
     if (tid < H) {
-      part_out[(size_t)H * D + tid] = have ? m_fin[tid] : -INFINITY;
-      part_out[(size_t)H * D + H + tid] = have ? sm.l_run[tid] : 0.0f;
+      sm.m_out[tid] = have ? m_fin[tid] : -INFINITY;
+      sm.l_out[tid] = have ? sm.l_run[tid] : 0.0f;
     }
+    cluster.sync();                                // every split's partials are published
+    // this CTA merges heads split, split + S, ...: first every (head, split)
+    // pair's (m, l) in one parallel round of remote loads, then per head the
+    // weights w_q = 2^(m_q - M) / sum_q 2^(m_q - M) l_q, then O = sum_q w_q O_q
+    const int S = a.splits;
+    const int nh = (H - split + S - 1) / S;
+    float (*mq_s)[kMaxTiles] = reinterpret_cast<float (*)[kMaxTiles]>(&sm.red_max[0][0]);   // [nh][S]
+    float (*lq_s)[kMaxTiles] = reinterpret_cast<float (*)[kMaxTiles]>(&sm.red_sum[0][0]);
+    if (tid < nh * kMaxTiles) {
+      const int i = tid / kMaxTiles, q = tid % kMaxTiles;
+      float m = -INFINITY, l = 0.0f;
+      if (q < S) {
+        const AttnSmem* rs = cluster.map_shared_rank(&sm, q);
+        m = rs->m_out[split + i * S];
+        l = rs->l_out[split + i * S];
+      }
+      mq_s[i][q] = m;
+      lq_s[i][q] = l;
+    }
+    __syncthreads();
+    if (tid < nh) {
+      float M = -INFINITY, L = 0.0f;
+#pragma unroll
+      for (int q = 0; q < kMaxTiles; ++q) M = fmaxf(M, mq_s[tid][q]);
+      float wq[kMaxTiles];
+#pragma unroll
+      for (int q = 0; q < kMaxTiles; ++q) {
+        wq[q] = mq_s[tid][q] == -INFINITY ? 0.0f : exp2f(mq_s[tid][q] - M);
+        L += wq[q] * lq_s[tid][q];
+      }
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll
+      for (int q = 0; q < kMaxTiles; ++q) mq_s[tid][q] = wq[q] * inv;   // the row's own entries only
+      if (a.lse)
+        a.lse[(size_t)r * H + split + tid * S] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
+    const float* ob[kMaxTiles];                    // every split's O, thread tid: dim tid (D == kThreads)
+#pragma unroll
+    for (int q = 0; q < kMaxTiles; ++q)
+      ob[q] = reinterpret_cast<const float*>(cluster.map_shared_rank(&sm, q < S ? q : 0)->k) + tid;
+    constexpr int kHG = 4;                         // heads whose remote loads go out together
+    for (int i0 = 0; i0 < nh; i0 += kHG) {
+      float v[kHG][kMaxTiles];
+#pragma unroll
+      for (int u = 0; u < kHG; ++u)
+#pragma unroll
+        for (int q = 0; q < kMaxTiles; ++q)
+          v[u][q] = (i0 + u < nh && q < S) ? ob[q][(split + (i0 + u) * S) * D] : 0.0f;
+#pragma unroll
+      for (int u = 0; u < kHG; ++u) {
+        if (i0 + u >= nh) break;
+        float acc = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kMaxTiles; ++q) acc += mq_s[i0 + u][q] * v[u][q];
+        const __nv_bfloat16 o = __float2bfloat16_rn(acc);
+        a.out[((size_t)r * H + split + (i0 + u) * S) * D + tid] = *reinterpret_cast<const uint16_t*>(&o);
+      }
+    }
+    cluster.sync();                                // no CTA leaves while another reads its partials
   }
   tc_fence_before();
   __syncthreads();
@@ -665,50 +736,69 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   }
 }
 
-// Log-sum-exp merge of the split partials: one block per (row, head).
-__global__ void __launch_bounds__(128) k_attn_merge(AttnArgs a) {
-  pdl_trigger();
-  pdl_wait();                    // the partials come from the previous kernel
-  const int r = blockIdx.x / a.H, h = blockIdx.x % a.H;
-  const int H = a.H, S = a.splits;
-  const float* base = a.part + (size_t)r * S * H * (D + 2);
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, base[(size_t)s * H * (D + 2) + (size_t)H * D + h]);
-  float L = 0.0f;
-  float wts[kMaxTiles];
-  for (int s = 0; s < S; ++s) {
-    const float ms = base[(size_t)s * H * (D + 2) + (size_t)H * D + h];
-    const float ls = base[(size_t)s * H * (D + 2) + (size_t)H * D + H + h];
-    wts[s] = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
-    L += wts[s] * ls;
+constexpr int kMaxDevices = 64;
+
+// Clusters of s CTAs (one CTA per SM) that the device holds at once.  A GPC
+// holds whole clusters, so s times this can fall short of the SM count.
+// Queried once per (device, s); 0 when the query fails.
+template <int H>
+int clusters_resident(int s, size_t smem) {
+  static std::atomic<int> known[kMaxDevices][kMaxTiles + 1];   // value + 1; 0 = not yet asked
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int v = known[dev][s].load(std::memory_order_relaxed);
+    if (v > 0) return v - 1;
   }
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.0f;
-    for (int s = 0; s < S; ++s) acc += wts[s] * base[(size_t)s * H * (D + 2) + (size_t)h * D + d];
-    const float o = L > 0.0f ? acc / L : 0.0f;
-    const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-    a.out[((size_t)r * H + h) * D + d] = *reinterpret_cast<const uint16_t*>(&ob);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = s;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_sparse_attn<H>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
   }
-  if (threadIdx.x == 0 && a.lse)
-    a.lse[(size_t)r * H + h] = (L > 0.0f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  if (dev >= 0 && dev < kMaxDevices) known[dev][s].store(n + 1, std::memory_order_relaxed);
+  return n;
 }
 
 template <int H>
-cudaError_t launch_h(const AttnArgs& a, cudaStream_t stream) {
+cudaError_t launch_h(const AttnArgs& args, cudaStream_t stream) {
   const size_t smem = sizeof(AttnSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(k_sparse_attn<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_dependent(k_sparse_attn<H>, dim3(a.num_rows * a.splits), dim3(kThreads), smem, stream, a);
-  if (e != cudaSuccess || a.splits == 1) return e;
-  return launch_dependent(k_attn_merge, dim3(a.num_rows * a.H), dim3(128), 0, stream, a);
+  // fewer splits where the rows' clusters would not all be resident at once
+  AttnArgs a = args;
+  while (a.splits > 1 && a.num_rows > clusters_resident<H>(a.splits, smem)) --a.splits;
+  if (a.splits == 1)
+    return launch_dependent(k_sparse_attn<H>, dim3(a.num_rows), dim3(kThreads), smem, stream, a);
+  // a row's splits form one cluster, which merges their partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_rows * a.splits, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_sparse_attn<H>, a);
 }
 
 }  // namespace
-
-size_t attn_partial_bytes(int32_t num_rows, int32_t n_heads, int32_t splits) {
-  if (splits <= 1) return 0;
-  return sizeof(float) * (size_t)num_rows * splits * n_heads * (D + 2);
-}
 
 int32_t attn_choose_splits(int32_t num_rows, int num_sms) {
   if (num_rows <= 0) return 1;

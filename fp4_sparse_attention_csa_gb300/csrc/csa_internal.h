@@ -99,12 +99,10 @@ struct AttnArgs {
   float softmax_scale;
   uint16_t* out;            // bf16 [R, H, 512]
   float* lse;               // [R, H] or null
-  float* part;              // split partials (o, m, l) or null when splits == 1
   int32_t splits;
   uint32_t* status;
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
-size_t attn_partial_bytes(int32_t num_rows, int32_t n_heads, int32_t splits);
 int32_t attn_choose_splits(int32_t num_rows, int num_sms);
 
 }  // namespace csa

@@ -141,7 +141,10 @@ typedef struct {
   int32_t        max_rows_per_req; /* host bound on rows sharing one request      */
 } csa_rows_t;
 
-/* Workspace sizing: op = one of the CSA_OP_* values. */
+/* Workspace sizing: op = one of the CSA_OP_* values; bytes for num_rows rows
+ * of at most max_entries entries each.  n_heads is part of the signature so a
+ * caller need not change when a size comes to depend on it; none does now
+ * (attention's split partials are merged in shared memory).  0 = bad op. */
 enum { CSA_OP_APPEND = 0, CSA_OP_INDEX_SCORE = 1, CSA_OP_TOPK = 2,
        CSA_OP_SPARSE_ATTN = 3, CSA_OP_DECODE = 4 };
 CSA_API size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int32_t n_heads);

@@ -218,6 +218,33 @@ def test_sparse_attention_matches_oracle(H, ctx, rows):
     print(f"attention H={H}: max normalised err {norm:.2e}, rel L2 {l2:.2e}")
 
 
+@pytest.mark.parametrize("R", [30, 40, 60])
+def test_attention_cluster_split_counts(R):
+    """Row counts that give 5, 3 and 2 splits per row: the row's CTAs run as one
+    cluster and merge their partials in shared memory (5-CTA clusters may be cut
+    to fewer splits where they would not all be resident at once)."""
+    ctx = list(np.random.default_rng(R).integers(2100, 4000, R))
+    wl = W.custom("attn_cl", 90 + R, ctx, [1] * R, H=64, Hi=16, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    st.step_decode(s)
+    rc, flags = csa.csa_check_device_status(s["ws"])
+    assert rc == 0 and flags == 0, flags
+    ref = oracle.build_cache(wl)
+    q_idx, w, q = wl.step_queries()
+    out, lse, topk, scores = oracle.decode(ref, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale, threads=8)
+    gt = s["topk"].cpu().numpy()
+    n = wl.row_entries()
+    for r in range(wl.R):
+        parity.check_topk_row(gt[r], scores[r], int(n[r]))
+        if not np.array_equal(gt[r], topk[r]):
+            out[r], lse[r] = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], gt[r], q[r], wl.softmax_scale)
+    norm, l2 = parity.check_attention(s["out"].float().cpu().numpy(), out, s["lse"].cpu().numpy(), lse)
+    print(f"attention R={R}: max normalised err {norm:.2e}, rel L2 {l2:.2e}")
+
+
 def test_attention_many_rows_single_split():
     """Enough rows that each row runs in one CTA (no split merge)."""
     ctx = list(np.random.default_rng(7).integers(600, 1400, 160))
