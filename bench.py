@@ -37,22 +37,32 @@ CFG_OF = {"cfg1": 1, "cfg2": 2, "cfg3": 3, "cfg4": 4, "cfg5": 5, "cfg6": 6}
 # launch (k_score_prep + k_index_score) on the serving-batch workload, from one
 # ncu capture (profiles/k_index_score_serving_batch.txt).  It is reported only
 # while the kernel sources still hash to the fingerprint taken with it.
-SCORE_TRAFFIC = {"workload": "cfg4", "fingerprint": "33c720e8cce27143", "bytes": 2129408 + 160369664 + 5589504}
+SCORE_TRAFFIC = {"workload": "cfg4", "fingerprint": "53f43aa94921402a", "bytes": 2129408 + 160369664 + 5589504}
 
 
 def score_fingerprint():
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "fp4_sparse_attention_csa_gb300", "csrc")
-    for f in ("score.cu", "csa_device.cuh"):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(fh.read())
-    # of the internal header, the part the score kernel compiles against: up to
-    # its launcher's declaration (the other kernels' argument blocks follow it)
+    # the score kernels' device code, comments and blank lines left out:
+    # score.cu up to its host-side launcher, the device helpers, and the
+    # argument block from the internal header
+    def code(text):
+        out = []
+        for line in text.decode().splitlines():
+            line = line.split("//", 1)[0].rstrip()
+            if line:
+                out.append(line)
+        return "\n".join(out).encode()
+    with open(os.path.join(d, "score.cu"), "rb") as fh:
+        src = fh.read()
+    h.update(code(src[:src.index(b"size_t score_ws_bytes(")]))
+    with open(os.path.join(d, "csa_device.cuh"), "rb") as fh:
+        h.update(code(fh.read()))
     with open(os.path.join(d, "csa_internal.h"), "rb") as fh:
         hdr = fh.read()
-    end = hdr.index(b"launch_index_score")
-    h.update(hdr[:hdr.index(b"\n", end) + 1])
+    beg = hdr.index(b"struct ScoreArgs")
+    h.update(code(hdr[beg:hdr.index(b"};", beg) + 2]))
     return h.hexdigest()[:16]
 
 

@@ -101,7 +101,7 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
 
 csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                       const int32_t* topk, int32_t H, const void* q, float softmax_scale, void* out, float* lse,
-                      void* ws, cudaStream_t stream) {
+                      void* ws, Order order, cudaStream_t stream) {
   AttnArgs a;
   a.kv_pool = static_cast<const uint8_t*>(cache->kv_pool);
   a.page_table = cache->page_table;
@@ -123,7 +123,7 @@ csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, cons
   a.lse = lse;
   a.splits = attn_choose_splits(rows->num_rows, num_sms());
   a.status = static_cast<uint32_t*>(ws);
-  return from_cuda(launch_sparse_attn(a, stream));
+  return from_cuda(launch_sparse_attn(a, order, stream));
 }
 
 }  // namespace
@@ -234,7 +234,7 @@ csa_status_t csa_topk(int32_t num_rows, const float* scores, int32_t ld, const i
   a.max_n = max_n;
   a.out = out_idx;
   a.status = static_cast<uint32_t*>(ws);
-  return from_cuda(launch_topk(a, stream));
+  return from_cuda(launch_topk(a, Order::kStream, stream));
 }
 
 csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
@@ -248,7 +248,7 @@ csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* windo
   if (rows->num_rows == 0) return CSA_OK;
   if (!topk_idx || !q || !out || !aligned(q, 16) || !aligned(out, 16)) return CSA_ERR_INVALID_ARGUMENT;
   if (!ws || ws_bytes < kStatusBytes || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
-  return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, ws, stream);
+  return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, ws, Order::kStream, stream);
 }
 
 csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
@@ -281,8 +281,8 @@ csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window, co
   t.max_n = rows->max_entries;
   t.out = topk;
   t.status = static_cast<uint32_t*>(ws);
-  if ((s = from_cuda(launch_topk(t, stream))) != CSA_OK) return s;
-  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, ws, stream);
+  if ((s = from_cuda(launch_topk(t, Order::kChained, stream))) != CSA_OK) return s;
+  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, ws, Order::kChained, stream);
 }
 
 csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out) {

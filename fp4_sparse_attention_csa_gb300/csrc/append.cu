@@ -95,7 +95,6 @@ __device__ __forceinline__ void rope_last64(float (&v)[K], const float* cs, cons
 }
 
 __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
-  pdl_trigger();                 // the score step's prep reads nothing this kernel writes
   // request lookup table: tok_off staged once per block (one coalesced read
   // instead of a chain of dependent global loads per token)
   __shared__ int32_t s_off[kOffStage + 1];

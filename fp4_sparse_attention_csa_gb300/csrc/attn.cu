@@ -362,9 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const bool win_here = hw && t_beg == 0 && t_end > 0;
   const int m_beg = max(t_beg - hw, 0), m_end = max(t_end - hw, 0);   // main tiles [m_beg, m_end)
 
-  // ---- prologue, overlapping the previous kernel's tail: barriers, TMEM;
-  // then wait for it (the selected indices, and transitively the cache
-  // append of this step, are ready from there on)
+  // ---- prologue, overlapping the previous kernel's tail when chained after
+  // the top-k of the same call: barriers, TMEM; then wait for it (the
+  // selected indices are ready from there on).  The row inputs read above
+  // and the cache were complete before the call's first kernel started.
   pdl_trigger();
   if (tid == 0) {
     mbar_init(&sm.s_bar, 1);
@@ -771,7 +772,7 @@ int clusters_resident(int s, size_t smem) {
 }
 
 template <int H>
-cudaError_t launch_h(const AttnArgs& args, cudaStream_t stream) {
+cudaError_t launch_h(const AttnArgs& args, Order order, cudaStream_t stream) {
   const size_t smem = sizeof(AttnSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(k_sparse_attn<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -779,7 +780,7 @@ cudaError_t launch_h(const AttnArgs& args, cudaStream_t stream) {
   AttnArgs a = args;
   while (a.splits > 1 && a.num_rows > clusters_resident<H>(a.splits, smem)) --a.splits;
   if (a.splits == 1)
-    return launch_dependent(k_sparse_attn<H>, dim3(a.num_rows), dim3(kThreads), smem, stream, a);
+    return launch_kernel(order, k_sparse_attn<H>, dim3(a.num_rows), dim3(kThreads), smem, stream, a);
   // a row's splits form one cluster, which merges their partials
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_rows * a.splits, 1, 1);
@@ -791,10 +792,8 @@ cudaError_t launch_h(const AttnArgs& args, cudaStream_t stream) {
   attr[0].val.clusterDim.x = a.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1 + order_attr(order, attr + 1);
   return cudaLaunchKernelEx(&cfg, k_sparse_attn<H>, a);
 }
 
@@ -806,12 +805,12 @@ int32_t attn_choose_splits(int32_t num_rows, int num_sms) {
   return s < 1 ? 1 : (s > kMaxTiles ? kMaxTiles : s);
 }
 
-cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
+cudaError_t launch_sparse_attn(const AttnArgs& a, Order order, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;
   switch (a.H) {
-    case 16: return launch_h<16>(a, stream);
-    case 32: return launch_h<32>(a, stream);
-    case 64: return launch_h<64>(a, stream);
+    case 16: return launch_h<16>(a, order, stream);
+    case 32: return launch_h<32>(a, order, stream);
+    case 64: return launch_h<64>(a, order, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -8,23 +8,39 @@
 
 namespace csa {
 
-// Launch with programmatic dependent launch: the kernel may start while the
-// previous kernel in the stream is still running; it runs its prologue, then
-// griddepcontrol.wait (pdl_wait) blocks until that kernel has completed and
-// its memory is visible, before anything it produced is read.
+// How a kernel is ordered after the work before it in its stream.
+//  kStream   plain stream order: the kernel starts once everything enqueued
+//            before it has completed.  The first kernel of every public call
+//            is launched so; from then on the call's inputs are complete and
+//            no earlier call still reads the workspace.
+//  kChained  programmatic dependent launch, for the later kernels of a call:
+//            the kernel may start while the previous kernel of the same call is
+//            still running; it runs its prologue (and may read the call's
+//            inputs), then griddepcontrol.wait (pdl_wait) blocks until that
+//            kernel has completed and its memory is visible, before anything
+//            it produced is read.  (griddepcontrol.wait returns at once in a
+//            kStream launch.)
+enum class Order { kStream, kChained };
+
+// Adds the launch attribute for `order` at attr[0]; returns how many it added.
+inline unsigned order_attr(Order order, cudaLaunchAttribute* attr) {
+  if (order != Order::kChained) return 0;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  return 1;
+}
+
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                    cudaStream_t stream, Args... args) {
+inline cudaError_t launch_kernel(Order order, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = order_attr(order, attr);
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
@@ -82,7 +98,7 @@ struct TopkArgs {
   int32_t* out;            // [R, 512]
   uint32_t* status;
 };
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
+cudaError_t launch_topk(const TopkArgs& a, Order order, cudaStream_t stream);
 
 struct AttnArgs {
   const uint8_t* kv_pool;
@@ -102,7 +118,7 @@ struct AttnArgs {
   int32_t splits;
   uint32_t* status;
 };
-cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_sparse_attn(const AttnArgs& a, Order order, cudaStream_t stream);
 int32_t attn_choose_splits(int32_t num_rows, int num_sms);
 
 }  // namespace csa

@@ -153,9 +153,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* sm_w
   return off + x - v;
 }
 
-// Reads only the step's inputs, so it may run beside the cache append; it
-// waits for the previous kernel before it exits, so that everything after it
-// also sees that kernel's writes.
+// The first kernel of its call (plain stream order): everything before it in
+// the stream has completed when it starts, so its griddepcontrol.wait calls
+// return at once; they keep it correct under a chained launch too.
 __global__ void __launch_bounds__(128) k_score_prep(ScoreArgs a, uint8_t* ws) {
   pdl_trigger();
   const int R = a.num_rows, Hi = a.Hi, Hp = hi_pad(Hi);
@@ -623,12 +623,14 @@ cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, cudaStream_t str
   uint8_t* ws = reinterpret_cast<uint8_t*>(a.status);
   ScoreArgs ap = a;
   ap.grid = num_sms < kMaxGrid ? num_sms : kMaxGrid;
-  cudaError_t e = launch_dependent(k_score_prep, dim3(1 + a.num_rows), dim3(128), 0, stream, ap, ws);
+  // the prep is the call's first kernel: plain stream order (it reads the
+  // call's inputs and overwrites the workspace at once)
+  cudaError_t e = launch_kernel(Order::kStream, k_score_prep, dim3(1 + a.num_rows), dim3(128), 0, stream, ap, ws);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(ScoreSmem) + 1024;
   e = cudaFuncSetAttribute(k_index_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(k_index_score, dim3(ap.grid), dim3(kThreads), smem, stream, ap, ws);
+  return launch_kernel(Order::kChained, k_index_score, dim3(ap.grid), dim3(kThreads), smem, stream, ap, ws);
 }
 
 }  // namespace csa

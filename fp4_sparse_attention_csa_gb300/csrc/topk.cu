@@ -773,7 +773,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
+cudaError_t launch_topk(const TopkArgs& a, Order order, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;
   if (a.max_n <= kRowMax && (a.ld % 4) == 0 && ((uintptr_t)a.scores & 15u) == 0) {
     // CTAs per row: about one per 8K entries, up to 8, at most two CTAs per
@@ -802,10 +802,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
     attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1 + order_attr(order, attr + 1);
     return cudaLaunchKernelEx(&cfg, kern, a);
   }
   int C = (a.max_n + kStageMax - 1) / kStageMax;
@@ -828,10 +826,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1 + order_attr(order, attr + 1);
   return cudaLaunchKernelEx(&cfg, k_topk, a, C, slice_cap, staged);
 }
 

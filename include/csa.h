@@ -64,6 +64,12 @@
  *    skipped (outputs zero / -1) and a flag is OR-ed into the status word at
  *    the head of the workspace; read it with csa_check_device_status().
  *  - Calls that run concurrently need distinct workspaces.
+ *  - Stream order: a call's first kernel is an ordinary launch, so it starts
+ *    after all work enqueued before it on `stream` has completed; inputs may
+ *    come from any earlier work on the stream.  The later kernels of the same
+ *    call (csa_index_score, csa_decode) use programmatic dependent launch:
+ *    each may start while the call's previous kernel finishes and waits for
+ *    it before reading anything that kernel wrote.
  */
 #ifndef CSA_H
 #define CSA_H
