@@ -1,5 +1,6 @@
-"""Benchmark of one CSA decode step on GB300: csa_append of the step's new
-tokens + csa_decode (indexer score -> exact top-512 -> sparse attention), on
+"""Benchmark of one CSA decode step on GB300, one csa_step call: csa_append of
+the step's new tokens + csa_decode (indexer score -> exact top-512 -> sparse
+attention), on
 the serving-batch workload (128 requests x 1 row, 64 heads, log-uniform
 4k-128k token contexts pooled 2:1, shuffled pages).
 
@@ -258,8 +259,7 @@ def main():
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
 
     def step():
-        st.step_append(s)
-        st.step_decode(s)
+        st.step(s)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -351,8 +351,7 @@ def main():
                 stream.wait_event(up[i])
                 if i >= 2:
                     stream.wait_event(down[i - 2])            # its result has left the device
-                st.step_append(b)
-                st.step_decode(b)
+                st.step(b)
                 done[i].record(stream)
                 with torch.cuda.stream(back):
                     back.wait_event(done[i])
@@ -403,7 +402,8 @@ def main():
                    "path_unique_bytes": ab["total"], "path_gbs": path_gbs,
                    "path_frac_of_hbm": path_gbs / peak, "path_frac_of_8tbs": path_gbs / 8000.0,
                    "bytes": ab, "parallelism": f"replicas x{world}",
-                   "append": "csa_append_compress (RMSNorm + RoPE)" if args.compress else "csa_append"},
+                   "append": "csa_append_compress (RMSNorm + RoPE)" if args.compress else "csa_append",
+                   "call": "csa_step (append + decode in one call)"},
         "roofline": {"bound": "hbm", "kernel": "index score (k_score_prep + k_index_score)",
                      "achieved": score_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": score_gbs / peak, "traffic": traffic,

@@ -75,11 +75,13 @@ def lib():
             L.csa_sparse_attn.argtypes = [vp, vp, vp, vp, i32, vp, f32, vp, vp, vp, sz, vp]
             L.csa_decode.argtypes = [vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
             L.csa_index_score_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp]
+            L.csa_step.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp,
+                                   vp, vp, sz, vp]
             L.csa_check_device_status.argtypes = [vp, vp, C.POINTER(C.c_uint32)]
             L.csa_status_string.argtypes = [i32]
             L.csa_status_string.restype = C.c_char_p
-            for fn in ("csa_append", "csa_index_score", "csa_topk", "csa_sparse_attn", "csa_decode",
-                       "csa_index_score_noalloc", "csa_check_device_status"):
+            for fn in ("csa_append", "csa_append_compress", "csa_index_score", "csa_topk", "csa_sparse_attn",
+                       "csa_decode", "csa_step", "csa_index_score_noalloc", "csa_check_device_status"):
                 getattr(L, fn).restype = C.c_int
             _lib = L
     return _lib
@@ -182,6 +184,17 @@ def csa_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_s
                           int(n_idx_heads), _ptr(q_idx), _ptr(w), int(n_heads), _ptr(q), float(softmax_scale),
                           _ptr(out), _ptr(lse), _ptr(topk_out), _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "csa_decode")
+
+
+def csa_step(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, compress, rows, n_idx_heads,
+             q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, ws, stream=None):
+    """csa_append(_compress) then csa_decode in one call (compress may be None)."""
+    rc = lib().csa_step(C.byref(cache), C.byref(window) if window is not None else None, _ptr(pos0),
+                        _ptr(tok_off), int(total_tokens), _ptr(kv_in), _ptr(idx_in), _ptr(pending),
+                        C.byref(compress) if compress is not None else None, C.byref(rows), int(n_idx_heads),
+                        _ptr(q_idx), _ptr(w), int(n_heads), _ptr(q), float(softmax_scale), _ptr(out), _ptr(lse),
+                        _ptr(topk_out), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "csa_step")
 
 
 def csa_check_device_status(ws, stream=None):

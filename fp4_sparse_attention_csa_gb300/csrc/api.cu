@@ -68,7 +68,8 @@ DecodeLayout decode_layout(int32_t R, int32_t max_entries) {
 csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
 csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t Hi, const void* q_idx,
-                       const float* w, float* scores, int64_t ld, void* ws, cudaStream_t stream) {
+                       const float* w, float* scores, int64_t ld, void* ws, Order prep_order,
+                       cudaStream_t stream) {
   ScoreArgs a;
   a.idx_pool = cache->idx_pool;
   a.page_table = cache->page_table;
@@ -96,7 +97,7 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
   a.scores = scores;
   a.ld = ld;
   a.status = static_cast<uint32_t*>(ws);
-  return from_cuda(launch_index_score(a, num_sms(), stream));
+  return from_cuda(launch_index_score(a, num_sms(), prep_order, stream));
 }
 
 csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
@@ -126,39 +127,11 @@ csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, cons
   return from_cuda(launch_sparse_attn(a, order, stream));
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int32_t n_heads) {
-  if (num_rows < 0 || max_entries < 0) return 0;
-  (void)n_heads;                     // no size depends on the head count
-  switch (op) {
-    case CSA_OP_APPEND:
-    case CSA_OP_TOPK:
-      return kStatusBytes;
-    case CSA_OP_INDEX_SCORE:
-      return align_up(score_ws_bytes(num_rows, CSA_MAX_IDX_HEADS));
-    case CSA_OP_SPARSE_ATTN:
-      return kStatusBytes;
-    case CSA_OP_DECODE:
-      return decode_layout(num_rows, max_entries).end;
-    default:
-      return 0;
-  }
-}
-
-csa_status_t csa_append(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
-                        const int32_t* tok_off, int32_t total_tokens, const void* kv_in, const void* idx_in,
-                        void* pending, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  return csa_append_compress(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, nullptr, ws,
-                             ws_bytes, stream);
-}
-
-csa_status_t csa_append_compress(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
-                                 const int32_t* tok_off, int32_t total_tokens, const void* kv_in,
-                                 const void* idx_in, void* pending, const csa_compress_t* compress, void* ws,
-                                 size_t ws_bytes, cudaStream_t stream) {
+// Validates csa_append's arguments and fills the kernel's; no launch.
+csa_status_t append_args(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
+                         const int32_t* tok_off, int32_t total_tokens, const void* kv_in, const void* idx_in,
+                         void* pending, const csa_compress_t* compress, void* ws, size_t ws_bytes,
+                         AppendArgs* out) {
   csa_status_t s = check_cache(cache);
   if (s != CSA_OK) return s;
   if ((s = check_window(window, 1)) != CSA_OK) return s;
@@ -198,6 +171,91 @@ csa_status_t csa_append_compress(const csa_cache_t* cache, const csa_window_t* w
       return CSA_ERR_INVALID_ARGUMENT;
     if (!(compress->eps >= 0.0f)) return CSA_ERR_INVALID_ARGUMENT;
   }
+  *out = a;
+  return CSA_OK;
+}
+
+csa_status_t check_decode(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
+                          int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
+                          const void* out, const void* ws, size_t ws_bytes) {
+  csa_status_t s = check_cache(cache);
+  if (s != CSA_OK) return s;
+  if ((s = check_rows(rows, cache)) != CSA_OK) return s;
+  if ((s = check_window(window, rows->max_rows_per_req)) != CSA_OK) return s;
+  if (n_idx_heads < 1 || n_idx_heads > CSA_MAX_IDX_HEADS || n_heads < 1 || n_heads > CSA_MAX_HEADS)
+    return CSA_ERR_UNSUPPORTED;
+  if (rows->num_rows == 0) return CSA_OK;
+  if (!q_idx || !w || !q || !out || !aligned(q_idx, 16) || !aligned(q, 16) || !aligned(out, 16))
+    return CSA_ERR_INVALID_ARGUMENT;
+  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries);
+  if (!ws || ws_bytes < L.end || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  return CSA_OK;
+}
+
+// index score -> top-512 -> attention, arguments already checked; `first` is
+// the order of the score prep, the first of these kernels.
+csa_status_t run_decode(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
+                        int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
+                        float softmax_scale, void* out, float* lse, int32_t* topk_out, void* ws, Order first,
+                        cudaStream_t stream) {
+  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* scores = reinterpret_cast<float*>(base + L.scores);
+  int32_t* topk = topk_out ? topk_out : reinterpret_cast<int32_t*>(base + L.topk);
+  const int64_t ld = (int64_t)scores_ld(rows->max_entries);
+  csa_status_t s;
+  if ((s = run_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, first, stream)) != CSA_OK) return s;
+  TopkArgs t;
+  t.scores = scores;
+  t.ld = ld;
+  t.num_rows = rows->num_rows;
+  t.n_valid = nullptr;
+  t.row_pos = rows->row_pos;
+  t.P = cache->pool_ratio;
+  t.max_n = rows->max_entries;
+  t.out = topk;
+  t.status = static_cast<uint32_t*>(ws);
+  if ((s = from_cuda(launch_topk(t, Order::kChained, stream))) != CSA_OK) return s;
+  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, ws, Order::kChained, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int32_t n_heads) {
+  if (num_rows < 0 || max_entries < 0) return 0;
+  (void)n_heads;                     // no size depends on the head count
+  switch (op) {
+    case CSA_OP_APPEND:
+    case CSA_OP_TOPK:
+      return kStatusBytes;
+    case CSA_OP_INDEX_SCORE:
+      return align_up(score_ws_bytes(num_rows, CSA_MAX_IDX_HEADS));
+    case CSA_OP_SPARSE_ATTN:
+      return kStatusBytes;
+    case CSA_OP_DECODE:
+      return decode_layout(num_rows, max_entries).end;
+    default:
+      return 0;
+  }
+}
+
+csa_status_t csa_append(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
+                        const int32_t* tok_off, int32_t total_tokens, const void* kv_in, const void* idx_in,
+                        void* pending, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return csa_append_compress(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, nullptr, ws,
+                             ws_bytes, stream);
+}
+
+csa_status_t csa_append_compress(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
+                                 const int32_t* tok_off, int32_t total_tokens, const void* kv_in,
+                                 const void* idx_in, void* pending, const csa_compress_t* compress, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  AppendArgs a;
+  const csa_status_t s =
+      append_args(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, compress, ws, ws_bytes, &a);
+  if (s != CSA_OK) return s;
   return from_cuda(launch_append(a, stream));
 }
 
@@ -214,7 +272,7 @@ csa_status_t csa_index_score(const csa_cache_t* cache, const csa_rows_t* rows, i
   if (ld < rows->max_entries || ld < 1) return CSA_ERR_INVALID_ARGUMENT;
   if (!ws || ws_bytes < score_ws_bytes(rows->num_rows, CSA_MAX_IDX_HEADS) || !aligned(ws, 256))
     return CSA_ERR_WORKSPACE_TOO_SMALL;
-  return run_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, stream);
+  return run_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, Order::kStream, stream);
 }
 
 csa_status_t csa_topk(int32_t num_rows, const float* scores, int32_t ld, const int32_t* n_valid, int32_t max_n,
@@ -255,35 +313,33 @@ csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window, co
                         int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
                         float softmax_scale, void* out, float* lse, int32_t* topk_out, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
-  csa_status_t s = check_cache(cache);
-  if (s != CSA_OK) return s;
-  if ((s = check_rows(rows, cache)) != CSA_OK) return s;
-  if ((s = check_window(window, rows->max_rows_per_req)) != CSA_OK) return s;
-  if (n_idx_heads < 1 || n_idx_heads > CSA_MAX_IDX_HEADS || n_heads < 1 || n_heads > CSA_MAX_HEADS)
-    return CSA_ERR_UNSUPPORTED;
-  if (rows->num_rows == 0) return CSA_OK;
-  if (!q_idx || !w || !q || !out || !aligned(q_idx, 16) || !aligned(q, 16) || !aligned(out, 16))
-    return CSA_ERR_INVALID_ARGUMENT;
-  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries);
-  if (!ws || ws_bytes < L.end || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  float* scores = reinterpret_cast<float*>(base + L.scores);
-  int32_t* topk = topk_out ? topk_out : reinterpret_cast<int32_t*>(base + L.topk);
-  const int64_t ld = (int64_t)scores_ld(rows->max_entries);
-  if ((s = run_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, stream)) != CSA_OK) return s;
-  TopkArgs t;
-  t.scores = scores;
-  t.ld = ld;
-  t.num_rows = rows->num_rows;
-  t.n_valid = nullptr;
-  t.row_pos = rows->row_pos;
-  t.P = cache->pool_ratio;
-  t.max_n = rows->max_entries;
-  t.out = topk;
-  t.status = static_cast<uint32_t*>(ws);
-  if ((s = from_cuda(launch_topk(t, Order::kChained, stream))) != CSA_OK) return s;
-  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, ws, Order::kChained, stream);
+  const csa_status_t s = check_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, out, ws, ws_bytes);
+  if (s != CSA_OK || rows->num_rows == 0) return s;
+  return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, ws,
+                    Order::kStream, stream);
 }
+
+csa_status_t csa_step(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
+                      const int32_t* tok_off, int32_t total_tokens, const void* kv_in, const void* idx_in,
+                      void* pending, const csa_compress_t* compress, const csa_rows_t* rows, int32_t n_idx_heads,
+                      const void* q_idx, const float* w, int32_t n_heads, const void* q, float softmax_scale,
+                      void* out, float* lse, int32_t* topk_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  AppendArgs a;
+  csa_status_t s =
+      append_args(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, compress, ws, ws_bytes, &a);
+  if (s != CSA_OK) return s;
+  if ((s = check_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, out, ws, ws_bytes)) != CSA_OK)
+    return s;
+  if ((s = from_cuda(launch_append(a, stream))) != CSA_OK) return s;
+  if (rows->num_rows == 0) return CSA_OK;
+  // With an append kernel in flight, the score prep is chained to it: it reads
+  // only the step's inputs and the score workspace, which the append does not
+  // touch, and it waits for the append before it exits.  Without one it is the
+  // call's first kernel.
+  return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, ws,
+                    total_tokens > 0 ? Order::kChained : Order::kStream, stream);
+}
+
 
 csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out) {
   if (!ws || !flags_out) return CSA_ERR_INVALID_ARGUMENT;
@@ -364,5 +420,5 @@ extern "C" csa_status_t csa_index_score_noalloc(const csa_cache_t* cache, const 
   // every call starts with a clear status word; the rest of the scratch is
   // fully rewritten by the score step before it is read
   if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return CSA_ERR_CUDA;
-  return run_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, stream);
+  return run_score(cache, rows, n_idx_heads, q_idx, w, scores, ld, ws, Order::kStream, stream);
 }

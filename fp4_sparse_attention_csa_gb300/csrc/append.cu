@@ -95,6 +95,7 @@ __device__ __forceinline__ void rope_last64(float (&v)[K], const float* cs, cons
 }
 
 __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
+  pdl_trigger();                 // csa_step's score prep may start beside it (it reads nothing written here)
   // request lookup table: tok_off staged once per block (one coalesced read
   // instead of a chain of dependent global loads per token)
   __shared__ int32_t s_off[kOffStage + 1];

@@ -85,7 +85,8 @@ struct ScoreArgs {
   uint32_t* status;                    // head of the workspace
   int32_t grid;                        // score CTAs (set by the launcher)
 };
-cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, cudaStream_t stream);
+// prep_order: the score prep's order (kStream when it is its call's first kernel)
+cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, Order prep_order, cudaStream_t stream);
 
 struct TopkArgs {
   const float* scores;

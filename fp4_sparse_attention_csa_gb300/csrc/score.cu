@@ -153,9 +153,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* sm_w
   return off + x - v;
 }
 
-// The first kernel of its call (plain stream order): everything before it in
-// the stream has completed when it starts, so its griddepcontrol.wait calls
-// return at once; they keep it correct under a chained launch too.
+// Launched in plain stream order as its call's first kernel, or chained after
+// the step's cache append (csa_step), beside which it runs: it reads only the
+// call's inputs and writes only the score workspace.  It waits for the
+// previous kernel before it exits, so that everything after it also sees
+// that kernel's writes.
 __global__ void __launch_bounds__(128) k_score_prep(ScoreArgs a, uint8_t* ws) {
   pdl_trigger();
   const int R = a.num_rows, Hi = a.Hi, Hp = hi_pad(Hi);
@@ -618,14 +620,15 @@ size_t score_ws_bytes(int32_t R, int32_t Hi) {
 
 int score_group_rows(int32_t Hi) { return kMaxN / hi_pad(Hi); }
 
-cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, Order prep_order, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;
   uint8_t* ws = reinterpret_cast<uint8_t*>(a.status);
   ScoreArgs ap = a;
   ap.grid = num_sms < kMaxGrid ? num_sms : kMaxGrid;
-  // the prep is the call's first kernel: plain stream order (it reads the
-  // call's inputs and overwrites the workspace at once)
-  cudaError_t e = launch_kernel(Order::kStream, k_score_prep, dim3(1 + a.num_rows), dim3(128), 0, stream, ap, ws);
+  // the prep reads the call's inputs and overwrites the workspace at once:
+  // plain stream order when it is the call's first kernel, chained only after
+  // a kernel of the same call that touches neither (the step's append)
+  cudaError_t e = launch_kernel(prep_order, k_score_prep, dim3(1 + a.num_rows), dim3(128), 0, stream, ap, ws);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(ScoreSmem) + 1024;
   e = cudaFuncSetAttribute(k_index_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -9,7 +9,7 @@ import numpy as np
 import torch
 
 from . import (KV_PAGE_BYTES, IDX_PAGE_BYTES, OP_APPEND, OP_DECODE, csa_append, csa_append_compress,
-               make_compress, csa_decode,
+               make_compress, csa_decode, csa_step,
                csa_workspace_size, make_cache, make_rows, make_window)
 
 
@@ -138,6 +138,14 @@ class DeviceState:
             return
         csa_append(self.cache, self.window, s["pos0"], s["tok_off"], self.wl.R, s["kv_new"], s["idx_new"],
                    self.pending, self.ws_append, stream)
+
+    def step(self, s, stream=None):
+        """The step's append and decode in one csa_step call (the append's
+        device-side faults land in the decode workspace s["ws"])."""
+        wl = self.wl
+        csa_step(self.cache, self.window, s["pos0"], s["tok_off"], wl.R, s["kv_new"], s["idx_new"], self.pending,
+                 getattr(self, "compress", None), s["rows"], wl.Hi, s["q_idx"], s["w"], wl.H, s["q"],
+                 wl.softmax_scale, s["out"], s["lse"], s["topk"], s["ws"], stream)
 
     def step_decode(self, s, stream=None):
         wl = self.wl

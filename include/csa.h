@@ -67,9 +67,9 @@
  *  - Stream order: a call's first kernel is an ordinary launch, so it starts
  *    after all work enqueued before it on `stream` has completed; inputs may
  *    come from any earlier work on the stream.  The later kernels of the same
- *    call (csa_index_score, csa_decode) use programmatic dependent launch:
- *    each may start while the call's previous kernel finishes and waits for
- *    it before reading anything that kernel wrote.
+ *    call (csa_index_score, csa_decode, csa_step) use programmatic dependent
+ *    launch: each may start while the call's previous kernel finishes and
+ *    waits for it before reading anything that kernel wrote.
  */
 #ifndef CSA_H
 #define CSA_H
@@ -275,6 +275,26 @@ CSA_API csa_status_t csa_append_compress(const csa_cache_t* cache, const csa_win
                                          const void* kv_in, const void* idx_in, void* pending,
                                          const csa_compress_t* compress, void* ws, size_t ws_bytes,
                                          cudaStream_t stream);
+
+/* csa_step -- one decode step of a layer in one call: csa_append_compress of
+ * the step's new tokens (compress nullable: plain csa_append), then
+ * csa_decode of its query rows, on `stream`.  Arguments and results are those
+ * of the two calls made back to back, except that ws is csa_decode's
+ * workspace and also takes the append's device-side faults.  In one call the
+ * score step's preparation (indexer-q quantisation, segment table) runs beside
+ * the append kernel: it reads only the step's inputs and writes only the score
+ * workspace, which the append does not touch.  ([SGL] "Small-operator fusion
+ * and GEMV": a decode step is a chain of short kernels; "mHC: reduction fusion
+ * and overlap": the compressor's and the indexer's work overlapped.)
+ * All arguments are checked before the first launch. */
+CSA_API csa_status_t csa_step(const csa_cache_t* cache, const csa_window_t* window,
+                      const int32_t* pos0, const int32_t* tok_off, int32_t total_tokens,
+                      const void* kv_in, const void* idx_in, void* pending,
+                      const csa_compress_t* compress, const csa_rows_t* rows,
+                      int32_t n_idx_heads, const void* q_idx, const float* w,
+                      int32_t n_heads, const void* q, float softmax_scale,
+                      void* out, float* lse, int32_t* topk_out,
+                      void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, returns the status word's flags in *flags_out (host)
  * and clears it.  Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_FAULT. */

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_five_entry_points():
     names = declared_functions()
-    for n in ("csa_append", "csa_index_score", "csa_topk", "csa_sparse_attn", "csa_decode"):
+    for n in ("csa_append", "csa_index_score", "csa_topk", "csa_sparse_attn", "csa_decode", "csa_step"):
         assert n in names
 
 
@@ -49,6 +49,30 @@ def test_null_arguments_are_rejected_before_launch(lib):
     assert lib.csa_topk(1, None, 512, None, 512, 512, None, None, 0, None) == 1
     assert lib.csa_sparse_attn(None, None, None, None, 64, None, 1.0, None, None, None, 0, None) == 1
     assert lib.csa_decode(None, None, None, 64, None, None, 64, None, 1.0, None, None, None, None, 0, None) == 1
+
+
+def test_step_checks_both_halves_before_any_launch(lib):
+    """csa_step validates the append's and the decode's arguments before its
+    first launch: a bad decode half is rejected (1 = invalid argument, 3 =
+    workspace too small) although the append half is valid and has tokens.
+    Without a GPU a launch would return 4 (CUDA error) instead."""
+    assert lib.csa_step(None, None, None, None, 0, None, None, None, None, None, 64, None, None, 64, None, 1.0,
+                        None, None, None, None, 0, None) == 1
+    buf = (C.c_uint8 * 4096)()
+    base = (C.addressof(buf) + 255) & ~255
+    pt = (C.c_int32 * 4)()
+    ints = (C.c_int32 * 8)()
+    cache = csa.CsaCache(base, base, C.addressof(pt), 1, 1, 1, 2)
+    rows = csa.CsaRows(1, C.addressof(ints), C.addressof(ints), 16, 1)
+    args = [C.byref(cache), None, C.addressof(ints), C.addressof(ints), 1, base, base, base, None, C.byref(rows),
+            64, None, base, 64, base, 1.0, base, None, None, base, 4096, None]
+    assert lib.csa_step(*args) == 1                       # q_idx missing
+    args[11] = base
+    args[20] = 0
+    assert lib.csa_step(*args) == 3                       # decode workspace too small
+    args[20] = 4096
+    args[13] = 0
+    assert lib.csa_step(*args) == 2                       # n_heads out of range
 
 
 def test_bad_cache_descriptors(lib):

@@ -218,6 +218,36 @@ def test_sparse_attention_matches_oracle(H, ctx, rows):
     print(f"attention H={H}: max normalised err {norm:.2e}, rel L2 {l2:.2e}")
 
 
+@pytest.mark.parametrize("cfg,compress", [(3, False), (4, False), (3, True)])
+def test_step_call_equals_append_then_decode(cfg, compress):
+    """csa_step (the append and the decode in one call, the score prep running
+    beside the append) leaves every cache byte and every output bit equal to
+    csa_append followed by csa_decode."""
+    wl = W.config(cfg)
+    states = []
+    for fused in (False, True):
+        st = DeviceState(wl)
+        st.build_history()
+        if compress:
+            st.set_compress(W.compress_inputs(cfg, int(wl.ctx_len.max())))
+        s = st.step_inputs()
+        if fused:
+            st.step(s)
+        else:
+            st.step_append(s)
+            st.step_decode(s)
+        rc, flags = csa.csa_check_device_status(s["ws"])
+        assert rc == 0 and flags == 0, (fused, flags)
+        states.append((st, s))
+    (a, sa), (b, sb) = states
+    same = lambda x, y: torch.equal(x.contiguous().view(torch.uint8), y.contiguous().view(torch.uint8))
+    for name in ("kv_pool", "idx_pool", "win_codes", "win_scale", "pending"):
+        x, y = getattr(a, name), getattr(b, name)
+        assert (x is None and y is None) or same(x, y), name
+    for key in ("topk", "out", "lse"):
+        assert same(sa[key], sb[key]), key
+
+
 @pytest.mark.parametrize("R", [30, 40, 60])
 def test_attention_cluster_split_counts(R):
     """Row counts that give 5, 3 and 2 splits per row: the row's CTAs run as one
