@@ -1,8 +1,8 @@
-// The C ABI (include/csa.h): argument validation, workspace carving, TMA
-// tensor-map encoding and kernel launches.  No allocation, no host sync
-// except in csa_check_device_status.
+// The C ABI (include/csa.h): argument validation, workspace carving and
+// kernel launches.  No allocation, no host sync except in
+// csa_check_device_status (and the no-workspace entry point's one-time
+// scratch lookup).
 #include <cstdint>
-#include <cstring>
 #include <mutex>
 
 #include "csa_device.cuh"
