@@ -200,8 +200,9 @@ CSA_API csa_status_t csa_topk(int32_t num_rows, const float* scores, int32_t ld,
  * dequantised FP4 main-KV entries listed in topk_idx (ascending, -1 skipped;
  * page translation done here, [SGL] "DSpark adaptation and optimization") and
  * the FP8 window positions max(0,t-127)..t ([VLLM] "SWA bounded replay").
- * K = V = the shared 512-d latent (MQA).  Split over key blocks with a
- * log-sum-exp merge.
+ * K = V = the shared 512-d latent (MQA).  With fewer rows than SMs a row is
+ * split over key blocks; its CTAs form one thread-block cluster and merge by
+ * log-sum-exp in shared memory, so ws holds only the status word.
  *  q bf16 [R, H, 512]; out bf16 [R, H, 512]; lse fp32 [R, H] (nullable). */
 CSA_API csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* window,
                              const csa_rows_t* rows, const int32_t* topk_idx,
