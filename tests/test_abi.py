@@ -101,3 +101,24 @@ def test_workspace_sizes_without_device(lib):
     R, n = 128, 65536
     assert csa.csa_workspace_size(csa.OP_DECODE, R, n, 64) >= (
         csa.csa_workspace_size(csa.OP_INDEX_SCORE, R, n, 64) + 4 * R * n + 4 * R * 512)
+
+
+def test_empty_calls_return_ok_without_a_launch(lib):
+    """Zero rows (and zero tokens) is a valid call that launches nothing: on a
+    machine without a GPU any launch would fail with 4 (CUDA error)."""
+    buf = (C.c_uint8 * 4096)()
+    base = (C.addressof(buf) + 255) & ~255
+    pt = (C.c_int32 * 4)()
+    ints = (C.c_int32 * 8)()
+    cache = csa.CsaCache(base, base, C.addressof(pt), 1, 1, 1, 2)
+    rows = csa.CsaRows(0, None, None, 0, 1)
+    assert lib.csa_decode(C.byref(cache), None, C.byref(rows), 64, None, None, 64, None, 1.0, None, None, None,
+                          None, 0, None) == 0
+    assert lib.csa_index_score(C.byref(cache), C.byref(rows), 64, None, None, None, 1, None, 0, None) == 0
+    assert lib.csa_sparse_attn(C.byref(cache), None, C.byref(rows), None, 64, None, 1.0, None, None, None, 0,
+                               None) == 0
+    assert lib.csa_topk(0, None, 512, None, 0, 512, None, None, 0, None) == 0
+    assert lib.csa_append(C.byref(cache), None, C.addressof(ints), C.addressof(ints), 0, None, None, base, None, 0,
+                          None) == 0
+    assert lib.csa_step(C.byref(cache), None, C.addressof(ints), C.addressof(ints), 0, None, None, base, None,
+                        C.byref(rows), 64, None, None, 64, None, 1.0, None, None, None, None, 0, None) == 0
