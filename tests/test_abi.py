@@ -4,6 +4,7 @@ launch.  CPU only: no call here reaches a kernel."""
 import ctypes as C
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -122,3 +123,25 @@ def test_empty_calls_return_ok_without_a_launch(lib):
                           None) == 0
     assert lib.csa_step(C.byref(cache), None, C.addressof(ints), C.addressof(ints), 0, None, None, base, None,
                         C.byref(rows), 64, None, None, 64, None, 1.0, None, None, None, None, 0, None) == 0
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++11")])
+def test_header_compiles_as_plain_c_and_cpp(tmp_path, lang, std):
+    """include/csa.h is a plain C header (C99, and C++ through extern "C"):
+    a host program needs only it and the CUDA runtime's declarations."""
+    import shutil
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    if not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("no CUDA headers")
+    src = tmp_path / ("use." + ("c" if lang == "c" else "cpp"))
+    src.write_text('#include "csa.h"\n'
+                   'int main(void) { csa_status_t (*f)(const csa_cache_t*, const csa_window_t*, const int32_t*,'
+                   ' const int32_t*, int32_t, const void*, const void*, void*, void*, size_t, cudaStream_t)'
+                   ' = csa_append; (void)f; return (int)csa_workspace_size(CSA_OP_DECODE, 0, 0, 0) * 0; }\n')
+    p = subprocess.run([cc, "-std=" + std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src)],
+                       capture_output=True, text=True)
+    assert p.returncode == 0, p.stderr
