@@ -340,7 +340,6 @@ csa_status_t csa_step(const csa_cache_t* cache, const csa_window_t* window, cons
                     total_tokens > 0 ? Order::kChained : Order::kStream, stream);
 }
 
-
 csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out) {
   if (!ws || !flags_out) return CSA_ERR_INVALID_ARGUMENT;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
