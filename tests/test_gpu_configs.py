@@ -1,6 +1,7 @@
-"""End-to-end parity of the five decode-step workloads at full size, in the
+"""End-to-end parity of the six decode-step workloads at full size, in the
 same launch configuration the benchmark times: history built by csa_append,
-the step's tokens appended, then one csa_decode.
+then one csa_step (the step's tokens appended and its rows decoded in one
+call; csa_step equals csa_append + csa_decode bit for bit, a unit test).
 
   J-1  every byte of the main-KV pool, the indexer pool, the FP8 window and
        the pending tokens equals the oracle's.
@@ -36,12 +37,9 @@ def test_config_parity(cfg):
     st = DeviceState(wl)
     st.build_history()
     s = st.step_inputs()
-    st.step_append(s)
-    st.step_decode(s)
-    rc, flags = csa.csa_check_device_status(st.ws_append)
-    assert rc == 0 and flags == 0, ("append", flags)
+    st.step(s)
     rc, flags = csa.csa_check_device_status(s["ws"])
-    assert rc == 0 and flags == 0, ("decode", flags)
+    assert rc == 0 and flags == 0, ("step", flags)
 
     ref = oracle.build_cache(wl, threads=16)
     # ---- J-1
