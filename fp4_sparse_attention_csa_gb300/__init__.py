@@ -78,10 +78,12 @@ def lib():
             L.csa_step.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp,
                                    vp, vp, sz, vp]
             L.csa_check_device_status.argtypes = [vp, vp, C.POINTER(C.c_uint32)]
+            L.csa_set_wait_budget.argtypes = [C.c_int64]
             L.csa_status_string.argtypes = [i32]
             L.csa_status_string.restype = C.c_char_p
             for fn in ("csa_append", "csa_append_compress", "csa_index_score", "csa_topk", "csa_sparse_attn",
-                       "csa_decode", "csa_step", "csa_index_score_noalloc", "csa_check_device_status"):
+                       "csa_decode", "csa_step", "csa_index_score_noalloc", "csa_check_device_status",
+                       "csa_set_wait_budget"):
                 getattr(L, fn).restype = C.c_int
             _lib = L
     return _lib
@@ -198,10 +200,17 @@ def csa_step(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending,
 
 
 def csa_check_device_status(ws, stream=None):
-    """Synchronises the stream; returns (status, flags) and clears the flags."""
+    """Synchronises the stream; returns (status, flags) and clears the flags.
+    ws=None reads the status word of csa_index_score_noalloc's fixed array."""
     flags = C.c_uint32(0)
     rc = lib().csa_check_device_status(_ptr(ws), _stream(stream), C.byref(flags))
     return int(rc), int(flags.value)
+
+
+def csa_set_wait_budget(sm_clocks):
+    """Bound (in SM clocks) on each wait of the index score's pipeline; <= 0
+    restores the default.  Process-wide."""
+    _check(lib().csa_set_wait_budget(int(sm_clocks)), "csa_set_wait_budget")
 
 
 def csa_status_string(status):

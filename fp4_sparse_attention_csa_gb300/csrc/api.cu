@@ -3,19 +3,21 @@
 // csa_check_device_status (and the no-workspace entry point's one-time
 // scratch lookup).
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
-namespace csa {
-size_t score_ws_bytes(int32_t R, int32_t Hi);
-int score_group_rows(int32_t Hi);
-}  // namespace csa
-
 using namespace csa;
 
 namespace {
+
+// Budget of the index score's pipeline waits (csa_set_wait_budget).
+std::atomic<long long> g_wait_budget{kWaitBudget};
+
+// Device address of csa_index_score_noalloc's scratch array (end of file).
+cudaError_t noalloc_scratch(void** out);
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) & ~(a - 1); }
@@ -65,6 +67,9 @@ DecodeLayout decode_layout(int32_t R, int32_t max_entries) {
   return L;
 }
 
+// The attention kernel is compiled for these head counts only.
+bool attn_heads_supported(int32_t H) { return H == 16 || H == 32 || H == 64; }
+
 csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
 csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t Hi, const void* q_idx,
@@ -81,16 +86,8 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
   a.row_pos = rows->row_pos;
   a.num_rows = rows->num_rows;
   a.Hi = Hi;
-  // rows scored by one MMA: all of a request's rows when at least two TMEM
-  // accumulator buffers still fit, so the epilogue can overlap the MMAs
-  {
-    const int hp = (Hi + 7) & ~7;
-    int g = rows->max_rows_per_req < 1 ? 1 : rows->max_rows_per_req;
-    const int two_buf = (216 / hp) > 0 ? 216 / hp : 1;
-    if (g > two_buf) g = two_buf;
-    if (g > score_group_rows(Hi)) g = score_group_rows(Hi);
-    a.group_rows = g;
-  }
+  a.group_rows = score_group_rows(Hi, rows->max_rows_per_req);   // rows of a request scored by one MMA
+  a.wait_budget = g_wait_budget.load(std::memory_order_relaxed);
   a.max_entries = rows->max_entries;
   a.q_idx = static_cast<const uint16_t*>(q_idx);
   a.w = w;
@@ -182,7 +179,7 @@ csa_status_t check_decode(const csa_cache_t* cache, const csa_window_t* window, 
   if (s != CSA_OK) return s;
   if ((s = check_rows(rows, cache)) != CSA_OK) return s;
   if ((s = check_window(window, rows->max_rows_per_req)) != CSA_OK) return s;
-  if (n_idx_heads < 1 || n_idx_heads > CSA_MAX_IDX_HEADS || n_heads < 1 || n_heads > CSA_MAX_HEADS)
+  if (n_idx_heads < 1 || n_idx_heads > CSA_MAX_IDX_HEADS || !attn_heads_supported(n_heads))
     return CSA_ERR_UNSUPPORTED;
   if (rows->num_rows == 0) return CSA_OK;
   if (!q_idx || !w || !q || !out || !aligned(q_idx, 16) || !aligned(q, 16) || !aligned(out, 16))
@@ -302,7 +299,7 @@ csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* windo
   if (s != CSA_OK) return s;
   if ((s = check_rows(rows, cache)) != CSA_OK) return s;
   if ((s = check_window(window, rows->max_rows_per_req)) != CSA_OK) return s;
-  if (n_heads < 1 || n_heads > CSA_MAX_HEADS) return CSA_ERR_UNSUPPORTED;
+  if (!attn_heads_supported(n_heads)) return CSA_ERR_UNSUPPORTED;
   if (rows->num_rows == 0) return CSA_OK;
   if (!topk_idx || !q || !out || !aligned(q, 16) || !aligned(out, 16)) return CSA_ERR_INVALID_ARGUMENT;
   if (!ws || ws_bytes < kStatusBytes || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
@@ -341,7 +338,8 @@ csa_status_t csa_step(const csa_cache_t* cache, const csa_window_t* window, cons
 }
 
 csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out) {
-  if (!ws || !flags_out) return CSA_ERR_INVALID_ARGUMENT;
+  if (!flags_out) return CSA_ERR_INVALID_ARGUMENT;
+  if (!ws && noalloc_scratch(&ws) != cudaSuccess) return CSA_ERR_CUDA;   // the fixed scratch array's word
   if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
   uint32_t f = 0;
   if (cudaMemcpy(&f, ws, sizeof(f), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
@@ -350,6 +348,11 @@ csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* fl
   *flags_out = f;
   if (f & CSA_FLAG_TIMEOUT) return CSA_ERR_TIMEOUT;
   return f ? CSA_ERR_DEVICE_FAULT : CSA_OK;
+}
+
+csa_status_t csa_set_wait_budget(int64_t sm_clocks) {
+  g_wait_budget.store(sm_clocks > 0 ? (long long)sm_clocks : kWaitBudget, std::memory_order_relaxed);
+  return CSA_OK;
 }
 
 const char* csa_status_string(csa_status_t s) {
@@ -379,24 +382,32 @@ constexpr size_t kNoAllocScratchBytes = CSA_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_scratch_once[kMaxDevices];
-void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+std::mutex g_scratch_mu;
+std::atomic<void*> g_scratch_ptr[kMaxDevices];
 
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) on its first call.
+// Device address of the scratch array on the current device, looked up with
+// that device current on its first successful call and kept from then on.  A
+// lookup that fails (for example inside a stream capture) is not remembered:
+// the next call tries again.
 cudaError_t noalloc_scratch(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], [dev] {
-    void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    g_scratch_ptr[dev] = p;
-  });
-  if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
-  *out = g_scratch_ptr[dev];
+  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return e;
+      }
+      g_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
   return cudaSuccess;
 }
 

@@ -84,9 +84,12 @@ struct ScoreArgs {
   int64_t ld;
   uint32_t* status;                    // head of the workspace
   int32_t grid;                        // score CTAs (set by the launcher)
+  long long wait_budget;               // SM clocks a pipeline wait may take
 };
 // prep_order: the score prep's order (kStream when it is its call's first kernel)
 cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, Order prep_order, cudaStream_t stream);
+size_t score_ws_bytes(int32_t R, int32_t Hi);
+int score_group_rows(int32_t Hi, int32_t max_rows_per_req);
 
 struct TopkArgs {
   const float* scores;

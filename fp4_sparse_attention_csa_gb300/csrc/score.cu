@@ -9,31 +9,43 @@
 //
 // Two kernels:
 //  k_score_prep  block 0 builds the segment table (a segment = up to
-//                `group_rows` consecutive rows of one request, scored by one
-//                MMA N dimension) and each score CTA's first segment; blocks
-//                1..R quantise each row's q_idx to MXFP4 straight into the
-//                shared-memory image the MMA reads.
+//                `group_rows` consecutive rows of one request that see at
+//                least one entry, scored by one MMA N dimension) and each
+//                score CTA's first segment; blocks 1..R quantise each row's
+//                q_idx to MXFP4 straight into the shared-memory image the MMA
+//                reads.
 //  k_index_score persistent, one CTA per SM.  A work table of (segment, tile,
 //                pages) items is built in shared memory first, so no role
 //                touches global metadata per tile.  Roles:
 //                4 producer warps  one bulk copy per indexer page (4352 B: the
 //                        page layout is already the MMA operand layout), two
-//                        pages = one 128-entry tile per stage, 12 stages; the
-//                        copy engine is fed by several warps because one
-//                        warp's copy issue rate caps its bandwidth.
-//                4 MMA warps, one per TMEM accumulator buffer (tile t goes
-//                        to buffer t mod 4): the warp gathers the tile's E8M0
-//                        bytes into the tcgen05 scale-factor atom, and one
-//                        lane issues tcgen05.cp of the scales and two
-//                        kind::mxf4 MMAs (K = 64 each) per 128-column N chunk;
-//                        A = 128 entries x 128 dims, B = rows*heads x 128
-//                        dims, D = fp32 [entry lane, row*head column].  A
-//                        single issuing thread spends hundreds of cycles per
-//                        tile on tcgen05 issue, so four run side by side.
-//                4 epilogue warp groups on the 4 buffers: per entry lane,
-//                        sum_h w*relu(D) with packed fp32x2 fused multiply-adds
-//                        (even and odd heads in the two halves, added at the
-//                        end), coalesced fp32 score stores.
+//                        pages = one 128-entry tile per stage, 20 stages; several
+//                        warps feed the copy engine because one warp's copy
+//                        issue rate caps its bandwidth.  Every wait polls: a
+//                        thread suspended with a time hint was measured to wake
+//                        microseconds after a tcgen05.commit completed the phase.
+//                3 consumer warpgroups.  Group g takes tiles g, g+G, ... of the
+//                        CTA's range.  Its first warp gathers a tile's E8M0
+//                        bytes into the tcgen05 scale-factor atom and one lane
+//                        issues tcgen05.cp of the scales and two kind::mxf4
+//                        MMAs (K = 64 each): A = 128 entries x 128 dims, B =
+//                        rows*heads x 128 dims, D = fp32 [entry lane,
+//                        row*head column] in one of the group's TMEM
+//                        accumulators.  With two accumulators per group the
+//                        MMA of the group's next tile runs while its four warps
+//                        reduce the current one: per entry lane
+//                        sum_h w*relu(D) with packed fp32x2 fused
+//                        multiply-adds (even and odd heads in the two halves,
+//                        added at the end), coalesced fp32 score stores.  The
+//                        MMA issue and the reduction of a tile live in the same
+//                        warpgroup, so the only cross-role hand-offs per tile
+//                        are the page copy (stage full / free) and the MMA
+//                        completion.
+//
+// Every wait is bounded by the call's wait budget (SM clocks).  A wait that
+// runs out raises CSA_FLAG_TIMEOUT and stops the CTA's pipeline; before the
+// CTA exits it waits (with the default budget) for every bulk copy and tcgen05
+// operation it issued, then frees its TMEM.
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
@@ -45,52 +57,67 @@ struct Seg {
   int32_t b, r0, nrows, n;
 };
 
-constexpr int kStages = 12;
-constexpr int kMaxBuf = 4;                     // TMEM accumulator buffers = MMA warps = epilogue groups
-constexpr int kProducers = 4;                  // warps 0..3
-constexpr int kMmaWarp0 = kProducers;          // warps 4..7
-constexpr int kEpiWarp0 = kMmaWarp0 + kMaxBuf; // warps 8..23 (group g = warps 8+4g .. 8+4g+3)
-constexpr int kEpiWarps = 4 * kMaxBuf;
-constexpr int kWarps = kEpiWarp0 + kEpiWarps;
+constexpr int kStages = 20;
+constexpr int kGroups = 3;                         // consumer warpgroups
+constexpr int kProducers = 4;                      // warps 0..3
+constexpr int kCons0 = kProducers;                 // consumer warps 4..15
+constexpr int kWarps = kProducers + 4 * kGroups;
 constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxAcc = 2 * kGroups;               // TMEM accumulators in flight
 constexpr int kTileEntries = 128;
-constexpr int kStageA = 2 * IDX_PAGE;          // two whole pages = 16 groups of 544 B
-constexpr int kStageSF = 512;                  // scale-factor atom of 128 rows
-constexpr int kMaxN = CSA_MAX_ROW_GROUP_COLS;  // rows x padded heads per MMA group
-constexpr int kQData = kMaxN * 64;   // 24576
-constexpr int kQSF = kMaxN * 4;      // 1536
-constexpr int kItemCap = 512;        // work items per table chunk
-constexpr int kMaxGroupRows = 64;    // rows per segment (kMaxN / 8 heads at least)
-// TMEM columns: A scale factors 4 per buffer; q scale factors 2 parities x
-// 3 atoms x 4; then the accumulator buffers.
-constexpr int kTmemSFA = 0, kTmemSFB = 16, kTmemD = kTmemSFB + 24;
+constexpr int kStageA = 2 * IDX_PAGE;              // two whole pages = 16 groups of 544 B
+constexpr int kMaxN = CSA_MAX_ROW_GROUP_COLS;      // rows x padded heads per MMA (128)
+constexpr int kQData = kMaxN * 64;                 // 8192
+constexpr int kQSF = kMaxN * 4;                    // 512
+constexpr int kItemCap = 256;                      // work items per table chunk
+constexpr int kMaxGroupRows = kMaxN / 8;           // rows per segment (8 heads at least)
+static_assert(kStages % kProducers == 0, "a stage belongs to one producer warp");
+static_assert(kMaxN == 128, "one scale-factor atom and one MMA N chunk per segment");
+// TMEM columns: q scale factors (2 parities x 4), then 4 per accumulator for the
+// tile's scale factors, then the accumulators.
+constexpr int kTmemSFB = 0, kTmemSFA = 8, kTmemD = kTmemSFA + 4 * kMaxAcc;
 
 struct Item {
   int32_t seg, tile, pg0, pg1;       // local segment index, tile in segment, pages (-1: none)
 };
 
 struct ScoreSmem {
-  uint8_t qdata[2][kQData];                    // 1024-aligned (24576 = 24 * 1024)
+  uint8_t qdata[2][kQData];                    // 1024-aligned (64-byte swizzle)
   uint8_t a[kStages][kStageA];                 // 16-aligned (8704 = 544 * 16)
-  uint8_t sfa_atom[kStages][kStageSF];
   uint8_t sfb_raw[2][kQSF];
   uint8_t sfb_atom[2][kQSF];
+  uint8_t sfa_atom[kMaxAcc][512];
   Item items[kItemCap];
   Seg segs[kItemCap];
   int32_t pref[kItemCap + 1];
-  alignas(16) float wseg[kEpiWarps][kMaxN];    // row kr's w at kr * Hp (16-byte aligned rows)
-  int32_t rown[kEpiWarps][kMaxGroupRows];
+  alignas(16) float wseg[4 * kGroups][kMaxN];  // per consumer warp: row kr's w at kr * Hp
+  int32_t rown[4 * kGroups][kMaxGroupRows];
   uint64_t full[kStages], empty[kStages];
-  uint64_t tfull[kMaxBuf], tempty[kMaxBuf];
+  uint64_t acc_full[kMaxAcc];
   uint64_t qfull[2], qempty[2], qready[2];
+  uint64_t drain[kGroups];
+  int32_t q_last[2];                           // latest segment whose q was loaded into each buffer
   uint32_t tmem_base;
   int32_t abort_flag;
 };
+
+static_assert(sizeof(ScoreSmem) + 1024 <= 227 * 1024, "one CTA per SM, within the opt-in shared memory");
 
 __host__ __device__ inline int hi_pad(int Hi) { return (Hi + 7) & ~7; }
 // MMA N for a group of N score columns: a multiple of 16, at least 64
 // (columns past N multiply stale rows of the B buffer and are never read).
 __host__ __device__ inline int mma_n(int N) { return N < 64 ? 64 : (N + 15) & ~15; }
+
+// Consumer groups and accumulators per group for accumulators of `cols`
+// TMEM columns: two per group (the next tile's MMA overlaps the current
+// reduction) when six fit, else as many groups as accumulators fit.
+__host__ __device__ inline void score_groups(int cols, int* G, int* NB) {
+  int A = (512 - kTmemD) / cols;
+  A = A < kMaxAcc ? A : kMaxAcc;
+  if (A >= 2 * kGroups) { *G = kGroups; *NB = 2; }
+  else if (A >= 4) { *G = 2; *NB = 2; }
+  else { *G = A < 1 ? 1 : (A > kGroups ? kGroups : A); *NB = 1; }
+}
 
 // Workspace carve-out of the score step (after the status word).
 constexpr int kMaxGrid = 1024;
@@ -163,38 +190,40 @@ __global__ void __launch_bounds__(128) k_score_prep(ScoreArgs a, uint8_t* ws) {
   const int R = a.num_rows, Hi = a.Hi, Hp = hi_pad(Hi);
   ScoreWs W = carve_score_ws(ws, R, Hi);
   if (blockIdx.x == 0) {
-    // ---- segment table: rows grouped by request, at most group_rows per segment
+    // ---- segment table: rows grouped by request, at most group_rows per
+    // segment; segments whose rows see no entry are left out, so every segment
+    // has at least one tile
     __shared__ int sm_warp[4];
     __shared__ int carry_seg;
     if (threadIdx.x == 0) carry_seg = 0;
     __syncthreads();
     for (int base = 0; base < R; base += 128) {
       const int r = base + threadIdx.x;
-      int start = 0;
-      int b = 0, k_in_req = 0;
+      int keep = 0;
+      Seg s;
       if (r < R) {
-        b = __ldg(a.row_req + r);
+        const int b = __ldg(a.row_req + r);
         if (b < 0 || b >= a.num_requests || (r > 0 && __ldg(a.row_req + r - 1) > b))
           raise_flag(a.status, CSA_FLAG_ROW_INVALID);
-        k_in_req = r - lower_bound_req(a.row_req, R, b);
-        start = (k_in_req % a.group_rows) == 0;
+        const int k_in_req = r - lower_bound_req(a.row_req, R, b);
+        if (k_in_req >= 0 && (k_in_req % a.group_rows) == 0) {
+          const int rend = lower_bound_req(a.row_req, R, b + 1);
+          const int nrows = max(0, min(a.group_rows, rend - r));
+          int n = 0;
+          for (int k = 0; k < nrows; ++k) n = max(n, (__ldg(a.row_pos + r + k) + 1) / a.P);
+          const int cap = min(a.max_entries, a.max_pages * PAGE);
+          if (n > cap) {
+            raise_flag(a.status, CSA_FLAG_ROW_INVALID);
+            n = cap;
+          }
+          if (b < 0 || b >= a.num_requests) n = 0;
+          s.b = b; s.r0 = r; s.nrows = nrows; s.n = n;
+          keep = n > 0 ? 1 : 0;
+        }
       }
       int tot;
-      const int sid = block_exclusive_scan(start, &tot, sm_warp) + carry_seg;
-      if (start) {
-        const int rend = lower_bound_req(a.row_req, R, b + 1);
-        const int nrows = max(0, min(a.group_rows, rend - r));
-        int n = 0;
-        for (int k = 0; k < nrows; ++k) n = max(n, (__ldg(a.row_pos + r + k) + 1) / a.P);
-        const int cap = min(a.max_entries, a.max_pages * PAGE);
-        if (n > cap || b < 0 || b >= a.num_requests) {
-          raise_flag(a.status, CSA_FLAG_ROW_INVALID);
-          n = (b < 0 || b >= a.num_requests) ? 0 : min(n, cap);
-        }
-        Seg s;
-        s.b = b; s.r0 = r; s.nrows = nrows; s.n = n;
-        W.seg[sid] = s;
-      }
+      const int sid = block_exclusive_scan(keep, &tot, sm_warp) + carry_seg;
+      if (keep) W.seg[sid] = s;
       __syncthreads();
       if (threadIdx.x == 0) carry_seg += tot;
       __syncthreads();
@@ -309,20 +338,58 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   return d;
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ScoreSmem& sm, uint32_t* status) {
-  if (mbar_wait(bar, parity)) return true;
-  raise_flag(status, CSA_FLAG_TIMEOUT);
+// One thread's bounded wait; on time-out the CTA's pipeline is stopped.
+template <bool kPoll>
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ScoreSmem& sm, const ScoreArgs& a) {
+  if (mbar_wait_for<kPoll>(bar, parity, a.wait_budget)) return true;
+  raise_flag(a.status, CSA_FLAG_TIMEOUT);
   atomicExch(&sm.abort_flag, 1);
   return false;
 }
 
 // Whole-warp wait: lane 0 waits, the warp then agrees on the outcome, so a
 // time-out never leaves some lanes of a warp inside the loop and others out.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, ScoreSmem& sm, uint32_t* status) {
+template <bool kPoll>
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, ScoreSmem& sm, const ScoreArgs& a) {
   int ok = 1;
-  if (lane_id() == 0) ok = wait_or_abort(bar, parity, sm, status) ? 1 : 0;
+  if (lane_id() == 0) ok = wait_or_abort<kPoll>(bar, parity, sm, a) ? 1 : 0;
   __syncwarp();
   return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// Named barrier over the four warps of consumer group `grp` that also ORs a
+// flag across them, so every warp of the group takes the same branch after it.
+__device__ __forceinline__ bool group_sync_or(int grp, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(1 + grp)
+      : "memory");
+  return r != 0;
+}
+
+// A producer's wait for a free stage: the pipeline is usually full, so it
+// backs off between probes instead of taking issue slots from the consumers.
+__device__ __forceinline__ bool producer_wait(uint64_t* bar, uint32_t parity, ScoreSmem& sm, const ScoreArgs& a) {
+  if (mbar_try_wait_poll(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_poll(bar, parity)) {
+    __nanosleep(64);
+    if (clock64() - t0 > a.wait_budget) {
+      raise_flag(a.status, CSA_FLAG_TIMEOUT);
+      atomicExch(&sm.abort_flag, 1);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool aborted(const ScoreSmem& sm) {
+  return *reinterpret_cast<const volatile int32_t*>(&sm.abort_flag) != 0;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_t* ws) {
@@ -334,26 +401,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
   const uint8_t* ipool = static_cast<const uint8_t*>(a.idx_pool);
   pdl_trigger();
 
-  // TMEM: scale factors in columns [0, 48), accumulator buffer d at
-  // kTmemD + d * dstride; one epilogue warp group per buffer.
-  const int npad_max = mma_n(a.group_rows * Hp);       // largest MMA N of any segment
-  const int dstride = npad_max + 16;
-  const int nbuf = min(kMaxBuf, (512 - kTmemD) / dstride);
+  const int cols = mma_n(a.group_rows * Hp);           // TMEM columns of one accumulator
+  int G, NB;
+  score_groups(cols, &G, &NB);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    for (int d = 0; d < kMaxBuf; ++d) {
-      mbar_init(&sm.tfull[d], 1);
-      mbar_init(&sm.tempty[d], 4);
-    }
+    for (int d = 0; d < kMaxAcc; ++d) mbar_init(&sm.acc_full[d], 1);
     for (int d = 0; d < 2; ++d) {
       mbar_init(&sm.qfull[d], 1);
-      mbar_init(&sm.qempty[d], nbuf);            // every active MMA warp leaves each segment once
+      mbar_init(&sm.qempty[d], G);             // every group leaves each segment once
       mbar_init(&sm.qready[d], 1);
     }
+    for (int g = 0; g < kGroups; ++g) mbar_init(&sm.drain[g], 1);
+    sm.q_last[0] = sm.q_last[1] = -1;
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -368,17 +432,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
   const int per = (total + gridDim.x - 1) / gridDim.x;
   const int beg = min(total, (int)blockIdx.x * per), end = min(total, beg + per);
 
-  // Role state kept across work chunks.  A segment's ordinal within this CTA
-  // (ord) picks its q buffer (ord & 1) and the phases of the q barriers.
+  // Role state kept across work chunks.  Segments are numbered in this CTA's
+  // item order (ord = 0, 1, ...; every segment has a tile); ord picks the q
+  // buffer (ord & 1) and the phases of the q barriers.
   const int prod = warp < kProducers ? warp : -1;
-  const int iss = warp - kMmaWarp0;                          // MMA warp index (buffer) when in [0, nbuf)
-  int m_ord = -1, m_par = 0, m_N = 0;                        // MMA warp state
-  uint64_t m_bdesc = 0;
-  uint32_t m_idesc0 = 0, m_idesc1 = 0;
-  int m_nchunks = 0;
-  int e_gseg = -1, e_round = 0;                              // epilogue
-  int last_ord = -1;                                         // ordinal of the previous chunk's last item
-  int ord_base = 0;                                          // ordinal of this chunk's first segment
+  const int grp = warp >= kCons0 ? (warp - kCons0) >> 2 : -1;
+  const bool cons = grp >= 0 && grp < G;
+  const bool leader_warp = cons && (warp & 3) == 0;        // issues the group's MMAs
+  int p_last_it = -1;                                      // producer: last item copied
+  int l_ord = -1, l_par = 0, l_desc_ord = -1;             // leader: segment entered, descriptors
+  uint64_t l_bdesc = 0;
+  uint32_t l_id0 = 0, l_id1 = 0;
+  bool l_issued = false;
+  int u_issue = 0, u_done = 0;                             // group's own tiles issued / reduced
+  int e_gseg = -1;                                         // consumer warp: segment staged
+  int ord_base = 0;                                        // ordinal of the window's first segment
 
   int seg0 = (beg < end) ? W.cta_seg[blockIdx.x] : S;
   int it_base = 0;
@@ -390,11 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
     __syncthreads();
     const int c1 = min(min(end, c0 + kItemCap), sm.pref[nsw]);
     const int m = c1 - c0;
-    if (m <= 0) {                            // only empty segments in this window
-      seg0 += nsw;
-      __syncthreads();
-      continue;
-    }
     for (int i = tid; i < m; i += kThreads) {
       const int item = c0 + i;
       int lo = 0, hi = nsw - 1;              // largest j with pref[j] <= item
@@ -423,81 +486,106 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
     }
     __syncthreads();
 
-    if (prod >= 0 && lane == 0) {
-      // ================= producers: items it with it % kProducers == prod =================
-      int i = prod - (it_base % kProducers);
-      if (i < 0) i += kProducers;
-      for (; i < m; i += kProducers) {
-        if (sm.abort_flag) break;
-        const int it = it_base + i;
-        const Item e = sm.items[i];
-        const int ord = ord_base + e.seg;
-        const int prev_ord = (i > 0) ? ord_base + sm.items[i - 1].seg : last_ord;
-        if (ord != prev_ord) {                         // first item of a segment: load its q image
-          const Seg sg = sm.segs[e.seg];
-          const int par = ord & 1;
-          if (ord >= 2 && !wait_or_abort(&sm.qempty[par], ((ord >> 1) - 1) & 1, sm, a.status)) break;
-          const uint32_t bytes_d = (uint32_t)(sg.nrows * Hp * 64), bytes_s = (uint32_t)(sg.nrows * Hp * 4);
-          mbar_expect_tx(&sm.qfull[par], bytes_d + bytes_s);
-          if (bytes_d > 0) {   // nrows is in [1, group_rows] whenever the segment has tiles
+    if (prod >= 0) {
+      if (lane == 0) {
+        // ================= producers: items it with it % kProducers == prod =================
+        int i = prod - (it_base % kProducers);
+        if (i < 0) i += kProducers;
+        for (; i < m; i += kProducers) {
+          if (aborted(sm)) break;
+          const int it = it_base + i;
+          const Item e = sm.items[i];
+          const int ord = ord_base + e.seg;
+          // the first item of a segment in this CTA loads its q image (a chunk's
+          // first item continues the previous chunk's last segment when e.seg == 0)
+          const bool first = (i > 0) ? (sm.items[i - 1].seg != e.seg) : (it_base == 0 || e.seg != 0);
+          if (first) {
+            const Seg sg = sm.segs[e.seg];
+            const int par = ord & 1;
+            if (ord >= 2 && !producer_wait(&sm.qempty[par], ((ord >> 1) - 1) & 1, sm, a)) break;
+            const uint32_t bytes_d = (uint32_t)(sg.nrows * Hp * 64), bytes_s = (uint32_t)(sg.nrows * Hp * 4);
+            mbar_expect_tx(&sm.qfull[par], bytes_d + bytes_s);
             bulk_load(sm.qdata[par], W.qimg + (size_t)sg.r0 * Hp * 64, bytes_d, &sm.qfull[par]);
             bulk_load(sm.sfb_raw[par], W.qsf + (size_t)sg.r0 * Hp * 4, bytes_s, &sm.qfull[par]);
+            sm.q_last[par] = ord;                    // loads into one buffer are ordered by qempty
           }
+          const int s = it % kStages, use = it / kStages;
+          if (use > 0 && !producer_wait(&sm.empty[s], (use - 1) & 1, sm, a)) break;
+          const uint32_t bytes = (e.pg0 >= 0 ? (uint32_t)IDX_PAGE : 0u) + (e.pg1 >= 0 ? (uint32_t)IDX_PAGE : 0u);
+          mbar_expect_tx(&sm.full[s], bytes);
+          if (e.pg0 >= 0) bulk_load(sm.a[s], ipool + (size_t)e.pg0 * IDX_PAGE, IDX_PAGE, &sm.full[s]);
+          if (e.pg1 >= 0) bulk_load(sm.a[s] + IDX_PAGE, ipool + (size_t)e.pg1 * IDX_PAGE, IDX_PAGE, &sm.full[s]);
+          p_last_it = it;
         }
-        const int s = it % kStages, use = it / kStages;
-        if (use > 0 && !wait_or_abort(&sm.empty[s], (use - 1) & 1, sm, a.status)) break;
-        const uint32_t bytes = (e.pg0 >= 0 ? (uint32_t)IDX_PAGE : 0u) + (e.pg1 >= 0 ? (uint32_t)IDX_PAGE : 0u);
-        mbar_expect_tx(&sm.full[s], bytes);
-        if (e.pg0 >= 0) bulk_load(sm.a[s], ipool + (size_t)e.pg0 * IDX_PAGE, IDX_PAGE, &sm.full[s]);
-        if (e.pg1 >= 0) bulk_load(sm.a[s] + IDX_PAGE, ipool + (size_t)e.pg1 * IDX_PAGE, IDX_PAGE, &sm.full[s]);
       }
-    } else if (iss >= 0 && iss < nbuf) {
-      // ================= MMA warp iss: items it with it % nbuf == iss =================
-      const uint64_t adesc0 = smem_desc(smem_u32(sm.a[0]), 128, IDX_GROUP, kSwizzleNone);
+      __syncwarp();
+    } else if (cons) {
+      // ================= consumer group grp: items it with it % G == grp =================
+      const int q = warp & 3;                       // TMEM lane quarter of this warp
+      const int mrow = 32 * q + lane;               // entry within the tile
+      const int cw = warp - kCons0;
+      float* ew = sm.wseg[cw];                      // this warp's copy of the segment's w
+      int32_t* en = sm.rown[cw];                    // and of its rows' visible lengths
+      int first_own = grp - (it_base % G);
+      if (first_own < 0) first_own += G;
       const uint32_t sfb_t = tmem + kTmemSFB;
-      for (int i = 0; i < m; ++i) {
-        if (sm.abort_flag) break;
-        const Item e = sm.items[i];
-        const int ord = ord_base + e.seg;
-        if (ord != m_ord) {
-          // leaving a segment: its q buffer is free once this warp's MMAs complete
-          if (m_ord >= 0 && lane == 0) tc_commit(&sm.qempty[m_ord & 1]);
-          m_par = ord & 1;
-          if (!warp_wait(&sm.qfull[m_par], (ord >> 1) & 1, sm, a.status)) break;
-          m_N = sm.segs[e.seg].nrows * Hp;
-          const int natoms = (m_N + 127) / 128;
-          if (ord % nbuf == iss) {
-            // one warp per segment lays the q scales out as atoms and copies them
-            // to TMEM; the commit tells the other MMA warps the copy has landed.
-            // Rows past N inside the last atom hold stale bytes; their D columns
-            // are never read.
-            for (int c = 0; c < natoms; ++c)
-              sf_to_atom(sm.sfb_raw[m_par] + 512 * c, sm.sfb_atom[m_par] + 512 * c, lane);
+      const uint64_t adesc0 = smem_desc(smem_u32(sm.a[0]), 128, IDX_GROUP, kSwizzleNone);
+      bool ok = true;
+
+      // Leader warp: enter every segment up to ordinal `ord` in order.  Every
+      // group enters every segment of the CTA's range (so each q buffer is
+      // released by all of them, and the group that copies a segment's q
+      // scales to TMEM always reaches it), whether or not it has a tile there.
+      auto enter_upto = [&](int ord) -> bool {
+        while (l_ord < ord) {
+          const int o = l_ord + 1;
+          // leaving l_ord: its q buffer is free once this group's MMAs complete
+          if (l_ord >= 0 && lane == 0) tc_commit(&sm.qempty[l_ord & 1]);
+          const int par = o & 1;
+          if (!warp_wait<true>(&sm.qfull[par], (o >> 1) & 1, sm, a)) return false;
+          if (o % G == grp) {
+            // one group per segment lays the q scales out as an atom and copies it
+            // to TMEM; the commit tells every group the copy has landed.  Rows past
+            // N inside the atom hold stale bytes; their D columns are never read.
+            sf_to_atom(sm.sfb_raw[par], sm.sfb_atom[par], lane);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
               tc_fence_after();
-              for (int c = 0; c < natoms; ++c)
-                tmem_cp_32x128b_x4(sfb_t + 12 * m_par + 4 * c,
-                                   smem_desc(smem_u32(sm.sfb_atom[m_par] + 512 * c), 16, 128, kSwizzleNone));
-              tc_commit(&sm.qready[m_par]);
+              tmem_cp_32x128b_x4(sfb_t + 4 * par, smem_desc(smem_u32(sm.sfb_atom[par]), 16, 128, kSwizzleNone));
+              tc_commit(&sm.qready[par]);
             }
             __syncwarp();
           }
-          if (!warp_wait(&sm.qready[m_par], (ord >> 1) & 1, sm, a.status)) break;
-          const int Nm = mma_n(m_N);
-          m_nchunks = (Nm + 127) / 128;
-          m_bdesc = smem_desc(smem_u32(sm.qdata[m_par]), 16, 512, kSwizzle64B);
-          const uint32_t n_last = (uint32_t)(Nm - 128 * (m_nchunks - 1));   // N of the last chunk
-          m_idesc0 = idesc_mxf4(128, n_last, 0, 0);
-          m_idesc1 = idesc_mxf4(128, n_last, 2, 2);
-          m_ord = ord;
+          if (!warp_wait<true>(&sm.qready[par], (o >> 1) & 1, sm, a)) return false;
+          l_ord = o;
+        }
+        return true;
+      };
+
+      // Leader warp, before the group barrier: enter item i's segment, wait for
+      // its pages and lay its E8M0 bytes out as the tcgen05 scale-factor atom
+      // of the accumulator it will use (that atom and the accumulator's TMEM
+      // scale columns were last read by the MMA two tiles back, which has
+      // completed).
+      int p_it = -1;                                // item prepared, not yet launched
+      auto prepare = [&](int i) -> bool {
+        const Item e = sm.items[i];
+        const int ord = ord_base + e.seg;
+        if (l_desc_ord != ord) {                    // B operand and N of this segment
+          if (!enter_upto(ord)) return false;
+          const int N = sm.segs[e.seg].nrows * Hp;
+          l_par = ord & 1;
+          l_bdesc = smem_desc(smem_u32(sm.qdata[l_par]), 16, 512, kSwizzle64B);
+          l_id0 = idesc_mxf4(128, (uint32_t)mma_n(N), 0, 0);
+          l_id1 = idesc_mxf4(128, (uint32_t)mma_n(N), 2, 2);
+          l_desc_ord = ord;
         }
         const int it = it_base + i;
-        if (it % nbuf != iss) continue;
-        const int s = it % kStages, use = it / kStages, round = it / nbuf;
-        if (!warp_wait(&sm.full[s], use & 1, sm, a.status)) break;
-        // entry row r of the tile: page r / 64, group (r % 64) / 8, scale word (r % 8)
+        const int slot = grp * NB + (u_issue % NB);
+        const int s = it % kStages, use = it / kStages;
+        if (!warp_wait<true>(&sm.full[s], use & 1, sm, a)) return false;
+        // the tile's scale words: entry row r is page r / 64, group (r % 64) / 8, word r % 8
         {
           const uint8_t* st = sm.a[s];
           uint32_t wv[4];
@@ -506,43 +594,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
             const int r = lane + 32 * j;
             wv[j] = *reinterpret_cast<const uint32_t*>(st + (r >> 6) * IDX_PAGE + idx_scale_off(r & 63, 0));
           }
-          reinterpret_cast<uint4*>(sm.sfa_atom[s])[lane] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          reinterpret_cast<uint4*>(sm.sfa_atom[slot])[lane] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (round > 0 && !warp_wait(&sm.tempty[iss], (round - 1) & 1, sm, a.status)) break;
+        p_it = it;
+        return true;
+      };
+
+      // Leader warp, after the group barrier (the accumulator's previous tile
+      // has been reduced by all four warps): copy the scales to TMEM and issue
+      // the two MMAs of the prepared tile.
+      auto launch = [&]() {
+        if (p_it < 0) return;
+        const int it = p_it;
+        const int slot = grp * NB + (u_issue % NB);
+        const int s = it % kStages;
         if (lane == 0) {
           tc_fence_after();
-          const uint32_t sfa = tmem + kTmemSFA + 4 * iss;
-          tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[s]), 16, 128, kSwizzleNone));
+          const uint32_t sfa = tmem + kTmemSFA + 4 * slot;
+          tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[slot]), 16, 128, kSwizzleNone));
           // A: the two pages as they landed: 8-entry groups IDX_GROUP apart, 16-byte
           // core matrices 128 B apart along K (no swizzle); second K half at +256 B
           const uint64_t ad = adesc0 + (uint64_t)(s * (kStageA >> 4));
-          const uint32_t dcol = tmem + kTmemD + iss * dstride;
-          for (int c = 0; c < m_nchunks; ++c) {
-            const uint32_t sfb = sfb_t + 12 * m_par + 4 * c;
-            const uint64_t bd = m_bdesc + (uint64_t)(c * (128 * 64 >> 4));
-            const uint32_t id0 = (c + 1 < m_nchunks) ? idesc_mxf4(128, 128, 0, 0) : m_idesc0;
-            const uint32_t id1 = (c + 1 < m_nchunks) ? idesc_mxf4(128, 128, 2, 2) : m_idesc1;
-            mma_mxf4(dcol + c * 128, ad, bd, id0, sfa, sfb, 0u);
-            mma_mxf4(dcol + c * 128, ad + 16, bd + 2, id1, sfa, sfb, 1u);
-          }
+          const uint32_t dcol = tmem + kTmemD + slot * cols;
+          const uint32_t sfb = sfb_t + 4 * l_par;
+          mma_mxf4(dcol, ad, l_bdesc, l_id0, sfa, sfb, 0u);
+          mma_mxf4(dcol, ad + 16, l_bdesc + 2, l_id1, sfa, sfb, 1u);
           tc_commit(&sm.empty[s]);
-          tc_commit(&sm.tfull[iss]);
+          tc_commit(&sm.acc_full[slot]);
         }
         __syncwarp();
-      }
-    } else if (warp >= kEpiWarp0 && ((warp - kEpiWarp0) >> 2) < nbuf) {
-      // ================= epilogue group grp =================
-      const int grp = (warp - kEpiWarp0) >> 2;
-      const int q = warp & 3;                       // TMEM lane quarter of this warp
-      const int mrow = 32 * q + lane;               // entry within the tile
-      float* ew = sm.wseg[warp - kEpiWarp0];        // this warp's copy of the segment's w
-      int32_t* en = sm.rown[warp - kEpiWarp0];      // and of its rows' visible lengths
-      int i = grp - (it_base % nbuf);
-      if (i < 0) i += nbuf;
-      for (; i < m; i += nbuf) {
-        if (sm.abort_flag) break;
+        l_issued = true;
+        p_it = -1;
+        ++u_issue;
+      };
+
+      // All four warps: reduce item i from the group's oldest accumulator.
+      auto reduce = [&](int i) -> bool {
         const Item e = sm.items[i];
         const Seg sg = sm.segs[e.seg];
         const int gseg = seg0 + e.seg;
@@ -553,16 +642,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
           __syncwarp();
           e_gseg = gseg;
         }
-        if (!warp_wait(&sm.tfull[grp], e_round & 1, sm, a.status)) break;
+        const int slot = grp * NB + (u_done % NB);
         tc_fence_after();
         const int ient = e.tile * kTileEntries + mrow;
         const bool page_ok = (mrow < 64) ? (e.pg0 >= 0) : (e.pg1 >= 0);
-        const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + kTmemD + grp * dstride;
+        const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + kTmemD + slot * cols;
         for (int kr = 0; kr < sg.nrows; ++kr) {
           const float* wr = ew + kr * Hp;
-          uint64_t acc2 = 0ull;                     // (even heads, odd heads) partial sums, +0.0f each
+          // four independent (even head, odd head) fp32x2 chains, +0.0f each
+          uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
           float acc1 = 0.0f;                        // heads past the last full group of 32
           int h0 = 0;
+          for (; h0 + 64 <= Hi; h0 += 64) {         // two TMEM loads in flight, one wait
+            uint32_t v[64];
+            tmem_ld32(dbase + kr * Hp + h0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(dbase + kr * Hp + h0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wr + h0 + j);
+              uint64_t& c = acc2[(j >> 2) & 3];
+              c = ffma2(pack2(w4.x, w4.y), pack2(relu(v[j]), relu(v[j + 1])), c);
+              c = ffma2(pack2(w4.z, w4.w), pack2(relu(v[j + 2]), relu(v[j + 3])), c);
+            }
+          }
           for (; h0 + 32 <= Hi; h0 += 32) {
             uint32_t v[32];
             tmem_ld32(dbase + kr * Hp + h0, v);
@@ -570,8 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
               const float4 w4 = *reinterpret_cast<const float4*>(wr + h0 + j);
-              acc2 = ffma2(pack2(w4.x, w4.y), pack2(relu(v[j]), relu(v[j + 1])), acc2);
-              acc2 = ffma2(pack2(w4.z, w4.w), pack2(relu(v[j + 2]), relu(v[j + 3])), acc2);
+              uint64_t& c = acc2[(j >> 2) & 3];
+              c = ffma2(pack2(w4.x, w4.y), pack2(relu(v[j]), relu(v[j + 1])), c);
+              c = ffma2(pack2(w4.z, w4.w), pack2(relu(v[j + 2]), relu(v[j + 3])), c);
             }
           }
           for (; h0 < Hi; h0 += 16) {
@@ -582,26 +686,83 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
             for (int j = 0; j < 16; ++j)
               if (h0 + j < Hi) acc1 = fmaf(wr[h0 + j], relu(v[j]), acc1);
           }
-          const float acc = (lo_f32(acc2) + hi_f32(acc2)) + acc1;
+          const float s0 = lo_f32(acc2[0]) + hi_f32(acc2[0]), s1 = lo_f32(acc2[1]) + hi_f32(acc2[1]);
+          const float s2 = lo_f32(acc2[2]) + hi_f32(acc2[2]), s3 = lo_f32(acc2[3]) + hi_f32(acc2[3]);
+          const float acc = ((s0 + s1) + (s2 + s3)) + acc1;
           if (ient < en[kr] && ient < sg.n)
             a.scores[(size_t)(sg.r0 + kr) * a.ld + ient] = page_ok ? acc : -INFINITY;
         }
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.tempty[grp]);
-        ++e_round;
+        ++u_done;
+        return true;
+      };
+
+      // Per own tile u: the leader thread polls the MMA's completion, then a
+      // group barrier (which also agrees on stopping) tells the four warps the
+      // accumulator is ready and that every warp has finished the previous
+      // tile.  With two accumulators the leader warp then issues tile u+1
+      // into the other one before it joins the reduction of tile u; with one,
+      // the issue of tile u waits for the reduction of tile u-1.
+      auto acc_ready = [&](int u) {
+        if (leader_warp && lane == 0 && !aborted(sm)) {
+          const int slot = grp * NB + (u % NB);
+          wait_or_abort<true>(&sm.acc_full[slot], (u / NB) & 1, sm, a);
+        }
+      };
+      const int n_own = first_own < m ? (m - 1 - first_own) / G + 1 : 0;
+      if (NB == 2 && leader_warp && n_own > 0 && !aborted(sm)) {
+        if (prepare(first_own)) launch();
       }
+      for (int k = 0; k < n_own; ++k) {
+        const int ei = first_own + k * G;
+        if (NB == 1) {
+          if (leader_warp && !aborted(sm)) prepare(ei);
+          if (group_sync_or(grp, aborted(sm))) { ok = false; break; }
+          if (leader_warp) launch();
+        } else if (leader_warp && k + 1 < n_own && !aborted(sm)) {
+          prepare(ei + G);                          // overlaps the wait for tile k's MMA
+        }
+        acc_ready(u_done);
+        if (group_sync_or(grp, aborted(sm))) { ok = false; break; }
+        if (NB == 2 && leader_warp) launch();
+        reduce(ei);
+      }
+      // the chunk's segments past the group's last tile
+      if (leader_warp && ok && !aborted(sm)) enter_upto(ord_base + sm.items[m - 1].seg);
     }
     // ---- chunk done: every role has finished with this work table ----------------
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    last_ord = ord_base + sm.items[m - 1].seg;
-    ord_base = last_ord;
-    seg0 += sm.items[m - 1].seg;
+    const int last_seg = sm.items[m - 1].seg;
+    ord_base += last_seg;
+    seg0 += last_seg;
     it_base += m;
     c0 = c1;
     __syncthreads();
+    if (aborted(sm)) break;                         // read after a barrier: uniform
+  }
+
+  // ---- drain: every bulk copy this CTA issued has landed and every tcgen05
+  // operation has completed before shared memory and TMEM are released.  A
+  // stage belongs to one producer warp, so its latest use is that warp's; a q
+  // buffer is reloaded only after every group waited for its previous load,
+  // so only the latest load into each buffer can still be in flight.
+  __syncthreads();
+  if (prod >= 0 && lane == 0) {
+    for (int k = 0; k < kStages / kProducers; ++k) {
+      const int it = p_last_it - kProducers * k;   // this producer's most recent use of each of its stages
+      if (it < 0) break;
+      if (!mbar_wait(&sm.full[it % kStages], (it / kStages) & 1)) raise_flag(a.status, CSA_FLAG_TIMEOUT);
+    }
+    if (prod < 2) {
+      const int ql = sm.q_last[prod];
+      if (ql >= 0 && !mbar_wait(&sm.qfull[ql & 1], (ql >> 1) & 1)) raise_flag(a.status, CSA_FLAG_TIMEOUT);
+    }
+  }
+  if (leader_warp && lane == 0 && (l_issued || l_ord >= 0)) {
+    tc_commit(&sm.drain[grp]);
+    if (!mbar_wait(&sm.drain[grp], 0)) raise_flag(a.status, CSA_FLAG_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
@@ -618,7 +779,15 @@ size_t score_ws_bytes(int32_t R, int32_t Hi) {
   return reinterpret_cast<size_t>(w.qsf) + align256((size_t)R * hi_pad(Hi) * 4);
 }
 
-int score_group_rows(int32_t Hi) { return kMaxN / hi_pad(Hi); }
+// Rows of one request scored by one MMA: as many as keep the MMA's N (rows x
+// padded heads) within kMaxN; the score kernel then keeps at least three
+// accumulators in flight (six, two per consumer group, when N <= 80).
+int score_group_rows(int32_t Hi, int32_t max_rows_per_req) {
+  int g = kMaxN / hi_pad(Hi);
+  if (g > kMaxGroupRows) g = kMaxGroupRows;
+  if (max_rows_per_req >= 1 && g > max_rows_per_req) g = max_rows_per_req;
+  return g < 1 ? 1 : g;
+}
 
 cudaError_t launch_index_score(const ScoreArgs& a, int num_sms, Order prep_order, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;

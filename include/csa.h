@@ -97,9 +97,10 @@ extern "C" {
 #define CSA_IDX_ENTRY_BYTES   68
 #define CSA_KV_PAGE_BYTES     18432
 #define CSA_IDX_PAGE_BYTES    4352
-#define CSA_MAX_HEADS         64    /* attention heads per row (16, 32 or 64)   */
+#define CSA_MAX_HEADS         64    /* attention heads per row: 16, 32 or 64;
+                                       other counts return CSA_ERR_UNSUPPORTED  */
 #define CSA_MAX_IDX_HEADS     128   /* indexer heads per row                    */
-#define CSA_MAX_ROW_GROUP_COLS 384  /* rows-per-request x indexer heads scored
+#define CSA_MAX_ROW_GROUP_COLS 128  /* rows-per-request x indexer heads scored
                                        together; larger groups are split        */
 
 typedef enum {
@@ -210,8 +211,19 @@ CSA_API csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_
                              void* out, float* lse, void* ws, size_t ws_bytes,
                              cudaStream_t stream);
 
-/* csa_decode -- index score -> top-512 -> sparse attention in one call, all on
- * `stream`.  topk_out [R, 512] is optional (nullable). */
+/* csa_decode -- one decode step of one CSA layer for every query row: the
+ * indexer scores every visible entry, the exact top 512 are kept, and the
+ * rows attend to those entries plus their FP8 window ([SGL] "Architecture
+ * changes and KV cache compression": the indexer selects the top 512 global
+ * positions that take part in attention; "DSpark adaptation and
+ * optimization": the post-top-k filter and page translation in one step;
+ * [VLLM] "SWA bounded replay": the 128-position FP8 window).  Arguments are
+ * those of csa_index_score and csa_sparse_attn; everything is enqueued on
+ * `stream` (csa_index_score -> csa_topk -> csa_sparse_attn).
+ *  topk_out [R, 512] (nullable): the selected indices, ascending, -1 padded.
+ *  ws: csa_workspace_size(CSA_OP_DECODE, R, max_entries, n_heads) bytes,
+ *  256-byte aligned.  n_heads must be 16, 32 or 64 and n_idx_heads 1..128;
+ *  every argument is checked before the first launch. */
 CSA_API csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window,
                         const csa_rows_t* rows, int32_t n_idx_heads, const void* q_idx,
                         const float* w, int32_t n_heads, const void* q, float softmax_scale,
@@ -228,14 +240,16 @@ CSA_API csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* wi
  * library, present on every GPU that loads the library until the process
  * exits; nothing is allocated or freed.
  *  - The first call on each device looks up the array's device address with
- *    that device current; make that first call before any stream capture.
+ *    that device current; make that first call before any stream capture.  A
+ *    lookup that fails returns CSA_ERR_CUDA and is tried again next call.
  *  - Every call shares the one array and leaves its contents behind (the
  *    status word is cleared at the start of each call, the rest is rewritten
  *    before it is read).  Calls that overlap on the GPU -- other streams, or
  *    other host threads without ordering between them -- race on the array.
  *  - Scratch need is about num_rows x 8*ceil(n_idx_heads/8) x 68 B; a call
  *    that needs more than the array returns CSA_ERR_WORKSPACE_TOO_SMALL before
- *    any launch.  Device-detected faults are not reported by this variant.
+ *    any launch.  Device-detected faults land in the array's status word:
+ *    csa_check_device_status(NULL, stream, &flags) reads and clears it.
  *  Arguments are those of csa_index_score without ws / ws_bytes. */
 #define CSA_NOALLOC_SCRATCH_BYTES (4u << 20)
 CSA_API csa_status_t csa_index_score_noalloc(const csa_cache_t* cache, const csa_rows_t* rows,
@@ -298,8 +312,21 @@ CSA_API csa_status_t csa_step(const csa_cache_t* cache, const csa_window_t* wind
                       void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, returns the status word's flags in *flags_out (host)
- * and clears it.  Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_FAULT. */
+ * and clears it.  Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_FAULT.
+ * ws == NULL reads the status word of csa_index_score_noalloc's fixed scratch
+ * array on the current device. */
 CSA_API csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out);
+
+/* csa_set_wait_budget -- failure detection (no counterpart in the pages).
+ * Every wait of the index score's pipeline (a copy landing, an MMA
+ * completing, a buffer coming free) is bounded by this many SM clocks; a wait
+ * that runs out stops the kernel, which raises CSA_FLAG_TIMEOUT in the status
+ * word, waits for the copies and tensor-core work it already issued, frees
+ * its tensor memory and returns.  Process-wide; takes effect at the next
+ * call's launch.  sm_clocks <= 0 restores the default (3e9 clocks, about 1.5
+ * s).  A small budget is a way to exercise the time-out path without a
+ * fault; scores are incomplete after a time-out. */
+CSA_API csa_status_t csa_set_wait_budget(int64_t sm_clocks);
 
 CSA_API const char* csa_status_string(csa_status_t status);
 

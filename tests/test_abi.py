@@ -76,6 +76,36 @@ def test_step_checks_both_halves_before_any_launch(lib):
     assert lib.csa_step(*args) == 2                       # n_heads out of range
 
 
+def test_unsupported_head_counts_are_rejected_before_launch(lib):
+    """The attention kernel is built for 16, 32 and 64 heads and the index
+    score for 1..128 indexer heads: any other count returns 2 (unsupported)
+    from csa_decode, csa_step and csa_sparse_attn before a launch (without a
+    GPU a launch would return 4)."""
+    buf = (C.c_uint8 * 65536)()
+    base = (C.addressof(buf) + 255) & ~255
+    pt = (C.c_int32 * 4)()
+    ints = (C.c_int32 * 8)()
+    cache = csa.CsaCache(base, base, C.addressof(pt), 1, 1, 1, 2)
+    rows = csa.CsaRows(1, C.addressof(ints), C.addressof(ints), 16, 1)
+    ws_n = csa.csa_workspace_size(csa.OP_DECODE, 1, 16, 64)
+    assert ws_n <= 65536 - 256
+    for H, Hi in [(48, 64), (8, 64), (128, 64), (63, 64), (64, 0), (64, 129)]:
+        assert lib.csa_decode(C.byref(cache), None, C.byref(rows), Hi, base, base, H, base, 1.0, base, None, None,
+                              base, ws_n, None) == 2, (H, Hi)
+        assert lib.csa_step(C.byref(cache), None, C.addressof(ints), C.addressof(ints), 1, base, base, base, None,
+                            C.byref(rows), Hi, base, base, H, base, 1.0, base, None, None, base, ws_n, None) == 2
+    for H in (48, 8, 128):
+        assert lib.csa_sparse_attn(C.byref(cache), None, C.byref(rows), base, H, base, 1.0, base, None, base, 256,
+                                   None) == 2, H
+    for Hi in (0, 129):
+        assert lib.csa_index_score(C.byref(cache), C.byref(rows), Hi, base, base, base, 64, base, ws_n, None) == 2
+
+
+def test_wait_budget_setter(lib):
+    assert lib.csa_set_wait_budget(1000) == 0
+    assert lib.csa_set_wait_budget(0) == 0            # back to the default
+
+
 def test_bad_cache_descriptors(lib):
     buf = (C.c_uint8 * 256)()
     base = C.addressof(buf)

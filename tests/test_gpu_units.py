@@ -86,21 +86,9 @@ def test_append_flags_bad_page_without_writing():
 
 
 # ------------------------------------------------------------ index score
-@pytest.mark.parametrize("Hi,rows", [(16, 1), (64, 1), (64, 6), (16, 24), (32, 3)])
-def test_index_score_matches_oracle(Hi, rows):
-    ctx = [2, 127, 128, 129, 257, 1024 + 7, 1030, 4096 + 77]
-    wl = W.custom("score", 21 + Hi + rows, [c + rows for c in ctx], [rows] * len(ctx), H=16, Hi=Hi, shuffle=True)
-    st = DeviceState(wl)
-    st.build_history()
-    s = st.step_inputs()
-    st.step_append(s)
-    ld = ((wl.max_entries + 63) // 64) * 64
-    scores = torch.full((wl.R, ld), float("nan"), device="cuda")
-    ws = torch.zeros(csa.csa_workspace_size(csa.OP_INDEX_SCORE, wl.R, wl.max_entries, 16), dtype=torch.uint8,
-                     device="cuda")
-    csa.csa_index_score(st.cache, s["rows"], Hi, s["q_idx"], s["w"], scores, ld, ws)
-    rc, flags = csa.csa_check_device_status(ws)
-    assert rc == 0 and flags == 0, flags
+def _check_scores(wl, got, ld, Hi):
+    """Every visible score within the fp32 summation bound of the oracle's,
+    scores past a row's visible range untouched (NaN)."""
     ref = oracle.build_cache(wl)
     q_idx, w, _ = wl.step_queries()
     ref_sc = oracle.index_score(ref, wl.row_req, wl.row_pos, q_idx, w, ld)
@@ -112,7 +100,6 @@ def test_index_score_matches_oracle(Hi, rows):
     # gamma_(Hi+1) * mag of the exact value, so the two are within twice that.
     u = 2.0 ** -24
     tol_f = 2.0 * (Hi + 1) * u / (1.0 - (Hi + 1) * u)
-    got = scores.cpu().numpy()
     n = wl.row_entries()
     for r in range(wl.R):
         g, o, m = got[r, :n[r]], ref_sc[r, :n[r]], mag[r, :n[r]]
@@ -121,6 +108,49 @@ def test_index_score_matches_oracle(Hi, rows):
         err = np.abs(g[fin].astype(np.float64) - o[fin].astype(np.float64))
         assert (err <= tol_f * m[fin].astype(np.float64)).all(), (r, float((err / np.maximum(m[fin], 1e-30)).max()))
         assert np.isnan(got[r, n[r]:]).all(), "scores past the visible range must be untouched"
+
+
+def _score(st, s, wl, Hi):
+    ld = ((max(wl.max_entries, 1) + 63) // 64) * 64
+    scores = torch.full((wl.R, ld), float("nan"), device="cuda")
+    ws = torch.zeros(csa.csa_workspace_size(csa.OP_INDEX_SCORE, wl.R, wl.max_entries, 16), dtype=torch.uint8,
+                     device="cuda")
+    csa.csa_index_score(st.cache, s["rows"], Hi, s["q_idx"], s["w"], scores, ld, ws)
+    rc, flags = csa.csa_check_device_status(ws)
+    return scores, ld, rc, flags
+
+
+# Hi up to the declared 128; rows of one request share the MMA's N up to 128
+# columns (64 heads: 2 rows; 8 heads: 16 rows), so these cover one and two
+# accumulators per consumer group and multi-row segments.
+@pytest.mark.parametrize("Hi,rows", [(16, 1), (64, 1), (64, 6), (16, 24), (32, 3), (96, 1), (128, 1), (128, 3),
+                                     (40, 5), (8, 20)])
+def test_index_score_matches_oracle(Hi, rows):
+    ctx = [2, 127, 128, 129, 257, 1024 + 7, 1030, 4096 + 77]
+    wl = W.custom("score", 21 + Hi + rows, [c + rows for c in ctx], [rows] * len(ctx), H=16, Hi=Hi, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    scores, ld, rc, flags = _score(st, s, wl, Hi)
+    assert rc == 0 and flags == 0, flags
+    _check_scores(wl, scores.cpu().numpy(), ld, Hi)
+
+
+def test_index_score_rows_without_entries():
+    """Rows at position 0 of a pair-pooled cache see no entry: they get no
+    segment, write nothing, and the rows around them score as usual (a row
+    group made of such rows once left a gap in the segment numbering)."""
+    ctx = [1, 300, 1, 1, 5000, 1, 129, 1]
+    wl = W.custom("score0", 29, ctx, [1] * len(ctx), H=16, Hi=64, shuffle=True)
+    assert (wl.row_entries() == 0).sum() == 5
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    scores, ld, rc, flags = _score(st, s, wl, 64)
+    assert rc == 0 and flags == 0, flags
+    _check_scores(wl, scores.cpu().numpy(), ld, 64)
 
 
 def test_identical_entries_score_identically():
@@ -297,7 +327,7 @@ def test_attention_many_rows_single_split():
 
 
 # ------------------------------------------------------------------ decode
-@pytest.mark.parametrize("H,Hi,rows", [(16, 16, 1), (64, 64, 6), (32, 32, 2)])
+@pytest.mark.parametrize("H,Hi,rows", [(16, 16, 1), (64, 64, 6), (32, 32, 2), (64, 128, 2), (16, 96, 1)])
 def test_decode_end_to_end(H, Hi, rows):
     ctx = [1, 3, 513 * 2, 1024 + 1, 2500, 5000 + 3]
     wl = W.custom("dec", 51 + rows, ctx, [min(rows, c) for c in ctx], H=H, Hi=Hi, shuffle=True)
