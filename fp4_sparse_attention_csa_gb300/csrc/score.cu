@@ -21,26 +21,26 @@
 //                        page layout is already the MMA operand layout), two
 //                        pages = one 128-entry tile per stage, 20 stages; several
 //                        warps feed the copy engine because one warp's copy
-//                        issue rate caps its bandwidth.  Every wait polls: a
-//                        thread suspended with a time hint was measured to wake
-//                        microseconds after a tcgen05.commit completed the phase.
-//                3 consumer warpgroups.  Group g takes tiles g, g+G, ... of the
-//                        CTA's range.  Its first warp gathers a tile's E8M0
-//                        bytes into the tcgen05 scale-factor atom and one lane
-//                        issues tcgen05.cp of the scales and two kind::mxf4
+//                        issue rate caps its bandwidth.
+//                3 MMA warps, one per reduction group, each walking its
+//                        group's tiles in order: gathers a tile's
+//                        E8M0 bytes into the tcgen05 scale-factor atom, and one
+//                        lane issues tcgen05.cp of the scales and two kind::mxf4
 //                        MMAs (K = 64 each): A = 128 entries x 128 dims, B =
 //                        rows*heads x 128 dims, D = fp32 [entry lane,
-//                        row*head column] in one of the group's TMEM
-//                        accumulators.  With two accumulators per group the
-//                        MMA of the group's next tile runs while its four warps
-//                        reduce the current one: per entry lane
-//                        sum_h w*relu(D) with packed fp32x2 fused
-//                        multiply-adds (even and odd heads in the two halves,
-//                        added at the end), coalesced fp32 score stores.  The
-//                        MMA issue and the reduction of a tile live in the same
-//                        warpgroup, so the only cross-role hand-offs per tile
-//                        are the page copy (stage full / free) and the MMA
-//                        completion.
+//                        row*head column] in an accumulator of the tile's group.
+//                3 reduction warpgroups  tile t goes to group t mod 3, which
+//                        owns two TMEM accumulators: the MMA of its next tile
+//                        runs while its four warps (one per TMEM lane quarter)
+//                        reduce the current one, per entry lane
+//                        sum_h w*relu(D) with packed fp32x2 fused multiply-adds
+//                        in four independent chains, then coalesced fp32 score
+//                        stores.  Each warp waits for the accumulator and frees
+//                        it on its own: no barrier couples the warps of a group
+//                        or the groups to their MMA warp beyond the accumulator
+//                        hand-off itself.  (One issuing warp alone could not keep
+//                        up: the per-tile issue path, from the page's arrival to
+//                        the MMAs, takes several hundred cycles.)
 //
 // Every wait is bounded by the call's wait budget (SM clocks).  A wait that
 // runs out raises CSA_FLAG_TIMEOUT and stops the CTA's pipeline; before the
@@ -58,12 +58,16 @@ struct Seg {
 };
 
 constexpr int kStages = 20;
-constexpr int kGroups = 3;                         // consumer warpgroups
-constexpr int kProducers = 4;                      // warps 0..3
-constexpr int kCons0 = kProducers;                 // consumer warps 4..15
-constexpr int kWarps = kProducers + 4 * kGroups;
+constexpr int kGroups = 3;                         // reduction warpgroups, one MMA warp each
+constexpr int kMma0 = 0;                           // MMA warps 0..2 (warp g serves group g)
+constexpr int kCons0 = 4;                          // reduction warps 4..15
+constexpr int kProducers = 4;                      // producer warps 3, 16, 17, 18
+constexpr int kWarps = kCons0 + 4 * kGroups + kProducers - 1;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxAcc = 2 * kGroups;               // TMEM accumulators in flight
+__host__ __device__ constexpr int producer_of_warp(int w) {
+  return w == 3 ? 0 : (w >= kCons0 + 4 * kGroups ? 1 + w - (kCons0 + 4 * kGroups) : -1);
+}
 constexpr int kTileEntries = 128;
 constexpr int kStageA = 2 * IDX_PAGE;              // two whole pages = 16 groups of 544 B
 constexpr int kMaxN = CSA_MAX_ROW_GROUP_COLS;      // rows x padded heads per MMA (128)
@@ -86,14 +90,14 @@ struct ScoreSmem {
   uint8_t a[kStages][kStageA];                 // 16-aligned (8704 = 544 * 16)
   uint8_t sfb_raw[2][kQSF];
   uint8_t sfb_atom[2][kQSF];
-  uint8_t sfa_atom[kMaxAcc][512];
+  uint8_t sfa_atom[kStages][512];              // a stage's scale atom, rewritten after the stage is refilled
   Item items[kItemCap];
   Seg segs[kItemCap];
   int32_t pref[kItemCap + 1];
   alignas(16) float wseg[4 * kGroups][kMaxN];  // per consumer warp: row kr's w at kr * Hp
   int32_t rown[4 * kGroups][kMaxGroupRows];
   uint64_t full[kStages], empty[kStages];
-  uint64_t acc_full[kMaxAcc];
+  uint64_t acc_full[kMaxAcc], acc_empty[kMaxAcc];
   uint64_t qfull[2], qempty[2], qready[2];
   uint64_t drain[kGroups];
   int32_t q_last[2];                           // latest segment whose q was loaded into each buffer
@@ -108,7 +112,7 @@ __host__ __device__ inline int hi_pad(int Hi) { return (Hi + 7) & ~7; }
 // (columns past N multiply stale rows of the B buffer and are never read).
 __host__ __device__ inline int mma_n(int N) { return N < 64 ? 64 : (N + 15) & ~15; }
 
-// Consumer groups and accumulators per group for accumulators of `cols`
+// Reduction groups and accumulators per group for accumulators of `cols`
 // TMEM columns: two per group (the next tile's MMA overlaps the current
 // reduction) when six fit, else as many groups as accumulators fit.
 __host__ __device__ inline void score_groups(int cols, int* G, int* NB) {
@@ -357,21 +361,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, ScoreS
   return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
-// Named barrier over the four warps of consumer group `grp` that also ORs a
-// flag across them, so every warp of the group takes the same branch after it.
-__device__ __forceinline__ bool group_sync_or(int grp, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, %2, 128, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(1 + grp)
-      : "memory");
-  return r != 0;
-}
-
 // A producer's wait for a free stage: the pipeline is usually full, so it
 // backs off between probes instead of taking issue slots from the consumers.
 __device__ __forceinline__ bool producer_wait(uint64_t* bar, uint32_t parity, ScoreSmem& sm, const ScoreArgs& a) {
@@ -410,10 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    for (int d = 0; d < kMaxAcc; ++d) mbar_init(&sm.acc_full[d], 1);
+    for (int d = 0; d < kMaxAcc; ++d) {
+      mbar_init(&sm.acc_full[d], 1);
+      mbar_init(&sm.acc_empty[d], 4);           // the four warps of the owning group
+    }
     for (int d = 0; d < 2; ++d) {
       mbar_init(&sm.qfull[d], 1);
-      mbar_init(&sm.qempty[d], G);             // every group leaves each segment once
+      mbar_init(&sm.qempty[d], G);             // every MMA warp leaves each segment once
       mbar_init(&sm.qready[d], 1);
     }
     for (int g = 0; g < kGroups; ++g) mbar_init(&sm.drain[g], 1);
@@ -435,16 +427,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
   // Role state kept across work chunks.  Segments are numbered in this CTA's
   // item order (ord = 0, 1, ...; every segment has a tile); ord picks the q
   // buffer (ord & 1) and the phases of the q barriers.
-  const int prod = warp < kProducers ? warp : -1;
-  const int grp = warp >= kCons0 ? (warp - kCons0) >> 2 : -1;
+  const int prod = producer_of_warp(warp);
+  const int grp = (warp >= kCons0 && warp < kCons0 + 4 * kGroups) ? (warp - kCons0) >> 2 : -1;
   const bool cons = grp >= 0 && grp < G;
-  const bool leader_warp = cons && (warp & 3) == 0;        // issues the group's MMAs
+  const int mg = warp - kMma0;                             // MMA warp of group mg
+  const bool mma_warp = mg >= 0 && mg < G && warp < kMma0 + kGroups;
   int p_last_it = -1;                                      // producer: last item copied
-  int l_ord = -1, l_par = 0, l_desc_ord = -1;             // leader: segment entered, descriptors
+  int l_ord = -1, l_par = 0, l_desc_ord = -1;             // MMA warp: segment entered, descriptors
   uint64_t l_bdesc = 0;
   uint32_t l_id0 = 0, l_id1 = 0;
   bool l_issued = false;
-  int u_issue = 0, u_done = 0;                             // group's own tiles issued / reduced
   int e_gseg = -1;                                         // consumer warp: segment staged
   int ord_base = 0;                                        // ordinal of the window's first segment
 
@@ -519,34 +511,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
         }
       }
       __syncwarp();
-    } else if (cons) {
-      // ================= consumer group grp: items it with it % G == grp =================
-      const int q = warp & 3;                       // TMEM lane quarter of this warp
-      const int mrow = 32 * q + lane;               // entry within the tile
-      const int cw = warp - kCons0;
-      float* ew = sm.wseg[cw];                      // this warp's copy of the segment's w
-      int32_t* en = sm.rown[cw];                    // and of its rows' visible lengths
-      int first_own = grp - (it_base % G);
-      if (first_own < 0) first_own += G;
+    } else if (mma_warp) {
+      // ================= MMA warp mg: the items of group mg =================
       const uint32_t sfb_t = tmem + kTmemSFB;
       const uint64_t adesc0 = smem_desc(smem_u32(sm.a[0]), 128, IDX_GROUP, kSwizzleNone);
       bool ok = true;
-
-      // Leader warp: enter every segment up to ordinal `ord` in order.  Every
-      // group enters every segment of the CTA's range (so each q buffer is
-      // released by all of them, and the group that copies a segment's q
-      // scales to TMEM always reaches it), whether or not it has a tile there.
+      // Enter every segment up to ordinal `ord` in order.  Every MMA warp
+      // enters every segment of the CTA's range (so each q buffer is released
+      // by all of them, and the warp that copies a segment's q scales to TMEM
+      // always reaches it), whether or not its group has a tile there.
       auto enter_upto = [&](int ord) -> bool {
         while (l_ord < ord) {
           const int o = l_ord + 1;
-          // leaving l_ord: its q buffer is free once this group's MMAs complete
+          // leaving l_ord: its q buffer is free once this warp's MMAs complete
           if (l_ord >= 0 && lane == 0) tc_commit(&sm.qempty[l_ord & 1]);
           const int par = o & 1;
           if (!warp_wait<true>(&sm.qfull[par], (o >> 1) & 1, sm, a)) return false;
-          if (o % G == grp) {
-            // one group per segment lays the q scales out as an atom and copies it
-            // to TMEM; the commit tells every group the copy has landed.  Rows past
-            // N inside the atom hold stale bytes; their D columns are never read.
+          if (o % G == mg) {
+            // one warp per segment lays the q scales out as an atom and copies it
+            // to TMEM; the commit tells the others the copy has landed.  Rows
+            // past N inside the atom hold stale bytes; their D columns are never read.
             sf_to_atom(sm.sfb_raw[par], sm.sfb_atom[par], lane);
             fence_proxy_async_smem();
             __syncwarp();
@@ -559,21 +543,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
           }
           if (!warp_wait<true>(&sm.qready[par], (o >> 1) & 1, sm, a)) return false;
           l_ord = o;
+          l_issued = true;
         }
         return true;
       };
-
-      // Leader warp, before the group barrier: enter item i's segment, wait for
-      // its pages and lay its E8M0 bytes out as the tcgen05 scale-factor atom
-      // of the accumulator it will use (that atom and the accumulator's TMEM
-      // scale columns were last read by the MMA two tiles back, which has
-      // completed).
-      int p_it = -1;                                // item prepared, not yet launched
-      auto prepare = [&](int i) -> bool {
+      int i = mg - (it_base % G);
+      if (i < 0) i += G;
+      for (; i < m; i += G) {
+        if (aborted(sm)) { ok = false; break; }
         const Item e = sm.items[i];
         const int ord = ord_base + e.seg;
         if (l_desc_ord != ord) {                    // B operand and N of this segment
-          if (!enter_upto(ord)) return false;
+          if (!enter_upto(ord)) { ok = false; break; }
           const int N = sm.segs[e.seg].nrows * Hp;
           l_par = ord & 1;
           l_bdesc = smem_desc(smem_u32(sm.qdata[l_par]), 16, 512, kSwizzle64B);
@@ -582,9 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
           l_desc_ord = ord;
         }
         const int it = it_base + i;
-        const int slot = grp * NB + (u_issue % NB);
+        const int u = it / G;                        // the tile's index within its group
+        const int slot = mg * NB + (u % NB);
         const int s = it % kStages, use = it / kStages;
-        if (!warp_wait<true>(&sm.full[s], use & 1, sm, a)) return false;
+        if (!warp_wait<true>(&sm.full[s], use & 1, sm, a)) { ok = false; break; }
         // the tile's scale words: entry row r is page r / 64, group (r % 64) / 8, word r % 8
         {
           const uint8_t* st = sm.a[s];
@@ -594,26 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
             const int r = lane + 32 * j;
             wv[j] = *reinterpret_cast<const uint32_t*>(st + (r >> 6) * IDX_PAGE + idx_scale_off(r & 63, 0));
           }
-          reinterpret_cast<uint4*>(sm.sfa_atom[slot])[lane] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          reinterpret_cast<uint4*>(sm.sfa_atom[s])[lane] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        p_it = it;
-        return true;
-      };
-
-      // Leader warp, after the group barrier (the accumulator's previous tile
-      // has been reduced by all four warps): copy the scales to TMEM and issue
-      // the two MMAs of the prepared tile.
-      auto launch = [&]() {
-        if (p_it < 0) return;
-        const int it = p_it;
-        const int slot = grp * NB + (u_issue % NB);
-        const int s = it % kStages;
+        // the accumulator's previous tile has been reduced by its four warps
+        if (u >= NB && !warp_wait<true>(&sm.acc_empty[slot], ((u / NB) - 1) & 1, sm, a)) { ok = false; break; }
         if (lane == 0) {
           tc_fence_after();
           const uint32_t sfa = tmem + kTmemSFA + 4 * slot;
-          tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[slot]), 16, 128, kSwizzleNone));
+          tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(sm.sfa_atom[s]), 16, 128, kSwizzleNone));
           // A: the two pages as they landed: 8-entry groups IDX_GROUP apart, 16-byte
           // core matrices 128 B apart along K (no swizzle); second K half at +256 B
           const uint64_t ad = adesc0 + (uint64_t)(s * (kStageA >> 4));
@@ -626,23 +598,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
         }
         __syncwarp();
         l_issued = true;
-        p_it = -1;
-        ++u_issue;
-      };
-
-      // All four warps: reduce item i from the group's oldest accumulator.
-      auto reduce = [&](int i) -> bool {
+      }
+      // the chunk's segments past the group's last tile
+      if (ok && !aborted(sm)) enter_upto(ord_base + sm.items[m - 1].seg);
+    } else if (cons) {
+      // ================= reduction group grp: items it with it % G == grp =================
+      const int q = warp & 3;                       // TMEM lane quarter of this warp
+      const int mrow = 32 * q + lane;               // entry within the tile
+      const int cw = warp - kCons0;
+      float* ew = sm.wseg[cw];                      // this warp's copy of the segment's w
+      int32_t* en = sm.rown[cw];                    // and of its rows' visible lengths
+      int i = grp - (it_base % G);
+      if (i < 0) i += G;
+      for (; i < m; i += G) {
+        if (aborted(sm)) break;
         const Item e = sm.items[i];
         const Seg sg = sm.segs[e.seg];
         const int gseg = seg0 + e.seg;
         if (gseg != e_gseg) {                       // stage this segment's weights and row lengths
-          __syncwarp();                             // (per warp: no cross-warp barrier here)
+          __syncwarp();
           for (int x = lane; x < sg.nrows * Hi; x += 32) ew[(x / Hi) * Hp + x % Hi] = __ldg(a.w + (size_t)sg.r0 * Hi + x);
           for (int x = lane; x < sg.nrows; x += 32) en[x] = (__ldg(a.row_pos + sg.r0 + x) + 1) / a.P;
           __syncwarp();
           e_gseg = gseg;
         }
-        const int slot = grp * NB + (u_done % NB);
+        const int it = it_base + i;
+        const int u = it / G;
+        const int slot = grp * NB + (u % NB);
+        if (!warp_wait<true>(&sm.acc_full[slot], (u / NB) & 1, sm, a)) break;
         tc_fence_after();
         const int ient = e.tile * kTileEntries + mrow;
         const bool page_ok = (mrow < 64) ? (e.pg0 >= 0) : (e.pg1 >= 0);
@@ -653,19 +636,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
           uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
           float acc1 = 0.0f;                        // heads past the last full group of 32
           int h0 = 0;
-          for (; h0 + 64 <= Hi; h0 += 64) {         // two TMEM loads in flight, one wait
-            uint32_t v[64];
-            tmem_ld32(dbase + kr * Hp + h0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld32(dbase + kr * Hp + h0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              const float4 w4 = *reinterpret_cast<const float4*>(wr + h0 + j);
-              uint64_t& c = acc2[(j >> 2) & 3];
-              c = ffma2(pack2(w4.x, w4.y), pack2(relu(v[j]), relu(v[j + 1])), c);
-              c = ffma2(pack2(w4.z, w4.w), pack2(relu(v[j + 2]), relu(v[j + 3])), c);
-            }
-          }
           for (; h0 + 32 <= Hi; h0 += 32) {
             uint32_t v[32];
             tmem_ld32(dbase + kr * Hp + h0, v);
@@ -693,42 +663,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
             a.scores[(size_t)(sg.r0 + kr) * a.ld + ient] = page_ok ? acc : -INFINITY;
         }
         tc_fence_before();
-        ++u_done;
-        return true;
-      };
-
-      // Per own tile u: the leader thread polls the MMA's completion, then a
-      // group barrier (which also agrees on stopping) tells the four warps the
-      // accumulator is ready and that every warp has finished the previous
-      // tile.  With two accumulators the leader warp then issues tile u+1
-      // into the other one before it joins the reduction of tile u; with one,
-      // the issue of tile u waits for the reduction of tile u-1.
-      auto acc_ready = [&](int u) {
-        if (leader_warp && lane == 0 && !aborted(sm)) {
-          const int slot = grp * NB + (u % NB);
-          wait_or_abort<true>(&sm.acc_full[slot], (u / NB) & 1, sm, a);
-        }
-      };
-      const int n_own = first_own < m ? (m - 1 - first_own) / G + 1 : 0;
-      if (NB == 2 && leader_warp && n_own > 0 && !aborted(sm)) {
-        if (prepare(first_own)) launch();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[slot]);
       }
-      for (int k = 0; k < n_own; ++k) {
-        const int ei = first_own + k * G;
-        if (NB == 1) {
-          if (leader_warp && !aborted(sm)) prepare(ei);
-          if (group_sync_or(grp, aborted(sm))) { ok = false; break; }
-          if (leader_warp) launch();
-        } else if (leader_warp && k + 1 < n_own && !aborted(sm)) {
-          prepare(ei + G);                          // overlaps the wait for tile k's MMA
-        }
-        acc_ready(u_done);
-        if (group_sync_or(grp, aborted(sm))) { ok = false; break; }
-        if (NB == 2 && leader_warp) launch();
-        reduce(ei);
-      }
-      // the chunk's segments past the group's last tile
-      if (leader_warp && ok && !aborted(sm)) enter_upto(ord_base + sm.items[m - 1].seg);
     }
     // ---- chunk done: every role has finished with this work table ----------------
     tc_fence_before();
@@ -755,14 +692,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
       if (it < 0) break;
       if (!mbar_wait(&sm.full[it % kStages], (it / kStages) & 1)) raise_flag(a.status, CSA_FLAG_TIMEOUT);
     }
-    if (prod < 2) {
+    if (prod < 2) {                                 // producers 0 and 1 drain q buffers 0 and 1
       const int ql = sm.q_last[prod];
       if (ql >= 0 && !mbar_wait(&sm.qfull[ql & 1], (ql >> 1) & 1)) raise_flag(a.status, CSA_FLAG_TIMEOUT);
     }
   }
-  if (leader_warp && lane == 0 && (l_issued || l_ord >= 0)) {
-    tc_commit(&sm.drain[grp]);
-    if (!mbar_wait(&sm.drain[grp], 0)) raise_flag(a.status, CSA_FLAG_TIMEOUT);
+  if (mma_warp && lane == 0 && l_issued) {
+    tc_commit(&sm.drain[mg]);
+    if (!mbar_wait(&sm.drain[mg], 0)) raise_flag(a.status, CSA_FLAG_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
