@@ -203,16 +203,58 @@ def cpu_baseline(wl, rows_cap, budget_s=20.0):
     ref = oracle.build_cache(wl, requests=reqs, threads=cores)
     q_idx, w, q = wl.step_queries()
     rr, rp = wl.row_req[rows], wl.row_pos[rows]
-    done, t0 = 0, time.perf_counter()
-    while True:
-        oracle.decode(ref, rr, rp, q_idx[rows], w[rows], q[rows], wl.softmax_scale, threads=cores)
-        done += len(rows)
-        el = time.perf_counter() - t0
-        if el > budget_s * 0.5 or done >= 4 * len(rows):
-            break
-    return {"value": done / el, "unit": "rows/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(rows)} rows of {wl.name} (requests {reqs[0]}..{reqs[-1]}), x{done // len(rows)}; "
-                      f"score + top-512 + attention, {cores} threads"}
+
+    def rate(threads, n_rows, budget):
+        done, t0 = 0, time.perf_counter()
+        while True:
+            oracle.decode(ref, rr[:n_rows], rp[:n_rows], q_idx[rows][:n_rows], w[rows][:n_rows], q[rows][:n_rows],
+                          wl.softmax_scale, threads=threads)
+            done += n_rows
+            el = time.perf_counter() - t0
+            if el > budget or done >= 4 * n_rows:
+                return done / el, done // n_rows
+
+    value, reps = rate(cores, len(rows), budget_s * 0.5)
+    single, reps1 = rate(1, 1, budget_s * 0.25)        # one thread, one row of the same sample
+    return {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} rows of {wl.name} (requests {reqs[0]}..{reqs[-1]}), x{reps}; "
+                      f"score + top-512 + attention, {cores} threads",
+            "single_thread": {"value": single, "unit": "rows/s", "cores": 1,
+                              "sample": f"row 0 of the same sample, x{reps1}, one thread"}}
+
+
+def time_workload(cfg, steps, warmup, flush_l2):
+    """Median csa_step time of another workload, same protocol (L2 flushed
+    before every step, CUDA events on the launching stream)."""
+    import torch
+    from fp4_sparse_attention_csa_gb300.session import DeviceState
+    wl = W.config(cfg)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    stream = torch.cuda.current_stream()
+    for _ in range(max(warmup, 3)):
+        flush_l2()
+        st.step(s)
+    ev = []
+    for _ in range(steps):
+        flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st.step(s)
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = np.array([a.elapsed_time(b) for a, b in ev])
+    ab = algorithmic_bytes(wl, s["topk"].cpu().numpy())
+    med = float(np.median(ms))
+    gbs = ab["total"] / (med / 1e3) / 1e9
+    del st, s
+    torch.cuda.empty_cache()
+    return {"workload": W.CONFIG_NAMES[cfg], "rows_per_step": wl.R, "steps": steps,
+            "step_ms_median": med, "step_ms_p10": float(np.percentile(ms, 10)),
+            "step_ms_p90": float(np.percentile(ms, 90)), "rows_per_s": wl.R / (med / 1e3),
+            "path_unique_bytes": ab["total"], "path_gbs": gbs, "path_frac_of_8tbs": gbs / 8000.0}
 
 
 def main():
@@ -225,6 +267,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the speculative-verify step timed beside the serving batch")
     ap.add_argument("--compress", action="store_true",
                     help="append through csa_append_compress (RMSNorm + RoPE before quantisation)")
     args = ap.parse_args()
@@ -391,6 +435,11 @@ def main():
                "l2": "not flushed inside the pipeline (the cache pools exceed L2)",
                "serial_value": wl.R * args.steps * world / (serial_ms / 1e3)}
 
+    # ---- the other workload the bandwidth target names: speculative verify
+    secondary = None
+    if cfg == 4 and not args.no_secondary and not args.compress:
+        secondary = time_workload(3, max(10, min(args.steps, 50)), args.warmup, flush_l2)
+
     launches_per_step = 5          # append, score prep, index score, top-k, attention (splits merge in-cluster)
     if rank != 0:
         return
@@ -411,7 +460,8 @@ def main():
                    "path_frac_of_hbm": path_gbs / peak, "path_frac_of_8tbs": path_gbs / 8000.0,
                    "bytes": ab, "parallelism": f"replicas x{world}",
                    "append": "csa_append_compress (RMSNorm + RoPE)" if args.compress else "csa_append",
-                   "call": "csa_step (append + decode in one call)"},
+                   "call": "csa_step (append + decode in one call)",
+                   "secondary": secondary},
         "roofline": {"bound": "hbm", "kernel": "index score (k_score_prep + k_index_score)",
                      "achieved": score_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": score_gbs / peak, "traffic": traffic,

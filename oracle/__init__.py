@@ -69,6 +69,8 @@ def lib():
             L.or_topk_row.restype = None
             L.or_attention_row.argtypes = [vp, i32, i32, vp, i32, vp, f32, vp, vp]
             L.or_attention_row.restype = None
+            L.or_attention_row_rope.argtypes = [vp, i32, i32, vp, i32, vp, f32, vp, vp, i32, vp, vp]
+            L.or_attention_row_rope.restype = C.c_int
             L.or_decode.argtypes = [vp, i32, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, i64, i32]
             L.or_decode.restype = None
             _lib = L
@@ -244,6 +246,19 @@ def attention_row(cache, req, pos, topk, q_row, softmax_scale):
     lib().or_attention_row(C.byref(s), int(req), int(pos), _p(topk), H, _p(q_row),
                            float(softmax_scale), _p(out), _p(lse))
     return out, lse
+
+
+def attention_row_rope(cache, req, pos, topk, q_row, softmax_scale, rope_cos, rope_sin):
+    """attention_row with the query (row position) and the window tokens (their
+    positions) rotated by the tables; returns (out, lse, rc)."""
+    topk, q_row = _c(topk, np.int32), _c(q_row, np.uint16)
+    cs, sn = _c(rope_cos, np.float32), _c(rope_sin, np.float32)
+    H = q_row.size // D
+    out, lse = np.zeros((H, D), np.float32), np.zeros(H, np.float32)
+    s = cache.struct()
+    rc = lib().or_attention_row_rope(C.byref(s), int(req), int(pos), _p(topk), H, _p(q_row),
+                                     float(softmax_scale), _p(cs), _p(sn), int(cs.shape[0]), _p(out), _p(lse))
+    return out, lse, int(rc)
 
 
 def decode(cache, row_req, row_pos, q_idx, w, q, softmax_scale, threads=1):

@@ -460,9 +460,35 @@ static void dequant_main_entry(const or_cache_t* c, int32_t req, int32_t e, floa
   for (int d = 0; d < OR_D; ++d) v512[d] = or_e2m1_decode(nibble(data, d)) * or_e4m3_decode(sc[d / 16]);
 }
 
+/* The rotary reading for attention (no counterpart printed on the pages beyond
+ * "Q RoPE merged into the attention-buffer write", [SGL] "DSpark adaptation
+ * and optimization"): the same rotate-half as the compressor step above, on
+ * the last 64 dims, with table row = position.  The query of a row at
+ * position t is rotated with row t; a window token at position p, whose ring
+ * slot holds it raw, is rotated with row p before it serves as key and value
+ * (keys = values = the latent); the global entries were rotated when they
+ * were appended and are used as stored.  rope_cos == NULL: no rotation. */
+int or_attention_row_rope(const or_cache_t* c, int32_t req, int32_t pos,
+                          const int32_t* topk512, int32_t n_heads, const uint16_t* q_row,
+                          float softmax_scale, const float* rope_cos, const float* rope_sin,
+                          int32_t rope_rows, float* out, float* lse);
+
 void or_attention_row(const or_cache_t* c, int32_t req, int32_t pos,
                       const int32_t* topk512, int32_t n_heads, const uint16_t* q_row,
                       float softmax_scale, float* out, float* lse) {
+  (void)or_attention_row_rope(c, req, pos, topk512, n_heads, q_row, softmax_scale, NULL, NULL, 0, out, lse);
+}
+
+int or_attention_row_rope(const or_cache_t* c, int32_t req, int32_t pos,
+                          const int32_t* topk512, int32_t n_heads, const uint16_t* q_row,
+                          float softmax_scale, const float* rope_cos, const float* rope_sin,
+                          int32_t rope_rows, float* out, float* lse) {
+  const int rope = rope_cos != NULL && rope_sin != NULL;
+  if (rope && (pos < 0 || pos >= rope_rows)) {      /* no table row for this position */
+    for (int64_t i = 0; i < (int64_t)n_heads * OR_D; ++i) out[i] = 0.0f;
+    if (lse) for (int h = 0; h < n_heads; ++h) lse[h] = -INFINITY;
+    return -1;
+  }
   int32_t n = row_visible(pos, c->pool_ratio);
   int32_t nk = 0;
   float* keys = (float*)malloc(sizeof(float) * (size_t)(OR_TOPK + OR_WINDOW) * OR_D);
@@ -479,6 +505,9 @@ void or_attention_row(const or_cache_t* c, int32_t req, int32_t pos,
       const uint8_t* codes = c->win_codes + slot * OR_D;
       float s = c->win_scale[slot];
       for (int d = 0; d < OR_D; ++d) keys[(int64_t)nk * OR_D + d] = or_e4m3_decode(codes[d]) * s;
+      if (rope)
+        or_compress_vec(keys + (int64_t)nk * OR_D, OR_D, NULL, 0.0f, rope_cos + (int64_t)p * 32,
+                        rope_sin + (int64_t)p * 32);
       ++nk;
     }
   }
@@ -487,6 +516,7 @@ void or_attention_row(const or_cache_t* c, int32_t req, int32_t pos,
   for (int h = 0; h < n_heads; ++h) {
     float* o = out + (int64_t)h * OR_D;
     for (int d = 0; d < OR_D; ++d) q[d] = or_bf16_to_f32(q_row[(int64_t)h * OR_D + d]);
+    if (rope) or_compress_vec(q, OR_D, NULL, 0.0f, rope_cos + (int64_t)pos * 32, rope_sin + (int64_t)pos * 32);
     if (nk == 0) {
       for (int d = 0; d < OR_D; ++d) o[d] = 0.0f;
       if (lse) lse[h] = -INFINITY;
@@ -513,6 +543,7 @@ void or_attention_row(const or_cache_t* c, int32_t req, int32_t pos,
   }
   free(logit);
   free(keys);
+  return 0;
 }
 
 /* ======================================================================

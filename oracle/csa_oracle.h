@@ -121,6 +121,16 @@ void or_attention_row(const or_cache_t* c, int32_t req, int32_t pos,
                       const int32_t* topk512, int32_t n_heads, const uint16_t* q_row,
                       float softmax_scale, float* out /*[H,512]*/, float* lse /*[H]*/);
 
+/* or_attention_row with the query and the window tokens rotated (rotate-half
+ * on the last 64 dims, as or_compress_vec, with rope_cos/rope_sin row = the
+ * position: t for the query, p for a window token, which is rotated as key
+ * and value alike); global entries are used as stored.  NULL tables: no
+ * rotation.  Returns -1 (zero output, lse -inf) when t >= rope_rows. */
+int or_attention_row_rope(const or_cache_t* c, int32_t req, int32_t pos,
+                          const int32_t* topk512, int32_t n_heads, const uint16_t* q_row,
+                          float softmax_scale, const float* rope_cos, const float* rope_sin,
+                          int32_t rope_rows, float* out /*[H,512]*/, float* lse /*[H]*/);
+
 /* Whole decode step for all rows (score -> top-512 -> attention), split over
  * `threads` POSIX threads by row.  scores_ws: [num_rows, ld] scratch. */
 void or_decode(const or_cache_t* c, int32_t num_rows, const int32_t* row_req,

@@ -478,3 +478,95 @@ def test_compressed_append_token_by_token_equals_one_call(P):
     plain = oracle.Cache(B * pages_per_req, pt, P)
     plain.append(np.zeros(B, np.int32), np.array([0, L, 2 * L], np.int32), kvb.reshape(-1, 512), ixb.reshape(-1, 128))
     assert not np.array_equal(plain.kv_pool, one.kv_pool)     # the steps did change the entries
+
+
+# ---- P-12: rotary attention (query and window tokens; NEXT f-3) ------------------
+# A quarter turn (cos 0, sin 1) maps each pair (a, b) of the last 64 dims to
+# (-b, a): an exact permutation with a sign flip, both for E4M3 window codes and
+# for bf16 query bits.  So the rotary oracle with quarter-turn table rows must
+# equal the plain oracle (itself pinned by P-9) run on inputs permuted by hand.
+def _tables(rows, turned):
+    cs = np.ones((rows, 32), np.float32)
+    sn = np.zeros((rows, 32), np.float32)
+    for r in turned:
+        cs[r], sn[r] = 0.0, 1.0
+    return cs, sn
+
+
+def _turn_e4m3(codes):
+    c = codes.copy()
+    a, b = codes[448:480].copy(), codes[480:512].copy()
+    c[448:480] = b ^ np.uint8(0x80)                        # -b: the E4M3 sign bit
+    c[480:512] = a
+    return c
+
+
+def _turn_bf16(q_row):
+    q = q_row.copy()
+    a, b = q_row[..., 448:480].copy(), q_row[..., 480:512].copy()
+    q[..., 448:480] = b ^ np.uint16(0x8000)               # -b: the bf16 sign bit
+    q[..., 480:512] = a
+    return q
+
+
+def _rope_case():
+    wl, cache = _tiny_cache(700, Hi=2, H=3, seed=12)      # row at 699: 350 entries, window 572..699
+    q_idx, w, q = wl.step_queries()
+    _, _, topk, _ = oracle.decode(cache, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale)
+    return wl, cache, q, topk
+
+
+def test_rope_identity_tables_change_nothing():
+    wl, cache, q, topk = _rope_case()
+    cs, sn = _tables(700, [])
+    o, l, rc = oracle.attention_row_rope(cache, 0, 699, topk[0], q[0], wl.softmax_scale, cs, sn)
+    o0, l0 = oracle.attention_row(cache, 0, 699, topk[0], q[0], wl.softmax_scale)
+    assert rc == 0 and np.array_equal(o, o0) and np.array_equal(l, l0)
+
+
+def test_rope_window_token_turned_with_its_own_position():
+    """Only table row 600 turns: exactly the window token at position 600 is
+    rotated, as key and as value; the query (row 699) and the rest are not."""
+    wl, cache, q, topk = _rope_case()
+    cs, sn = _tables(700, [600])
+    o, l, rc = oracle.attention_row_rope(cache, 0, 699, topk[0], q[0], wl.softmax_scale, cs, sn)
+    codes, _ = cache.window_slot(0, 600)
+    codes[:] = _turn_e4m3(codes.copy())
+    o0, l0 = oracle.attention_row(cache, 0, 699, topk[0], q[0], wl.softmax_scale)
+    assert rc == 0 and np.array_equal(o, o0) and np.array_equal(l, l0)
+
+
+def test_rope_query_turned_with_the_row_position():
+    wl, cache, q, topk = _rope_case()
+    cs, sn = _tables(700, [699])
+    o, l, rc = oracle.attention_row_rope(cache, 0, 699, topk[0], q[0], wl.softmax_scale, cs, sn)
+    # row 699 also turns the window token at 699 (the row's own token)
+    codes, _ = cache.window_slot(0, 699)
+    codes[:] = _turn_e4m3(codes.copy())
+    o0, l0 = oracle.attention_row(cache, 0, 699, topk[0], _turn_bf16(q[0]), wl.softmax_scale)
+    assert rc == 0 and np.array_equal(o, o0) and np.array_equal(l, l0)
+
+
+def test_rope_leaves_global_entries_as_stored():
+    """Every table row turns: the query and all 128 window tokens are turned,
+    the 350 global entries (rotated when appended) are used as stored."""
+    wl, cache, q, topk = _rope_case()
+    cs, sn = _tables(700, range(700))
+    o, l, rc = oracle.attention_row_rope(cache, 0, 699, topk[0], q[0], wl.softmax_scale, cs, sn)
+    kv_before = cache.kv_pool.copy()
+    for p in range(572, 700):
+        codes, _ = cache.window_slot(0, p)
+        codes[:] = _turn_e4m3(codes.copy())
+    o0, l0 = oracle.attention_row(cache, 0, 699, topk[0], _turn_bf16(q[0]), wl.softmax_scale)
+    assert np.array_equal(cache.kv_pool, kv_before)
+    assert rc == 0 and np.array_equal(o, o0) and np.array_equal(l, l0)
+    # and the rotation is not a no-op here
+    o1, _ = oracle.attention_row(cache, 0, 699, topk[0], q[0], wl.softmax_scale)
+    assert not np.array_equal(o, o1)
+
+
+def test_rope_row_beyond_the_tables_is_rejected():
+    wl, cache, q, topk = _rope_case()
+    cs, sn = _tables(699, [])                              # rows 0..698 only
+    o, l, rc = oracle.attention_row_rope(cache, 0, 699, topk[0], q[0], wl.softmax_scale, cs, sn)
+    assert rc == -1 and not o.any() and np.isneginf(l).all()
