@@ -48,6 +48,11 @@ class CsaCompress(C.Structure):
                 ("rope_cos", C.c_void_p), ("rope_sin", C.c_void_p), ("rope_rows", C.c_int32)]
 
 
+class CsaAttnOpts(C.Structure):
+    _fields_ = [("plan_in", C.c_void_p), ("plan_out", C.c_void_p), ("rope_cos", C.c_void_p),
+                ("rope_sin", C.c_void_p), ("rope_rows", C.c_int32)]
+
+
 class CsaRows(C.Structure):
     _fields_ = [("num_rows", C.c_int32), ("row_req", C.c_void_p), ("row_pos", C.c_void_p),
                 ("max_entries", C.c_int32), ("max_rows_per_req", C.c_int32)]
@@ -77,13 +82,17 @@ def lib():
             L.csa_index_score_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp]
             L.csa_step.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp,
                                    vp, vp, sz, vp]
+            L.csa_step_ex.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp,
+                                      vp, vp, vp, sz, vp]
+            L.csa_sparse_attn_ex.argtypes = [vp, vp, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
+            L.csa_decode_ex.argtypes = [vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, vp, sz, vp]
             L.csa_check_device_status.argtypes = [vp, vp, C.POINTER(C.c_uint32)]
             L.csa_set_wait_budget.argtypes = [C.c_int64]
             L.csa_status_string.argtypes = [i32]
             L.csa_status_string.restype = C.c_char_p
             for fn in ("csa_append", "csa_append_compress", "csa_index_score", "csa_topk", "csa_sparse_attn",
                        "csa_decode", "csa_step", "csa_index_score_noalloc", "csa_check_device_status",
-                       "csa_set_wait_budget"):
+                       "csa_set_wait_budget", "csa_sparse_attn_ex", "csa_decode_ex", "csa_step_ex"):
                 getattr(L, fn).restype = C.c_int
             _lib = L
     return _lib
@@ -178,6 +187,42 @@ def csa_sparse_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, ou
                                C.byref(rows), _ptr(topk_idx), int(n_heads), _ptr(q), float(softmax_scale),
                                _ptr(out), _ptr(lse), _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "csa_sparse_attn")
+
+
+def make_attn_opts(plan_in=None, plan_out=None, rope_cos=None, rope_sin=None):
+    """Options of the attention step: plans [R, 512] int32, rotary tables [rows, 32] fp32."""
+    rows = 0 if rope_cos is None else int(rope_cos.shape[0])
+    return CsaAttnOpts(_ptr(plan_in), _ptr(plan_out), _ptr(rope_cos), _ptr(rope_sin), rows)
+
+
+def _opt(o):
+    return C.byref(o) if o is not None else None
+
+
+def csa_sparse_attn_ex(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, opts, ws, stream=None):
+    rc = lib().csa_sparse_attn_ex(C.byref(cache), C.byref(window) if window is not None else None,
+                                  C.byref(rows), _ptr(topk_idx), int(n_heads), _ptr(q), float(softmax_scale),
+                                  _ptr(out), _ptr(lse), _opt(opts), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "csa_sparse_attn_ex")
+
+
+def csa_decode_ex(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, opts,
+                  ws, stream=None):
+    rc = lib().csa_decode_ex(C.byref(cache), C.byref(window) if window is not None else None, C.byref(rows),
+                             int(n_idx_heads), _ptr(q_idx), _ptr(w), int(n_heads), _ptr(q), float(softmax_scale),
+                             _ptr(out), _ptr(lse), _ptr(topk_out), _opt(opts), _ptr(ws), _nbytes(ws),
+                             _stream(stream))
+    _check(rc, "csa_decode_ex")
+
+
+def csa_step_ex(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, compress, rows, n_idx_heads,
+                q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, opts, ws, stream=None):
+    rc = lib().csa_step_ex(C.byref(cache), C.byref(window) if window is not None else None, _ptr(pos0),
+                           _ptr(tok_off), int(total_tokens), _ptr(kv_in), _ptr(idx_in), _ptr(pending),
+                           C.byref(compress) if compress is not None else None, C.byref(rows), int(n_idx_heads),
+                           _ptr(q_idx), _ptr(w), int(n_heads), _ptr(q), float(softmax_scale), _ptr(out), _ptr(lse),
+                           _ptr(topk_out), _opt(opts), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "csa_step_ex")
 
 
 def csa_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, ws,

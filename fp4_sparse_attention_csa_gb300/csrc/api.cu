@@ -67,6 +67,19 @@ DecodeLayout decode_layout(int32_t R, int32_t max_entries) {
   return L;
 }
 
+// Attention options: pointers aligned, a plan read only where no selection is
+// computed, rotary tables with at least one row.
+csa_status_t check_attn_opts(const csa_attn_opts_t* o, bool plan_in_allowed) {
+  if (!o) return CSA_OK;
+  if (o->plan_in && (!plan_in_allowed || !aligned(o->plan_in, 4))) return CSA_ERR_INVALID_ARGUMENT;
+  if (o->plan_out && !aligned(o->plan_out, 4)) return CSA_ERR_INVALID_ARGUMENT;
+  if (o->plan_in && o->plan_out) return CSA_ERR_INVALID_ARGUMENT;
+  if ((o->rope_cos == nullptr) != (o->rope_sin == nullptr)) return CSA_ERR_INVALID_ARGUMENT;
+  if (o->rope_cos && (o->rope_rows < 1 || !aligned(o->rope_cos, 4) || !aligned(o->rope_sin, 4)))
+    return CSA_ERR_INVALID_ARGUMENT;
+  return CSA_OK;
+}
+
 // The attention kernel is compiled for these head counts only.
 bool attn_heads_supported(int32_t H) { return H == 16 || H == 32 || H == 64; }
 
@@ -99,8 +112,14 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
 
 csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                       const int32_t* topk, int32_t H, const void* q, float softmax_scale, void* out, float* lse,
-                      void* ws, Order order, cudaStream_t stream) {
+                      const csa_attn_opts_t* opts, void* ws, Order order, cudaStream_t stream) {
   AttnArgs a;
+  a.plan_in = opts ? opts->plan_in : nullptr;
+  a.plan_out = opts ? opts->plan_out : nullptr;
+  const bool rope = opts && opts->rope_cos && opts->rope_sin;
+  a.rope_cos = rope ? opts->rope_cos : nullptr;
+  a.rope_sin = rope ? opts->rope_sin : nullptr;
+  a.rope_rows = rope ? opts->rope_rows : 0;
   a.kv_pool = static_cast<const uint8_t*>(cache->kv_pool);
   a.page_table = cache->page_table;
   a.num_pages = cache->num_pages;
@@ -193,8 +212,8 @@ csa_status_t check_decode(const csa_cache_t* cache, const csa_window_t* window, 
 // the order of the score prep, the first of these kernels.
 csa_status_t run_decode(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                         int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
-                        float softmax_scale, void* out, float* lse, int32_t* topk_out, void* ws, Order first,
-                        cudaStream_t stream) {
+                        float softmax_scale, void* out, float* lse, int32_t* topk_out,
+                        const csa_attn_opts_t* opts, void* ws, Order first, cudaStream_t stream) {
   const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries);
   uint8_t* base = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(base + L.scores);
@@ -213,7 +232,7 @@ csa_status_t run_decode(const csa_cache_t* cache, const csa_window_t* window, co
   t.out = topk;
   t.status = static_cast<uint32_t*>(ws);
   if ((s = from_cuda(launch_topk(t, Order::kChained, stream))) != CSA_OK) return s;
-  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, ws, Order::kChained, stream);
+  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, opts, ws, Order::kChained, stream);
 }
 
 }  // namespace
@@ -295,25 +314,46 @@ csa_status_t csa_topk(int32_t num_rows, const float* scores, int32_t ld, const i
 csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                              const int32_t* topk_idx, int32_t n_heads, const void* q, float softmax_scale,
                              void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return csa_sparse_attn_ex(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, nullptr, ws,
+                            ws_bytes, stream);
+}
+
+csa_status_t csa_sparse_attn_ex(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
+                                const int32_t* topk_idx, int32_t n_heads, const void* q, float softmax_scale,
+                                void* out, float* lse, const csa_attn_opts_t* opts, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
   csa_status_t s = check_cache(cache);
   if (s != CSA_OK) return s;
   if ((s = check_rows(rows, cache)) != CSA_OK) return s;
   if ((s = check_window(window, rows->max_rows_per_req)) != CSA_OK) return s;
   if (!attn_heads_supported(n_heads)) return CSA_ERR_UNSUPPORTED;
+  if ((s = check_attn_opts(opts, true)) != CSA_OK) return s;
   if (rows->num_rows == 0) return CSA_OK;
-  if (!topk_idx || !q || !out || !aligned(q, 16) || !aligned(out, 16)) return CSA_ERR_INVALID_ARGUMENT;
+  const bool planned = opts && opts->plan_in;
+  if ((!topk_idx && !planned) || !q || !out || !aligned(q, 16) || !aligned(out, 16)) return CSA_ERR_INVALID_ARGUMENT;
   if (!ws || ws_bytes < kStatusBytes || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
-  return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, ws, Order::kStream, stream);
+  return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, opts, ws, Order::kStream,
+                  stream);
 }
 
 csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                         int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
                         float softmax_scale, void* out, float* lse, int32_t* topk_out, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
-  const csa_status_t s = check_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, out, ws, ws_bytes);
-  if (s != CSA_OK || rows->num_rows == 0) return s;
-  return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, ws,
-                    Order::kStream, stream);
+  return csa_decode_ex(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out,
+                       nullptr, ws, ws_bytes, stream);
+}
+
+csa_status_t csa_decode_ex(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
+                           int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
+                           float softmax_scale, void* out, float* lse, int32_t* topk_out,
+                           const csa_attn_opts_t* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status_t s = check_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, out, ws, ws_bytes);
+  if (s != CSA_OK) return s;
+  if ((s = check_attn_opts(opts, false)) != CSA_OK) return s;
+  if (rows->num_rows == 0) return s;
+  return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, opts,
+                    ws, Order::kStream, stream);
 }
 
 csa_status_t csa_step(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
@@ -321,20 +361,32 @@ csa_status_t csa_step(const csa_cache_t* cache, const csa_window_t* window, cons
                       void* pending, const csa_compress_t* compress, const csa_rows_t* rows, int32_t n_idx_heads,
                       const void* q_idx, const float* w, int32_t n_heads, const void* q, float softmax_scale,
                       void* out, float* lse, int32_t* topk_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return csa_step_ex(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, compress, rows,
+                     n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, nullptr, ws, ws_bytes,
+                     stream);
+}
+
+csa_status_t csa_step_ex(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
+                         const int32_t* tok_off, int32_t total_tokens, const void* kv_in, const void* idx_in,
+                         void* pending, const csa_compress_t* compress, const csa_rows_t* rows,
+                         int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
+                         float softmax_scale, void* out, float* lse, int32_t* topk_out,
+                         const csa_attn_opts_t* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
   AppendArgs a;
   csa_status_t s =
       append_args(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, compress, ws, ws_bytes, &a);
   if (s != CSA_OK) return s;
   if ((s = check_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, out, ws, ws_bytes)) != CSA_OK)
     return s;
+  if ((s = check_attn_opts(opts, false)) != CSA_OK) return s;
   if ((s = from_cuda(launch_append(a, stream))) != CSA_OK) return s;
   if (rows->num_rows == 0) return CSA_OK;
   // With an append kernel in flight, the score prep is chained to it: it reads
   // only the step's inputs and the score workspace, which the append does not
   // touch, and it waits for the append before it exits.  Without one it is the
   // call's first kernel.
-  return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, ws,
-                    total_tokens > 0 ? Order::kChained : Order::kStream, stream);
+  return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, opts,
+                    ws, total_tokens > 0 ? Order::kChained : Order::kStream, stream);
 }
 
 csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out) {

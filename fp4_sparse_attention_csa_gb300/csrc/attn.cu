@@ -246,9 +246,27 @@ __device__ __forceinline__ void dequant_main(const RawMain& g, AttnSmem& sm, int
   }
 }
 
+// Rotate-half on the pair (a, b) = (dim 448 + j, dim 480 + j) of the last 64
+// dims: a' = a*c - b*s, b' = b*c + a*s, each product and the sum rounded once
+// (no fused multiply-add).  `mine` holds this thread's 16 values, `other` the
+// partner's (the other half of the pairs); lower: this thread holds the a's.
+__device__ __forceinline__ void rotate16(float (&mine)[16], const float (&other)[16], bool lower,
+                                         const float* cs, const float* sn) {
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const float c = __ldg(cs + t), s = __ldg(sn + t);
+    mine[t] = lower ? __fsub_rn(__fmul_rn(mine[t], c), __fmul_rn(other[t], s))
+                    : __fadd_rn(__fmul_rn(mine[t], c), __fmul_rn(other[t], s));
+  }
+}
+
 // Window token chunks: s = 2^e * mu, mu in [1, 2); codes * 2^e go to the
-// fp16 K rows (exact), mu scales the logit and p.
-__device__ __forceinline__ void dequant_win(const RawWin& g, AttnSmem& sm, int key, int q) {
+// fp16 K rows (exact), mu scales the logit and p.  With rotary tables the
+// token's last 64 dims are rotated with its position's row first (in fp32,
+// then rounded to fp16): lanes q and q ^ 2 of a key hold the two halves.
+// rcos / rsin must be null in all lanes of a warp or in none.
+__device__ __forceinline__ void dequant_win(const RawWin& g, AttnSmem& sm, int key, int q, const float* rcos,
+                                            const float* rsin) {
   uint8_t* krow_base = sm.k + (key >> 3) * 1024;
   float pow2 = 0.0f, mu = 0.0f;
   if (g.valid && g.ws > 0.0f) {
@@ -278,6 +296,28 @@ __device__ __forceinline__ void dequant_win(const RawWin& g, AttnSmem& sm, int k
           const __half2 v = __floats2half2_rn(x.x * pow2, x.y * pow2);
           o[wd * 2 + hh] = *reinterpret_cast<const uint32_t*>(&v);
         }
+      }
+    }
+    if (i == 7 && rcos != nullptr) {             // dims 448 + 16q .. +15: the rotated part
+      float mine[16], other[16];
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) {
+        uint32_t f[2];
+        e4m3x4_to_f16(w4[wd], f);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&f[hh]));
+          mine[4 * wd + 2 * hh] = x.x * pow2;      // exact: an E4M3 value times a power of two
+          mine[4 * wd + 2 * hh + 1] = x.y * pow2;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 16; ++t) other[t] = __shfl_xor_sync(0xFFFFFFFFu, mine[t], 16);
+      rotate16(mine, other, q < 2, rcos + 16 * (q & 1), rsin + 16 * (q & 1));
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const __half2 v = __floats2half2_rn(mine[2 * t], mine[2 * t + 1]);
+        o[t] = *reinterpret_cast<const uint32_t*>(&v);
       }
     }
     const int c16 = 4 * i + q;
@@ -350,7 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
 
   const int b = __ldg(a.row_req + r);
   const int pos = __ldg(a.row_pos + r);
-  const bool row_ok = (b >= 0 && b < a.num_requests && pos >= 0);
+  const bool rope = a.rope_cos != nullptr;
+  // with rotary tables a row needs a table row for its position
+  const bool row_ok = (b >= 0 && b < a.num_requests && pos >= 0) && (!rope || pos < a.rope_rows);
   if (!row_ok && tid == 0) raise_flag(a.status, CSA_FLAG_ROW_INVALID);
   const int n = row_ok ? (pos + 1) / a.P : 0;
   const int nsel = min(n, TOPK);
@@ -387,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   if (win_here) gather_win(a, b, pos, key, gq, wraw);
   const int j = tid;                              // TOPK == kThreads: one selected entry per thread
   const bool jin = j < nsel && j >= m_beg * kTileKeys && j < m_end * kTileKeys;
-  int e = jin ? __ldg(a.topk + (size_t)r * TOPK + j) : -1;
+  int e = jin ? __ldg((a.plan_in ? a.plan_in : a.topk) + (size_t)r * TOPK + j) : -1;
   constexpr int kQChunks = H * 64 / kThreads;     // 16-byte chunks of Q per thread
   uint4 qv[kQChunks];
   const uint16_t* qr = a.q + (size_t)r * H * D;
@@ -398,7 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   }
   {
     int pg = -1, slot = 0;
-    if (e >= 0) {
+    if (e >= 0 && a.plan_in) {                    // a resolved entry: page * 64 + slot
+      if ((e >> 6) >= a.num_pages) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
+      else { pg = e >> 6; slot = e & (PAGE - 1); }
+    } else if (e >= 0) {
       if (e >= n || e / PAGE >= a.max_pages) {
         raise_flag(a.status, CSA_FLAG_TOPK_OOB);
       } else {
@@ -407,6 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
         else { pg = p; slot = e % PAGE; }
       }
     }
+    // the plan: every slot of the row written once (its tile's CTA, or split
+    // 0 for the padding past the selection)
+    if (a.plan_out && (jin || (split == 0 && j >= nsel)))
+      a.plan_out[(size_t)r * TOPK + j] = pg >= 0 ? pg * PAGE + slot : -1;
     if (pg >= 0) {
       const uint8_t* src = a.kv_pool + (size_t)pg * KV_PAGE;
       prefetch_l2(src + slot * 256, 256);
@@ -415,15 +464,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     sm.ent_pg[j] = pg;
     sm.ent_slot[j] = (uint8_t)slot;
   }
-  // Q: bf16 -> fp16, K-major 128B swizzle
+  // Q: bf16 -> fp16, K-major 128B swizzle.  With rotary tables the last 64
+  // dims of every head are rotated with the row's table row first (fp32, then
+  // rounded to fp16): chunks 56..59 hold the a's, 60..63 the b's, lane ^ 4.
+  const float* qcos = (rope && row_ok) ? a.rope_cos + (size_t)pos * 32 : nullptr;
+  const float* qsin = (rope && row_ok) ? a.rope_sin + (size_t)pos * 32 : nullptr;
 #pragma unroll
   for (int i = 0; i < kQChunks; ++i) {
     const int c = tid + i * kThreads, h = c >> 6, ch = c & 63, kc = ch >> 3;
     const uint32_t w[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
     uint32_t o[4];
+    float f[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const __half2 hv = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+      f[2 * k] = __uint_as_float(w[k] << 16);
+      f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+    if (rope) {
+      float g[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) g[k] = __shfl_xor_sync(0xFFFFFFFFu, f[k], 4);
+      if (ch >= 56 && qcos != nullptr) {
+        const int j0 = (ch & 3) * 8;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float cc = __ldg(qcos + j0 + k), ss = __ldg(qsin + j0 + k);
+          f[k] = ch < 60 ? __fsub_rn(__fmul_rn(f[k], cc), __fmul_rn(g[k], ss))
+                         : __fadd_rn(__fmul_rn(f[k], cc), __fmul_rn(g[k], ss));
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 hv = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
       o[k] = *reinterpret_cast<const uint32_t*>(&hv);
     }
     *reinterpret_cast<uint4*>(sm.q + kc * (H * 128) + (h >> 3) * 1024 + swz128(h & 7, ch & 7)) =
@@ -587,7 +660,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   if (win_here) {
     if (m_beg < m_end) gather_main(a, sm, m_beg, key, gq, cur);
     // ---------------- the window tile ----------------
-    dequant_win(wraw, sm, key, gq);
+    {
+      // this thread's window token position; a key past the row's position is
+      // empty (zero) and uses the row's own table row.  Whether to rotate is
+      // the same for the whole CTA: the rotation exchanges values between lanes.
+      const int p = min(pos, max(0, pos - (WIN - 1)) + key);
+      const bool rot = rope && row_ok;
+      dequant_win(wraw, sm, key, gq, rot ? a.rope_cos + (size_t)p * 32 : nullptr,
+                  rot ? a.rope_sin + (size_t)p * 32 : nullptr);
+    }
     ok = compute(0, true);
     it = 1;
   }

@@ -121,6 +121,11 @@ struct AttnArgs {
   float* lse;               // [R, H] or null
   int32_t splits;
   uint32_t* status;
+  const int32_t* plan_in;   // [R, 512] resolved entries (page * 64 + slot, -1 none) read instead of topk
+  int32_t* plan_out;        // [R, 512] or null: the resolved entries written here
+  const float* rope_cos;    // [rope_rows, 32] or null: query and window tokens rotated
+  const float* rope_sin;
+  int32_t rope_rows;
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, Order order, cudaStream_t stream);
 int32_t attn_choose_splits(int32_t num_rows, int num_sms);

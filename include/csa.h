@@ -230,6 +230,52 @@ CSA_API csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* wi
                         void* out, float* lse, int32_t* topk_out,
                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Options of the attention step (csa_sparse_attn_ex, csa_decode_ex,
+ * csa_step_ex); NULL = none of them.
+ *  plan_out  [R, 512] int32 (nullable): the resolved cache entry of every
+ *            selected index, page * 64 + slot (-1: none), as the attention
+ *            step looked it up -- the plan that further layers reading the
+ *            same cache reuse ([SGL] "Small-operator fusion and GEMV": per-step
+ *            indices built once and shared across layers).
+ *  plan_in   [R, 512] int32 (nullable; csa_sparse_attn_ex only, then topk_idx
+ *            may be NULL): a plan written by an earlier call for the same rows
+ *            and cache, read instead of topk_idx: no page-table lookup.  Its
+ *            entries are trusted apart from the pool bound (page >= num_pages
+ *            raises CSA_FLAG_PAGE_OOB and the entry is skipped).
+ *  rope_cos, rope_sin  [rope_rows, 32] fp32 (both or neither): the query's last
+ *            64 dims are rotated with table row t (the row's position) and each
+ *            window token's with row p (its position), as key and as value,
+ *            by the rotate-half rule of csa_append_compress; global entries are
+ *            used as stored (rotated when appended) ([SGL] "DSpark adaptation
+ *            and optimization": Q RoPE merged into the attention-buffer write).
+ *            A row with t >= rope_rows raises CSA_FLAG_ROW_INVALID and gets a
+ *            zero output and lse -inf. */
+typedef struct {
+  const int32_t* plan_in;
+  int32_t*       plan_out;
+  const float*   rope_cos;
+  const float*   rope_sin;
+  int32_t        rope_rows;
+} csa_attn_opts_t;
+
+/* csa_sparse_attn with options; arguments and errors otherwise as
+ * csa_sparse_attn.  CSA_ERR_INVALID_ARGUMENT for a misaligned option pointer,
+ * one rotary table without the other, rope_rows < 1, or both plan_in and
+ * plan_out. */
+CSA_API csa_status_t csa_sparse_attn_ex(const csa_cache_t* cache, const csa_window_t* window,
+                                        const csa_rows_t* rows, const int32_t* topk_idx,
+                                        int32_t n_heads, const void* q, float softmax_scale,
+                                        void* out, float* lse, const csa_attn_opts_t* opts,
+                                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* csa_decode with options for its attention step (plan_in not allowed: the
+ * decode makes its own selection; plan_out receives that selection resolved). */
+CSA_API csa_status_t csa_decode_ex(const csa_cache_t* cache, const csa_window_t* window,
+                                   const csa_rows_t* rows, int32_t n_idx_heads, const void* q_idx,
+                                   const float* w, int32_t n_heads, const void* q, float softmax_scale,
+                                   void* out, float* lse, int32_t* topk_out, const csa_attn_opts_t* opts,
+                                   void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* csa_index_score_noalloc -- the same scores as csa_index_score, without a
  * workspace argument.  The pages have no counterpart to this entry point; it
  * exists for callers that cannot call cudaMalloc: a serving loop that reserves
@@ -310,6 +356,18 @@ CSA_API csa_status_t csa_step(const csa_cache_t* cache, const csa_window_t* wind
                       int32_t n_heads, const void* q, float softmax_scale,
                       void* out, float* lse, int32_t* topk_out,
                       void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* csa_step with options for its attention step (as csa_decode_ex).  With the
+ * compressor's rotary tables passed again in opts, the keys rotated at append,
+ * the query and the window tokens share one rotation. */
+CSA_API csa_status_t csa_step_ex(const csa_cache_t* cache, const csa_window_t* window,
+                                 const int32_t* pos0, const int32_t* tok_off, int32_t total_tokens,
+                                 const void* kv_in, const void* idx_in, void* pending,
+                                 const csa_compress_t* compress, const csa_rows_t* rows,
+                                 int32_t n_idx_heads, const void* q_idx, const float* w,
+                                 int32_t n_heads, const void* q, float softmax_scale,
+                                 void* out, float* lse, int32_t* topk_out, const csa_attn_opts_t* opts,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, returns the status word's flags in *flags_out (host)
  * and clears it.  Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_FAULT.

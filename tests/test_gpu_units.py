@@ -454,3 +454,183 @@ def test_append_compress_flags_positions_beyond_the_tables():
     ref = oracle.Cache(wl.num_pages, wl.page_table, wl.P, wl.win_cap)
     assert ref.append(np.zeros(1, np.int32), np.array([0, 200], np.int32), x, y, compress=cmp) == -3
     _pools_equal(st, ref)                                 # entries 0..49 written, the rest untouched
+
+
+# ------------------------------------------ decode plan (NEXT f-4) and rotary q (f-3)
+def _host_plan(wl, topk):
+    """Each selected index through the page table: page * 64 + slot, -1 kept."""
+    plan = np.full_like(topk, -1)
+    for r in range(wl.R):
+        b = int(wl.row_req[r])
+        for j, e in enumerate(topk[r]):
+            if e >= 0:
+                plan[r, j] = int(wl.page_table[b, e // 64]) * 64 + int(e) % 64
+    return plan
+
+
+def test_decode_plan_is_the_resolved_selection_and_later_layers_reuse_it():
+    """csa_decode_ex writes the plan (every selected index resolved through the
+    page table); a further layer's csa_sparse_attn_ex reading that plan instead
+    of the indices gives the same bits as reading the indices."""
+    ctx = [700, 2500, 5003, 9000, 130, 3]
+    wl = W.custom("plan2", 62, ctx, [1] * len(ctx), H=64, Hi=64, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    plan = torch.full((wl.R, 512), -7, dtype=torch.int32, device="cuda")
+    csa.csa_decode_ex(st.cache, st.window, s["rows"], wl.Hi, s["q_idx"], s["w"], wl.H, s["q"], wl.softmax_scale,
+                      s["out"], s["lse"], s["topk"], csa.make_attn_opts(plan_out=plan), s["ws"])
+    rc, flags = csa.csa_check_device_status(s["ws"])
+    assert rc == 0 and flags == 0, flags
+    topk = s["topk"].cpu().numpy()
+    assert np.array_equal(plan.cpu().numpy(), _host_plan(wl, topk))
+    ws_a = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    g = np.random.default_rng(8)
+    for layer in (1, 2):
+        q_l = torch.from_numpy(W.f32_to_bf16_bits(g.standard_normal((wl.R, wl.H, 512)).astype(np.float32))
+                               .view(np.int16)).cuda().view(torch.bfloat16)
+        o_i, l_i = torch.empty_like(s["out"]), torch.empty_like(s["lse"])
+        o_p, l_p = torch.empty_like(s["out"]), torch.empty_like(s["lse"])
+        csa.csa_sparse_attn(st.cache, st.window, s["rows"], s["topk"], wl.H, q_l, wl.softmax_scale, o_i, l_i, ws_a)
+        csa.csa_sparse_attn_ex(st.cache, st.window, s["rows"], None, wl.H, q_l, wl.softmax_scale, o_p, l_p,
+                               csa.make_attn_opts(plan_in=plan), ws_a)
+        rc, flags = csa.csa_check_device_status(ws_a)
+        assert rc == 0 and flags == 0, flags
+        assert torch.equal(o_i, o_p) and torch.equal(l_i, l_p)
+
+
+_E2M1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0.0, -.5, -1, -1.5, -2, -3, -4, -6], np.float64)
+
+
+def _rope_key_norm(ref, b, pos, sel):
+    """Largest norm of the last 64 dims over a row's keys (selected entries and
+    window tokens); rotations keep it."""
+    best = 0.0
+    for e in sel[sel >= 0]:
+        data, sc = ref.main_entry(b, int(e))
+        codes = np.stack([data & 15, data >> 4], axis=1).reshape(-1)
+        v = _E2M1[codes] * np.repeat([oracle.e4m3_decode(c) for c in sc], 16)
+        best = max(best, float(np.linalg.norm(v[448:])))
+    for p in range(max(0, pos - 127), pos + 1):
+        codes, s = ref.window_slot(b, p)
+        v = np.array([oracle.e4m3_decode(c) for c in codes[448:]]) * s
+        best = max(best, float(np.linalg.norm(v)))
+    return best
+
+
+def _check_rope_attention(wl, ref, topk, q, out, lse, o_ref, l_ref):
+    """J-3 on the outputs.  For lse: the rotated query and window tokens are
+    rounded once to fp16 for the tensor cores (unrotated, both are exact there),
+    so each logit may move by scale * 2 * 2^-11 * |q_rope| * |k_rope| on top of
+    the fp32 rounding the 1e-4 rule covers (Cauchy-Schwarz over the 64 rotated
+    dims); the lse moves by at most the largest such change."""
+    norm, l2 = parity.check_attention(out, o_ref)
+    u = 2.0 ** -11
+    for r in range(wl.R):
+        qn = np.linalg.norm(W.bf16_bits_to_f32(q[r]).astype(np.float64)[:, 448:], axis=1)
+        kn = _rope_key_norm(ref, int(wl.row_req[r]), int(wl.row_pos[r]), topk[r])
+        tol = parity.LSE_TOL + wl.softmax_scale * 2 * u * qn * kn
+        assert (np.abs(lse[r].astype(np.float64) - l_ref[r]) <= tol).all(), r
+    return norm, l2
+
+
+def _rope_tables(seed, rows):
+    c = W.compress_inputs(seed, rows)
+    return torch.from_numpy(c["rope_cos"]).cuda(), torch.from_numpy(c["rope_sin"]).cuda(), c
+
+
+@pytest.mark.parametrize("H,ctx,rows", [(64, [1, 60, 700, 2100, 5000], 1), (16, [400, 3000], 6)])
+def test_rotary_attention_matches_oracle(H, ctx, rows):
+    """The query and the window tokens rotated inside the attention step, the
+    global entries as stored, against the oracle's rotary attention (J-3)."""
+    wl = W.custom("rope", 63 + H, ctx, [min(rows, c) for c in ctx], H=H, Hi=16, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    ref = oracle.build_cache(wl)
+    q_idx, w, q = wl.step_queries()
+    _, _, topk, _ = oracle.decode(ref, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale)
+    cs, sn, c = _rope_tables(63, int(wl.ctx_len.max()))
+    out = torch.empty((wl.R, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((wl.R, H), device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    csa.csa_sparse_attn_ex(st.cache, st.window, s["rows"], torch.from_numpy(topk).cuda(), H, s["q"],
+                           wl.softmax_scale, out, lse, csa.make_attn_opts(rope_cos=cs, rope_sin=sn), ws)
+    rc, flags = csa.csa_check_device_status(ws)
+    assert rc == 0 and flags == 0, flags
+    o_ref = np.zeros((wl.R, H, 512), np.float32)
+    l_ref = np.zeros((wl.R, H), np.float32)
+    for r in range(wl.R):
+        o_ref[r], l_ref[r], rc_o = oracle.attention_row_rope(ref, wl.row_req[r], wl.row_pos[r], topk[r], q[r],
+                                                             wl.softmax_scale, c["rope_cos"], c["rope_sin"])
+        assert rc_o == 0
+    norm, l2 = _check_rope_attention(wl, ref, topk, q, out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref)
+    print(f"rotary attention H={H}: max normalised err {norm:.2e}, rel L2 {l2:.2e}")
+    # a row past the tables is flagged and left empty
+    short_c, short_s = cs[: int(wl.row_pos.max())].contiguous(), sn[: int(wl.row_pos.max())].contiguous()
+    csa.csa_sparse_attn_ex(st.cache, st.window, s["rows"], torch.from_numpy(topk).cuda(), H, s["q"],
+                           wl.softmax_scale, out, lse, csa.make_attn_opts(rope_cos=short_c, rope_sin=short_s), ws)
+    rc, flags = csa.csa_check_device_status(ws)
+    assert rc == 5 and (flags & csa.FLAG_ROW_INVALID)
+    last = int(np.argmax(wl.row_pos))
+    assert not out[last].float().any() and torch.isneginf(lse[last]).all()
+
+
+def test_step_ex_rotates_keys_query_and_window_with_one_table():
+    """csa_step_ex with the compressor's rotary tables in both places equals
+    csa_append_compress + csa_decode_ex bit for bit, and matches the oracle
+    (compressed cache, rotary attention on the GPU's selection)."""
+    ctx = [3000, 4100, 777, 5003]
+    wl = W.custom("steprope", 64, ctx, [6, 6, 6, 6], H=64, Hi=64, shuffle=True)
+    cs, sn, c = _rope_tables(64, int(wl.ctx_len.max()))
+    dev = {k: (torch.from_numpy(v).cuda() if isinstance(v, np.ndarray) else v) for k, v in c.items()}
+    comp = csa.make_compress(dev["kv_gamma"], dev["idx_gamma"], dev["eps"], dev["rope_cos"], dev["rope_sin"])
+    opts = csa.make_attn_opts(rope_cos=cs, rope_sin=sn)
+    states = []
+    for fused in (False, True):
+        st = DeviceState(wl)
+        st.set_compress(c)
+        # history through the compressed append too
+        pos0 = np.zeros(wl.B, np.int32)
+        cnt = wl.hist_len.astype(np.int64)
+        xs, ys = zip(*[wl.tokens(b, 0, int(wl.hist_len[b])) for b in range(wl.B)])
+        csa.csa_append_compress(st.cache, st.window, torch.from_numpy(pos0).cuda(),
+                                torch.from_numpy(np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)).cuda(),
+                                int(cnt.sum()), torch.from_numpy(np.concatenate(xs).view(np.int16)).cuda(),
+                                torch.from_numpy(np.concatenate(ys).view(np.int16)).cuda(), st.pending, comp,
+                                st.ws_append)
+        s = st.step_inputs()
+        if fused:
+            csa.csa_step_ex(st.cache, st.window, s["pos0"], s["tok_off"], wl.R, s["kv_new"], s["idx_new"],
+                            st.pending, comp, s["rows"], wl.Hi, s["q_idx"], s["w"], wl.H, s["q"], wl.softmax_scale,
+                            s["out"], s["lse"], s["topk"], opts, s["ws"])
+        else:
+            csa.csa_append_compress(st.cache, st.window, s["pos0"], s["tok_off"], wl.R, s["kv_new"], s["idx_new"],
+                                    st.pending, comp, st.ws_append)
+            csa.csa_decode_ex(st.cache, st.window, s["rows"], wl.Hi, s["q_idx"], s["w"], wl.H, s["q"],
+                              wl.softmax_scale, s["out"], s["lse"], s["topk"], opts, s["ws"])
+        rc, flags = csa.csa_check_device_status(s["ws"])
+        assert rc == 0 and flags == 0, (fused, flags)
+        states.append((st, s))
+    (a, sa), (b, sb) = states
+    for key in ("topk", "out", "lse"):
+        assert torch.equal(sa[key], sb[key]), key
+    assert torch.equal(a.kv_pool, b.kv_pool) and torch.equal(a.idx_pool, b.idx_pool)
+    ref = oracle.Cache(wl.num_pages, wl.page_table, wl.P, wl.win_cap)
+    xs, ys = zip(*[wl.tokens(bq, 0, int(wl.ctx_len[bq])) for bq in range(wl.B)])
+    tok = np.concatenate([[0], np.cumsum(wl.ctx_len)]).astype(np.int32)
+    assert ref.append(np.zeros(wl.B, np.int32), tok, np.concatenate(xs), np.concatenate(ys), compress=c) == 0
+    assert np.array_equal(b.kv_pool.cpu().numpy(), ref.kv_pool)
+    q_idx, w, q = wl.step_queries()
+    _, _, _, scores = oracle.decode(ref, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale)
+    gt = sb["topk"].cpu().numpy()
+    n = wl.row_entries()
+    o_ref = np.zeros((wl.R, wl.H, 512), np.float32)
+    l_ref = np.zeros((wl.R, wl.H), np.float32)
+    for r in range(wl.R):
+        parity.check_topk_row(gt[r], scores[r], int(n[r]))
+        o_ref[r], l_ref[r], _ = oracle.attention_row_rope(ref, wl.row_req[r], wl.row_pos[r], gt[r], q[r],
+                                                          wl.softmax_scale, c["rope_cos"], c["rope_sin"])
+    _check_rope_attention(wl, ref, gt, q, sb["out"].float().cpu().numpy(), sb["lse"].cpu().numpy(), o_ref, l_ref)
