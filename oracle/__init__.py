@@ -69,6 +69,8 @@ def lib():
             L.or_topk_row.restype = None
             L.or_attention_row.argtypes = [vp, i32, i32, vp, i32, vp, f32, vp, vp]
             L.or_attention_row.restype = None
+            L.or_topk_two_level.argtypes = [vp, i32, i32, vp]
+            L.or_topk_two_level.restype = None
             L.or_attention_row_rope.argtypes = [vp, i32, i32, vp, i32, vp, f32, vp, vp, i32, vp, vp]
             L.or_attention_row_rope.restype = C.c_int
             L.or_decode.argtypes = [vp, i32, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, i64, i32]
@@ -235,6 +237,15 @@ def topk_row(scores, n):
     sc = _c(scores[:n], np.float32)
     out = np.zeros(TOPK, np.int32)
     lib().or_topk_row(_p(sc), int(n), _p(out))
+    return out
+
+
+def topk_two_level(scores, n, blocks):
+    """Two-level candidate filter: top `blocks` pages of 64 by their largest
+    score, then the exact top-512 among their entries."""
+    sc = _c(scores[:n], np.float32)
+    out = np.zeros(TOPK, np.int32)
+    lib().or_topk_two_level(_p(sc), int(n), int(blocks), _p(out))
     return out
 
 

@@ -442,6 +442,47 @@ void or_topk_row(const float* scores, int32_t n, int32_t* out512) {
 }
 
 /* ======================================================================
+ * Two-level candidate filter (NEXT f-2; [SGL] "Architecture changes and KV
+ * cache compression": CSA2 narrows the indexer's search before the top 512;
+ * "DSpark adaptation and optimization": chosen candidate blocks expand
+ * straight into a token mask).  The pages give no block size or block score;
+ * the reading used here:
+ *   1. a block is a page of 64 entries, block b = entries 64b .. 64b+63 (< n);
+ *   2. its score is the largest score among its entries;
+ *   3. the blocks are ordered by (block score descending, block index
+ *      ascending) and the first `blocks` of them are kept;
+ *   4. the candidates are the entries of the kept blocks; among them the 512
+ *      largest by (score descending, index ascending) are returned in
+ *      ascending index order, padded with -1.
+ * ====================================================================== */
+void or_topk_two_level(const float* scores, int32_t n, int32_t blocks, int32_t* out512) {
+  const int32_t nb = (n + OR_PAGE - 1) / OR_PAGE;
+  or_pair_t* bs = (or_pair_t*)malloc(sizeof(or_pair_t) * (size_t)(nb > 0 ? nb : 1));
+  for (int32_t b = 0; b < nb; ++b) {
+    float m = scores[(int64_t)b * OR_PAGE];
+    for (int32_t i = b * OR_PAGE + 1; i < n && i < (b + 1) * OR_PAGE; ++i)
+      if (scores[i] > m) m = scores[i];
+    bs[b].s = m;
+    bs[b].i = b;
+  }
+  qsort(bs, (size_t)nb, sizeof(or_pair_t), cmp_pair);
+  const int32_t kept = blocks < nb ? (blocks > 0 ? blocks : 0) : nb;
+  /* a mask of the kept blocks, then the candidates in ascending index order */
+  uint8_t* keep = (uint8_t*)calloc((size_t)(nb > 0 ? nb : 1), 1);
+  for (int32_t j = 0; j < kept; ++j) keep[bs[j].i] = 1;
+  float* cand = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+  int32_t* cidx = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+  int32_t m = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (keep[i / OR_PAGE]) { cand[m] = scores[i]; cidx[m] = i; ++m; }
+  }
+  int32_t sel[OR_TOPK];
+  or_topk_row(cand, m, sel);                      /* positions within the candidate list */
+  for (int32_t j = 0; j < OR_TOPK; ++j) out512[j] = sel[j] >= 0 ? cidx[sel[j]] : -1;
+  free(bs); free(keep); free(cand); free(cidx);
+}
+
+/* ======================================================================
  * Sparse MQA attention over the selected entries and the FP8 window.
  * Keys = values = the dequantised 512-d latent (shared by all heads):
  *   global entry: e2m1 * E4M3 block scale;  window token: E4M3 * fp32 scale.

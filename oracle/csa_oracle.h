@@ -115,6 +115,11 @@ void or_index_score(const or_cache_t* c, int32_t num_rows, const int32_t* row_re
 /* Exact top-512 of scores[0..n): ascending index order, padded with -1. */
 void or_topk_row(const float* scores, int32_t n, int32_t* out512);
 
+/* Two-level candidate filter: blocks of 64 entries scored by their largest
+ * score, the first `blocks` by (block score desc, block index asc) kept, then
+ * the exact top-512 among their entries (ascending, -1 padded). */
+void or_topk_two_level(const float* scores, int32_t n, int32_t blocks, int32_t* out512);
+
 /* Sparse MQA attention for one row: keys = the selected global entries
  * (ascending) followed by the window positions max(0,t-127)..t. */
 void or_attention_row(const or_cache_t* c, int32_t req, int32_t pos,

@@ -570,3 +570,48 @@ def test_rope_row_beyond_the_tables_is_rejected():
     cs, sn = _tables(699, [])                              # rows 0..698 only
     o, l, rc = oracle.attention_row_rope(cache, 0, 699, topk[0], q[0], wl.softmax_scale, cs, sn)
     assert rc == -1 and not o.any() and np.isneginf(l).all()
+
+
+# ---- P-13: two-level candidate filter (NEXT f-2) ---------------------------------
+@pytest.mark.parametrize("n", [1, 63, 64, 65, 700, 5000, 40000])
+def test_two_level_keeping_every_block_is_the_flat_selection(n):
+    g = np.random.default_rng(n)
+    sc = (g.integers(0, 300, n) / 7).astype(np.float32)    # many ties
+    nb = (n + 63) // 64
+    assert np.array_equal(oracle.topk_two_level(sc, n, nb), oracle.topk_row(sc, n))
+    assert np.array_equal(oracle.topk_two_level(sc, n, nb + 9), oracle.topk_row(sc, n))
+
+
+@pytest.mark.parametrize("seed,ties", [(1, False), (2, True), (3, True)])
+def test_two_level_with_512_blocks_is_the_flat_selection(seed, ties):
+    """Every entry of the flat top 512 lies in a block whose largest score is at
+    least the 512th score, and (ties broken toward lower indices at both levels)
+    those blocks are among the first 512 blocks: 512 kept blocks lose nothing."""
+    g = np.random.default_rng(seed)
+    n = 64 * 1500 + 17
+    sc = g.standard_normal(n).astype(np.float32)
+    if ties:
+        sc = np.round(sc * 4) / 4                         # heavy ties, also at rank 512
+        sc[::97] = sc.max()
+    assert np.array_equal(oracle.topk_two_level(sc, n, 512), oracle.topk_row(sc, n))
+
+
+def test_two_level_keeps_only_the_chosen_blocks():
+    sc = np.zeros(128, np.float32)
+    sc[5] = 9.0                                           # block 0: one high entry
+    sc[64:] = 5.0                                         # block 1: all medium
+    out = oracle.topk_two_level(sc, 128, 1)
+    assert list(out[:64]) == list(range(64)) and (out[64:] == -1).all()
+    out = oracle.topk_two_level(sc, 128, 2)
+    assert list(out[:128]) == list(range(128))
+
+
+def test_two_level_equal_block_scores_go_to_the_lower_block():
+    sc = np.full(64 * 3, -1.0, np.float32)
+    sc[70] = 2.0                                          # block 1
+    sc[130] = 2.0                                         # block 2, same block score
+    sc[10] = 1.0                                          # block 0, lower score
+    out = oracle.topk_two_level(sc, 64 * 3, 1)
+    assert list(out[:64]) == list(range(64, 128))
+    out = oracle.topk_two_level(sc, 64 * 3, 2)
+    assert list(out[:128]) == list(range(64, 192))
