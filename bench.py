@@ -269,6 +269,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the speculative-verify step timed beside the serving batch")
+    ap.add_argument("--candidate-blocks", type=int, default=0,
+                    help="select through the two-level candidate filter with this many 64-entry blocks "
+                         "(a variant; 0 = the exact top-512 over every entry)")
     ap.add_argument("--compress", action="store_true",
                     help="append through csa_append_compress (RMSNorm + RoPE before quantisation)")
     args = ap.parse_args()
@@ -310,8 +313,10 @@ def main():
         flush.zero_()
         torch.sum(flush, dim=0, keepdim=True, out=flush_sink)
 
+    opts = csa.make_opts(candidate_blocks=args.candidate_blocks) if args.candidate_blocks > 0 else None
+
     def step():
-        st.step(s)
+        st.step(s, opts=opts)
 
     for _ in range(max(args.warmup, 3)):
         flush_l2()
@@ -359,6 +364,18 @@ def main():
 
     topk = s["topk"].cpu().numpy()
     ab = algorithmic_bytes(wl, topk)
+    selection = "exact top-512 over every visible entry"
+    if opts is not None:
+        # recall of the filtered selection against the flat one on the same step
+        s_flat = dict(s)
+        s_flat["topk"] = s["topk"].clone()
+        s_flat["out"], s_flat["lse"] = s["out"].clone(), s["lse"].clone()
+        st.step(s_flat)
+        flat = s_flat["topk"].cpu().numpy()
+        rec = [len(set(flat[r][flat[r] >= 0]) & set(topk[r][topk[r] >= 0])) / max(1, int((flat[r] >= 0).sum()))
+               for r in range(wl.R)]
+        selection = {"kind": f"two-level candidate filter, {args.candidate_blocks} blocks of 64 entries",
+                     "recall_of_flat_top512_mean": float(np.mean(rec)), "recall_min": float(np.min(rec))}
     traffic = None
     if cfg == 4 and score_fingerprint() == SCORE_TRAFFIC["fingerprint"]:
         traffic = SCORE_TRAFFIC["bytes"]
@@ -437,7 +454,7 @@ def main():
 
     # ---- the other workload the bandwidth target names: speculative verify
     secondary = None
-    if cfg == 4 and not args.no_secondary and not args.compress:
+    if cfg == 4 and not args.no_secondary and not args.compress and opts is None:
         secondary = time_workload(3, max(10, min(args.steps, 50)), args.warmup, flush_l2)
 
     launches_per_step = 5          # append, score prep, index score, top-k, attention (splits merge in-cluster)
@@ -460,7 +477,7 @@ def main():
                    "path_frac_of_hbm": path_gbs / peak, "path_frac_of_8tbs": path_gbs / 8000.0,
                    "bytes": ab, "parallelism": f"replicas x{world}",
                    "append": "csa_append_compress (RMSNorm + RoPE)" if args.compress else "csa_append",
-                   "call": "csa_step (append + decode in one call)",
+                   "call": "csa_step (append + decode in one call)", "selection": selection,
                    "secondary": secondary},
         "roofline": {"bound": "hbm", "kernel": "index score (k_score_prep + k_index_score)",
                      "achieved": score_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",

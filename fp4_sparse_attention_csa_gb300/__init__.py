@@ -48,9 +48,9 @@ class CsaCompress(C.Structure):
                 ("rope_cos", C.c_void_p), ("rope_sin", C.c_void_p), ("rope_rows", C.c_int32)]
 
 
-class CsaAttnOpts(C.Structure):
+class CsaOpts(C.Structure):
     _fields_ = [("plan_in", C.c_void_p), ("plan_out", C.c_void_p), ("rope_cos", C.c_void_p),
-                ("rope_sin", C.c_void_p), ("rope_rows", C.c_int32)]
+                ("rope_sin", C.c_void_p), ("rope_rows", C.c_int32), ("candidate_blocks", C.c_int32)]
 
 
 class CsaRows(C.Structure):
@@ -84,6 +84,7 @@ def lib():
                                    vp, vp, sz, vp]
             L.csa_step_ex.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp,
                                       vp, vp, vp, sz, vp]
+            L.csa_topk_two_level.argtypes = [i32, vp, i32, vp, i32, i32, vp, vp, sz, vp]
             L.csa_sparse_attn_ex.argtypes = [vp, vp, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
             L.csa_decode_ex.argtypes = [vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, vp, sz, vp]
             L.csa_check_device_status.argtypes = [vp, vp, C.POINTER(C.c_uint32)]
@@ -92,7 +93,8 @@ def lib():
             L.csa_status_string.restype = C.c_char_p
             for fn in ("csa_append", "csa_append_compress", "csa_index_score", "csa_topk", "csa_sparse_attn",
                        "csa_decode", "csa_step", "csa_index_score_noalloc", "csa_check_device_status",
-                       "csa_set_wait_budget", "csa_sparse_attn_ex", "csa_decode_ex", "csa_step_ex"):
+                       "csa_set_wait_budget", "csa_sparse_attn_ex", "csa_decode_ex", "csa_step_ex",
+                       "csa_topk_two_level"):
                 getattr(L, fn).restype = C.c_int
             _lib = L
     return _lib
@@ -182,6 +184,12 @@ def csa_topk(num_rows, scores, ld, n_valid, max_n, k, out_idx, ws=None, stream=N
     _check(rc, "csa_topk")
 
 
+def csa_topk_two_level(num_rows, scores, ld, n_valid, max_n, blocks, out_idx, ws=None, stream=None):
+    rc = lib().csa_topk_two_level(int(num_rows), _ptr(scores), int(ld), _ptr(n_valid), int(max_n), int(blocks),
+                                  _ptr(out_idx), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "csa_topk_two_level")
+
+
 def csa_sparse_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, ws, stream=None):
     rc = lib().csa_sparse_attn(C.byref(cache), C.byref(window) if window is not None else None,
                                C.byref(rows), _ptr(topk_idx), int(n_heads), _ptr(q), float(softmax_scale),
@@ -189,10 +197,11 @@ def csa_sparse_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, ou
     _check(rc, "csa_sparse_attn")
 
 
-def make_attn_opts(plan_in=None, plan_out=None, rope_cos=None, rope_sin=None):
-    """Options of the attention step: plans [R, 512] int32, rotary tables [rows, 32] fp32."""
+def make_opts(plan_in=None, plan_out=None, rope_cos=None, rope_sin=None, candidate_blocks=0):
+    """Options of the selection and attention steps: plans [R, 512] int32,
+    rotary tables [rows, 32] fp32, two-level candidate blocks (0: flat)."""
     rows = 0 if rope_cos is None else int(rope_cos.shape[0])
-    return CsaAttnOpts(_ptr(plan_in), _ptr(plan_out), _ptr(rope_cos), _ptr(rope_sin), rows)
+    return CsaOpts(_ptr(plan_in), _ptr(plan_out), _ptr(rope_cos), _ptr(rope_sin), rows, int(candidate_blocks))
 
 
 def _opt(o):

@@ -69,7 +69,7 @@ DecodeLayout decode_layout(int32_t R, int32_t max_entries) {
 
 // Attention options: pointers aligned, a plan read only where no selection is
 // computed, rotary tables with at least one row.
-csa_status_t check_attn_opts(const csa_attn_opts_t* o, bool plan_in_allowed) {
+csa_status_t check_attn_opts(const csa_opts_t* o, bool plan_in_allowed) {
   if (!o) return CSA_OK;
   if (o->plan_in && (!plan_in_allowed || !aligned(o->plan_in, 4))) return CSA_ERR_INVALID_ARGUMENT;
   if (o->plan_out && !aligned(o->plan_out, 4)) return CSA_ERR_INVALID_ARGUMENT;
@@ -77,6 +77,7 @@ csa_status_t check_attn_opts(const csa_attn_opts_t* o, bool plan_in_allowed) {
   if ((o->rope_cos == nullptr) != (o->rope_sin == nullptr)) return CSA_ERR_INVALID_ARGUMENT;
   if (o->rope_cos && (o->rope_rows < 1 || !aligned(o->rope_cos, 4) || !aligned(o->rope_sin, 4)))
     return CSA_ERR_INVALID_ARGUMENT;
+  if (o->candidate_blocks < 0 || o->candidate_blocks > kTwoLevelMaxBlocks) return CSA_ERR_UNSUPPORTED;
   return CSA_OK;
 }
 
@@ -112,7 +113,7 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
 
 csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                       const int32_t* topk, int32_t H, const void* q, float softmax_scale, void* out, float* lse,
-                      const csa_attn_opts_t* opts, void* ws, Order order, cudaStream_t stream) {
+                      const csa_opts_t* opts, void* ws, Order order, cudaStream_t stream) {
   AttnArgs a;
   a.plan_in = opts ? opts->plan_in : nullptr;
   a.plan_out = opts ? opts->plan_out : nullptr;
@@ -213,7 +214,7 @@ csa_status_t check_decode(const csa_cache_t* cache, const csa_window_t* window, 
 csa_status_t run_decode(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                         int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
                         float softmax_scale, void* out, float* lse, int32_t* topk_out,
-                        const csa_attn_opts_t* opts, void* ws, Order first, cudaStream_t stream) {
+                        const csa_opts_t* opts, void* ws, Order first, cudaStream_t stream) {
   const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries);
   uint8_t* base = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(base + L.scores);
@@ -231,7 +232,10 @@ csa_status_t run_decode(const csa_cache_t* cache, const csa_window_t* window, co
   t.max_n = rows->max_entries;
   t.out = topk;
   t.status = static_cast<uint32_t*>(ws);
-  if ((s = from_cuda(launch_topk(t, Order::kChained, stream))) != CSA_OK) return s;
+  const int32_t blocks = opts ? opts->candidate_blocks : 0;
+  if ((s = from_cuda(blocks > 0 ? launch_topk_two_level(t, blocks, Order::kChained, stream)
+                                : launch_topk(t, Order::kChained, stream))) != CSA_OK)
+    return s;
   return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, opts, ws, Order::kChained, stream);
 }
 
@@ -311,6 +315,27 @@ csa_status_t csa_topk(int32_t num_rows, const float* scores, int32_t ld, const i
   return from_cuda(launch_topk(a, Order::kStream, stream));
 }
 
+csa_status_t csa_topk_two_level(int32_t num_rows, const float* scores, int32_t ld, const int32_t* n_valid,
+                                int32_t max_n, int32_t blocks, int32_t* out_idx, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
+  if (blocks < 1 || blocks > kTwoLevelMaxBlocks || max_n > kTwoLevelMaxEntries) return CSA_ERR_UNSUPPORTED;
+  if (num_rows < 0 || max_n < 0 || ld < max_n || ld < 1) return CSA_ERR_INVALID_ARGUMENT;
+  if (num_rows == 0) return CSA_OK;
+  if (!scores || !n_valid || !out_idx || !aligned(scores, 16) || (ld % 4) != 0) return CSA_ERR_INVALID_ARGUMENT;
+  if (ws && ws_bytes < kStatusBytes) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  TopkArgs a;
+  a.scores = scores;
+  a.ld = ld;
+  a.num_rows = num_rows;
+  a.n_valid = n_valid;
+  a.row_pos = nullptr;
+  a.P = 1;
+  a.max_n = max_n;
+  a.out = out_idx;
+  a.status = static_cast<uint32_t*>(ws);
+  return from_cuda(launch_topk_two_level(a, blocks, Order::kStream, stream));
+}
+
 csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                              const int32_t* topk_idx, int32_t n_heads, const void* q, float softmax_scale,
                              void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -320,7 +345,7 @@ csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* windo
 
 csa_status_t csa_sparse_attn_ex(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                                 const int32_t* topk_idx, int32_t n_heads, const void* q, float softmax_scale,
-                                void* out, float* lse, const csa_attn_opts_t* opts, void* ws, size_t ws_bytes,
+                                void* out, float* lse, const csa_opts_t* opts, void* ws, size_t ws_bytes,
                                 cudaStream_t stream) {
   csa_status_t s = check_cache(cache);
   if (s != CSA_OK) return s;
@@ -347,10 +372,11 @@ csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* window, co
 csa_status_t csa_decode_ex(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                            int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
                            float softmax_scale, void* out, float* lse, int32_t* topk_out,
-                           const csa_attn_opts_t* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                           const csa_opts_t* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
   csa_status_t s = check_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, out, ws, ws_bytes);
   if (s != CSA_OK) return s;
   if ((s = check_attn_opts(opts, false)) != CSA_OK) return s;
+  if (opts && opts->candidate_blocks > 0 && rows->max_entries > kTwoLevelMaxEntries) return CSA_ERR_UNSUPPORTED;
   if (rows->num_rows == 0) return s;
   return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, opts,
                     ws, Order::kStream, stream);
@@ -371,7 +397,7 @@ csa_status_t csa_step_ex(const csa_cache_t* cache, const csa_window_t* window, c
                          void* pending, const csa_compress_t* compress, const csa_rows_t* rows,
                          int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
                          float softmax_scale, void* out, float* lse, int32_t* topk_out,
-                         const csa_attn_opts_t* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                         const csa_opts_t* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
   AppendArgs a;
   csa_status_t s =
       append_args(cache, window, pos0, tok_off, total_tokens, kv_in, idx_in, pending, compress, ws, ws_bytes, &a);
@@ -379,6 +405,7 @@ csa_status_t csa_step_ex(const csa_cache_t* cache, const csa_window_t* window, c
   if ((s = check_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, out, ws, ws_bytes)) != CSA_OK)
     return s;
   if ((s = check_attn_opts(opts, false)) != CSA_OK) return s;
+  if (opts && opts->candidate_blocks > 0 && rows->max_entries > kTwoLevelMaxEntries) return CSA_ERR_UNSUPPORTED;
   if ((s = from_cuda(launch_append(a, stream))) != CSA_OK) return s;
   if (rows->num_rows == 0) return CSA_OK;
   // With an append kernel in flight, the score prep is chained to it: it reads

@@ -103,6 +103,10 @@ struct TopkArgs {
   uint32_t* status;
 };
 cudaError_t launch_topk(const TopkArgs& a, Order order, cudaStream_t stream);
+// Two-level candidate filter: blocks in [1, 128], rows up to 262144 entries.
+cudaError_t launch_topk_two_level(const TopkArgs& a, int32_t blocks, Order order, cudaStream_t stream);
+constexpr int32_t kTwoLevelMaxBlocks = 128;
+constexpr int32_t kTwoLevelMaxEntries = 262144;
 
 struct AttnArgs {
   const uint8_t* kv_pool;

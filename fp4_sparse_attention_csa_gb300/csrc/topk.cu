@@ -771,7 +771,195 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Two-level candidate filter (CSA2 reading): blocks of 64 entries scored by
+// their largest score, the first `blocks` of them by (block score desc, block
+// index asc) kept, then the exact top-512 among the kept blocks' entries.  One
+// CTA per row: block maxima from the L2-resident scores, an exact radix select
+// of the B-th block key (ties to the lower block), the kept blocks' entries
+// compacted in ascending order (only the row's last block can be ragged, so
+// the candidate list is contiguous), an exact radix select of the 512th
+// candidate, output in ascending order.
+constexpr int kTwoMaxBlocks = 4096;        // rows up to 262144 entries
+constexpr int kTwoMaxKept = 128;           // blocks kept: at most 8192 candidates
+constexpr int kTwoCand = kTwoMaxKept * 64;
+
+struct alignas(16) TwoSmem {
+  uint32_t bkey[kTwoMaxBlocks];            // block maxima as order-preserving keys
+  uint32_t cand_key[kTwoCand];
+  int32_t kept[kTwoMaxKept];               // kept blocks, ascending
+  uint32_t hist[2048];
+  uint32_t warp_a[kWarps];
+  uint32_t sel_bin, sel_need;
+};
+
+// Radix select of the need-th largest of `m` keys given by key_at (a block-wide
+// three-pass 11/11/10-bit select): the key T and how many of those equal to T
+// are taken (need - keys strictly above T).
+template <typename F>
+__device__ void two_radix(F key_at, int m, uint32_t need, TwoSmem& sm, uint32_t* T_out, uint32_t* take_out) {
+  const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
+  uint32_t prefix = 0, mask = 0, rem = need;
+  const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+  for (int p = 0; p < 3; ++p) {
+    const int sh = shifts[p], nbv = 1 << widths[p];
+    for (int i = tid; i < 2048; i += kThreads) sm.hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < m; i += kThreads) {
+      const uint32_t k = key_at(i);
+      if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> sh) & (uint32_t)(nbv - 1)], 1u);
+    }
+    __syncthreads();
+    constexpr int per = 2048 / kThreads;
+    uint32_t c[per], mine = 0;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      const int b = per * tid + j;
+      c[j] = b < nbv ? sm.hist[b] : 0u;
+      mine += c[j];
+    }
+    uint32_t incl = mine;                       // suffix sums over higher threads
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    if (lane == 0) sm.warp_a[warp] = incl;
+    __syncthreads();
+    uint32_t acc = incl - mine;
+    for (int w2 = warp + 1; w2 < kWarps; ++w2) acc += sm.warp_a[w2];
+#pragma unroll
+    for (int j = per - 1; j >= 0; --j) {
+      if (acc < rem && acc + c[j] >= rem) {
+        sm.sel_bin = (uint32_t)(per * tid + j);
+        sm.sel_need = rem - acc;
+      }
+      acc += c[j];
+    }
+    __syncthreads();
+    prefix |= sm.sel_bin << sh;
+    mask |= (uint32_t)(nbv - 1) << sh;
+    rem = sm.sel_need;
+    __syncthreads();
+  }
+  *T_out = prefix;
+  *take_out = rem;
+}
+
+// Block-wide exclusive scan of one count per thread (512 threads).
+__device__ __forceinline__ uint32_t two_scan(uint32_t v, uint32_t* total, TwoSmem& sm) {
+  const int lane = lane_id(), warp = warp_id();
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm.warp_a[warp] = x;
+  __syncthreads();
+  uint32_t off = 0, tot = 0;
+  for (int w2 = 0; w2 < kWarps; ++w2) {
+    const uint32_t c = sm.warp_a[w2];
+    if (w2 < warp) off += c;
+    tot += c;
+  }
+  __syncthreads();
+  *total = tot;
+  return off + x - v;
+}
+
+__global__ void __launch_bounds__(kThreads) k_topk_two_level(TopkArgs a, int32_t blocks) {
+  pdl_trigger();
+  pdl_wait();                    // the scores come from the previous kernel
+  extern __shared__ __align__(16) uint8_t smem[];
+  TwoSmem& sm = *reinterpret_cast<TwoSmem*>(smem);
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const float* row = a.scores + (size_t)r * a.ld;
+  int32_t* out = a.out + (size_t)r * TOPK;
+  int n = a.n_valid ? __ldg(a.n_valid + r) : (__ldg(a.row_pos + r) + 1) / a.P;
+  if (n < 0 || n > a.max_n) {
+    if (tid == 0) raise_flag(a.status, CSA_FLAG_ROW_INVALID);
+    n = n < 0 ? 0 : a.max_n;
+  }
+  const int nb = (n + 63) / 64;
+  // ---- block maxima (16-byte loads: a block is 64 consecutive scores) --------------
+  for (int bl = tid; bl < nb; bl += kThreads) {
+    const float4* p4 = reinterpret_cast<const float4*>(row + (size_t)bl * 64);
+    const int cnt = min(64, n - bl * 64);
+    float m = -INFINITY;
+    if (cnt == 64) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float4 v = __ldg(p4 + j);
+        m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+      }
+    } else {
+      for (int j = 0; j < cnt; ++j) m = fmaxf(m, __ldg(row + (size_t)bl * 64 + j));
+    }
+    sm.bkey[bl] = score_key(m == 0.0f ? 0.0f : m);
+  }
+  __syncthreads();
+  // ---- the kept blocks: keys above the B-th, then equal keys by lower index --------
+  const int kb = min(blocks, nb);
+  uint32_t Tb = 0, take_b = (uint32_t)kb;
+  if (kb < nb) two_radix([&](int i) { return sm.bkey[i]; }, nb, (uint32_t)kb, sm, &Tb, &take_b);
+  {
+    uint32_t eq_base = 0, kept_base = 0;
+    for (int c0 = 0; c0 < nb; c0 += kThreads) {
+      const int bl = c0 + tid;
+      const uint32_t k = bl < nb ? sm.bkey[bl] : 0u;
+      const uint32_t is_eq = (bl < nb && kb < nb && k == Tb) ? 1u : 0u;
+      uint32_t tot_eq;
+      const uint32_t eq_rank = eq_base + two_scan(is_eq, &tot_eq, sm);
+      const uint32_t keep = (bl < nb && (kb >= nb || k > Tb || (is_eq && eq_rank < take_b))) ? 1u : 0u;
+      uint32_t tot_keep;
+      const uint32_t pos = kept_base + two_scan(keep, &tot_keep, sm);
+      if (keep && pos < (uint32_t)kTwoMaxKept) sm.kept[pos] = bl;
+      eq_base += tot_eq;
+      kept_base += tot_keep;
+    }
+  }
+  __syncthreads();
+  // ---- candidates: the kept blocks' entries in ascending order ----------------------
+  const int last_cnt = n - 64 * (nb - 1);                  // entries of the row's last block
+  const int m = kb == 0 ? 0 : (sm.kept[kb - 1] == nb - 1 ? 64 * (kb - 1) + last_cnt : 64 * kb);
+  for (int c = tid; c < m; c += kThreads) {
+    const float v = __ldg(row + (size_t)sm.kept[c >> 6] * 64 + (c & 63));
+    sm.cand_key[c] = score_key(v == 0.0f ? 0.0f : v);
+  }
+  __syncthreads();
+  auto entry = [&](int c) { return sm.kept[c >> 6] * 64 + (c & 63); };
+  if (m <= TOPK) {
+    for (int i = tid; i < TOPK; i += kThreads) out[i] = i < m ? entry(i) : -1;
+    return;
+  }
+  uint32_t T, take;
+  two_radix([&](int i) { return sm.cand_key[i]; }, m, (uint32_t)TOPK, sm, &T, &take);
+  uint32_t eq_base = 0, sel_base = 0;
+  for (int c0 = 0; c0 < m; c0 += kThreads) {
+    const int c = c0 + tid;
+    const uint32_t k = c < m ? sm.cand_key[c] : 0u;
+    const uint32_t is_eq = (c < m && k == T) ? 1u : 0u;
+    uint32_t tot_eq;
+    const uint32_t eq_rank = eq_base + two_scan(is_eq, &tot_eq, sm);
+    const uint32_t sel = (c < m && (k > T || (is_eq && eq_rank < take))) ? 1u : 0u;
+    uint32_t tot_sel;
+    const uint32_t pos = sel_base + two_scan(sel, &tot_sel, sm);
+    if (sel && pos < (uint32_t)TOPK) out[pos] = entry(c);
+    eq_base += tot_eq;
+    sel_base += tot_sel;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_topk_two_level(const TopkArgs& a, int32_t blocks, Order order, cudaStream_t stream) {
+  if (a.num_rows <= 0) return cudaSuccess;
+  const size_t smem = sizeof(TwoSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_topk_two_level, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(order, k_topk_two_level, dim3(a.num_rows), dim3(kThreads), smem, stream, a, blocks);
+}
 
 cudaError_t launch_topk(const TopkArgs& a, Order order, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;

@@ -9,7 +9,7 @@ import numpy as np
 import torch
 
 from . import (KV_PAGE_BYTES, IDX_PAGE_BYTES, OP_APPEND, OP_DECODE, csa_append, csa_append_compress,
-               make_compress, csa_decode, csa_step,
+               make_compress, csa_decode, csa_step, csa_step_ex,
                csa_workspace_size, make_cache, make_rows, make_window)
 
 
@@ -139,10 +139,16 @@ class DeviceState:
         csa_append(self.cache, self.window, s["pos0"], s["tok_off"], self.wl.R, s["kv_new"], s["idx_new"],
                    self.pending, self.ws_append, stream)
 
-    def step(self, s, stream=None):
-        """The step's append and decode in one csa_step call (the append's
-        device-side faults land in the decode workspace s["ws"])."""
+    def step(self, s, stream=None, opts=None):
+        """The step's append and decode in one csa_step call (csa_step_ex with
+        options); the append's device-side faults land in the decode workspace
+        s["ws"]."""
         wl = self.wl
+        if opts is not None:
+            csa_step_ex(self.cache, self.window, s["pos0"], s["tok_off"], wl.R, s["kv_new"], s["idx_new"],
+                        self.pending, getattr(self, "compress", None), s["rows"], wl.Hi, s["q_idx"], s["w"], wl.H,
+                        s["q"], wl.softmax_scale, s["out"], s["lse"], s["topk"], opts, s["ws"], stream)
+            return
         csa_step(self.cache, self.window, s["pos0"], s["tok_off"], wl.R, s["kv_new"], s["idx_new"], self.pending,
                  getattr(self, "compress", None), s["rows"], wl.Hi, s["q_idx"], s["w"], wl.H, s["q"],
                  wl.softmax_scale, s["out"], s["lse"], s["topk"], s["ws"], stream)

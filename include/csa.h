@@ -230,8 +230,12 @@ CSA_API csa_status_t csa_decode(const csa_cache_t* cache, const csa_window_t* wi
                         void* out, float* lse, int32_t* topk_out,
                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Options of the attention step (csa_sparse_attn_ex, csa_decode_ex,
- * csa_step_ex); NULL = none of them.
+/* Options of the selection and attention steps (csa_sparse_attn_ex,
+ * csa_decode_ex, csa_step_ex); NULL = none of them.
+ *  candidate_blocks  0: the exact top-512 over every visible entry.  B in
+ *            [1, 128] (csa_decode_ex / csa_step_ex): the two-level candidate
+ *            filter of csa_topk_two_level instead ([SGL] "Architecture changes
+ *            and KV cache compression": CSA2 narrows the indexer's search).
  *  plan_out  [R, 512] int32 (nullable): the resolved cache entry of every
  *            selected index, page * 64 + slot (-1: none), as the attention
  *            step looked it up -- the plan that further layers reading the
@@ -256,7 +260,25 @@ typedef struct {
   const float*   rope_cos;
   const float*   rope_sin;
   int32_t        rope_rows;
-} csa_attn_opts_t;
+  int32_t        candidate_blocks;
+} csa_opts_t;
+
+/* csa_topk_two_level -- the two-level candidate filter (NEXT f-2), a variant of
+ * csa_topk, not its replacement ([SGL] "Architecture changes and KV cache
+ * compression": CSA2 narrows the indexer's search before the top 512;
+ * "DSpark adaptation and optimization": chosen candidate blocks expand
+ * straight into a token mask).  The pages give no block size or block score;
+ * this library's reading: a block is 64 consecutive entries (a page),
+ * scored by its largest score; the first `blocks` blocks by (block score
+ * descending, block index ascending) are kept; the exact top-512 among their
+ * entries by (score descending, index ascending) is written in ascending
+ * order, padded with -1.  With blocks >= ceil(n/64) or blocks >= 512 the
+ * result equals csa_topk's.  blocks in [1, 128] (CSA_ERR_UNSUPPORTED
+ * otherwise); max_n <= 262144; scores 16-byte aligned, ld a multiple of 4.
+ * Other arguments as csa_topk. */
+CSA_API csa_status_t csa_topk_two_level(int32_t num_rows, const float* scores, int32_t ld,
+                                        const int32_t* n_valid, int32_t max_n, int32_t blocks,
+                                        int32_t* out_idx, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* csa_sparse_attn with options; arguments and errors otherwise as
  * csa_sparse_attn.  CSA_ERR_INVALID_ARGUMENT for a misaligned option pointer,
@@ -265,7 +287,7 @@ typedef struct {
 CSA_API csa_status_t csa_sparse_attn_ex(const csa_cache_t* cache, const csa_window_t* window,
                                         const csa_rows_t* rows, const int32_t* topk_idx,
                                         int32_t n_heads, const void* q, float softmax_scale,
-                                        void* out, float* lse, const csa_attn_opts_t* opts,
+                                        void* out, float* lse, const csa_opts_t* opts,
                                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* csa_decode with options for its attention step (plan_in not allowed: the
@@ -273,7 +295,7 @@ CSA_API csa_status_t csa_sparse_attn_ex(const csa_cache_t* cache, const csa_wind
 CSA_API csa_status_t csa_decode_ex(const csa_cache_t* cache, const csa_window_t* window,
                                    const csa_rows_t* rows, int32_t n_idx_heads, const void* q_idx,
                                    const float* w, int32_t n_heads, const void* q, float softmax_scale,
-                                   void* out, float* lse, int32_t* topk_out, const csa_attn_opts_t* opts,
+                                   void* out, float* lse, int32_t* topk_out, const csa_opts_t* opts,
                                    void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* csa_index_score_noalloc -- the same scores as csa_index_score, without a
@@ -366,7 +388,7 @@ CSA_API csa_status_t csa_step_ex(const csa_cache_t* cache, const csa_window_t* w
                                  const csa_compress_t* compress, const csa_rows_t* rows,
                                  int32_t n_idx_heads, const void* q_idx, const float* w,
                                  int32_t n_heads, const void* q, float softmax_scale,
-                                 void* out, float* lse, int32_t* topk_out, const csa_attn_opts_t* opts,
+                                 void* out, float* lse, int32_t* topk_out, const csa_opts_t* opts,
                                  void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, returns the status word's flags in *flags_out (host)

@@ -175,3 +175,11 @@ def test_header_compiles_as_plain_c_and_cpp(tmp_path, lang, std):
                         "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src)],
                        capture_output=True, text=True)
     assert p.returncode == 0, p.stderr
+
+
+def test_two_level_filter_bounds_before_launch(lib):
+    assert lib.csa_topk_two_level(1, None, 512, None, 512, 0, None, None, 0, None) == 2       # blocks < 1
+    assert lib.csa_topk_two_level(1, None, 512, None, 512, 129, None, None, 0, None) == 2     # blocks > 128
+    assert lib.csa_topk_two_level(1, None, 300000, None, 262145, 8, None, None, 0, None) == 2  # row too long
+    assert lib.csa_topk_two_level(1, None, 512, None, 512, 8, None, None, 0, None) == 1       # NULL scores
+    assert lib.csa_topk_two_level(0, None, 512, None, 512, 8, None, None, 0, None) == 0       # nothing to do

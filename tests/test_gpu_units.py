@@ -480,7 +480,7 @@ def test_decode_plan_is_the_resolved_selection_and_later_layers_reuse_it():
     st.step_append(s)
     plan = torch.full((wl.R, 512), -7, dtype=torch.int32, device="cuda")
     csa.csa_decode_ex(st.cache, st.window, s["rows"], wl.Hi, s["q_idx"], s["w"], wl.H, s["q"], wl.softmax_scale,
-                      s["out"], s["lse"], s["topk"], csa.make_attn_opts(plan_out=plan), s["ws"])
+                      s["out"], s["lse"], s["topk"], csa.make_opts(plan_out=plan), s["ws"])
     rc, flags = csa.csa_check_device_status(s["ws"])
     assert rc == 0 and flags == 0, flags
     topk = s["topk"].cpu().numpy()
@@ -494,7 +494,7 @@ def test_decode_plan_is_the_resolved_selection_and_later_layers_reuse_it():
         o_p, l_p = torch.empty_like(s["out"]), torch.empty_like(s["lse"])
         csa.csa_sparse_attn(st.cache, st.window, s["rows"], s["topk"], wl.H, q_l, wl.softmax_scale, o_i, l_i, ws_a)
         csa.csa_sparse_attn_ex(st.cache, st.window, s["rows"], None, wl.H, q_l, wl.softmax_scale, o_p, l_p,
-                               csa.make_attn_opts(plan_in=plan), ws_a)
+                               csa.make_opts(plan_in=plan), ws_a)
         rc, flags = csa.csa_check_device_status(ws_a)
         assert rc == 0 and flags == 0, flags
         assert torch.equal(o_i, o_p) and torch.equal(l_i, l_p)
@@ -557,7 +557,7 @@ def test_rotary_attention_matches_oracle(H, ctx, rows):
     lse = torch.empty((wl.R, H), device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     csa.csa_sparse_attn_ex(st.cache, st.window, s["rows"], torch.from_numpy(topk).cuda(), H, s["q"],
-                           wl.softmax_scale, out, lse, csa.make_attn_opts(rope_cos=cs, rope_sin=sn), ws)
+                           wl.softmax_scale, out, lse, csa.make_opts(rope_cos=cs, rope_sin=sn), ws)
     rc, flags = csa.csa_check_device_status(ws)
     assert rc == 0 and flags == 0, flags
     o_ref = np.zeros((wl.R, H, 512), np.float32)
@@ -571,7 +571,7 @@ def test_rotary_attention_matches_oracle(H, ctx, rows):
     # a row past the tables is flagged and left empty
     short_c, short_s = cs[: int(wl.row_pos.max())].contiguous(), sn[: int(wl.row_pos.max())].contiguous()
     csa.csa_sparse_attn_ex(st.cache, st.window, s["rows"], torch.from_numpy(topk).cuda(), H, s["q"],
-                           wl.softmax_scale, out, lse, csa.make_attn_opts(rope_cos=short_c, rope_sin=short_s), ws)
+                           wl.softmax_scale, out, lse, csa.make_opts(rope_cos=short_c, rope_sin=short_s), ws)
     rc, flags = csa.csa_check_device_status(ws)
     assert rc == 5 and (flags & csa.FLAG_ROW_INVALID)
     last = int(np.argmax(wl.row_pos))
@@ -587,7 +587,7 @@ def test_step_ex_rotates_keys_query_and_window_with_one_table():
     cs, sn, c = _rope_tables(64, int(wl.ctx_len.max()))
     dev = {k: (torch.from_numpy(v).cuda() if isinstance(v, np.ndarray) else v) for k, v in c.items()}
     comp = csa.make_compress(dev["kv_gamma"], dev["idx_gamma"], dev["eps"], dev["rope_cos"], dev["rope_sin"])
-    opts = csa.make_attn_opts(rope_cos=cs, rope_sin=sn)
+    opts = csa.make_opts(rope_cos=cs, rope_sin=sn)
     states = []
     for fused in (False, True):
         st = DeviceState(wl)
@@ -634,3 +634,68 @@ def test_step_ex_rotates_keys_query_and_window_with_one_table():
         o_ref[r], l_ref[r], _ = oracle.attention_row_rope(ref, wl.row_req[r], wl.row_pos[r], gt[r], q[r],
                                                           wl.softmax_scale, c["rope_cos"], c["rope_sin"])
     _check_rope_attention(wl, ref, gt, q, sb["out"].float().cpu().numpy(), sb["lse"].cpu().numpy(), o_ref, l_ref)
+
+
+# ------------------------------------------------ two-level candidate filter (NEXT f-2)
+@pytest.mark.parametrize("n", [1, 64, 65, 511, 700, 5000, 70000, 262144])
+def test_topk_two_level_exact(n):
+    g = np.random.default_rng(n + 5)
+    R = 3
+    ld = max(64, ((n + 63) // 64) * 64)
+    sc = (g.integers(0, 400, (R, ld)) / 16).astype(np.float32)   # many exact ties
+    sc[1] = -sc[1]
+    sc[2, : n // 2] = 0.0
+    sc[2, n // 3: n // 2] = -0.0
+    nv = np.array([n, n, n], np.int32)
+    nb = (n + 63) // 64
+    d_sc, d_nv = torch.from_numpy(sc).cuda(), torch.from_numpy(nv).cuda()
+    out = torch.empty((R, 512), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    for B in sorted({1, 7, 64, 128, min(nb, 128)}):
+        csa.csa_topk_two_level(R, d_sc, ld, d_nv, n, B, out, ws)
+        got = out.cpu().numpy()
+        for r in range(R):
+            assert np.array_equal(got[r], oracle.topk_two_level(sc[r], n, B)), (B, r)
+    rc, flags = csa.csa_check_device_status(ws)
+    assert rc == 0 and flags == 0
+
+
+def test_decode_with_two_level_filter():
+    """csa_decode_ex with candidate_blocks selects exactly what the standalone
+    filter selects from the same scores, and attends over that selection."""
+    ctx = [700, 9000, 30000, 2500, 64000, 129]
+    wl = W.custom("two", 65, ctx, [1] * len(ctx), H=64, Hi=64, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    B = 32
+    csa.csa_decode_ex(st.cache, st.window, s["rows"], wl.Hi, s["q_idx"], s["w"], wl.H, s["q"], wl.softmax_scale,
+                      s["out"], s["lse"], s["topk"], csa.make_opts(candidate_blocks=B), s["ws"])
+    rc, flags = csa.csa_check_device_status(s["ws"])
+    assert rc == 0 and flags == 0, flags
+    ld = ((wl.max_entries + 63) // 64) * 64
+    scores = torch.full((wl.R, ld), float("nan"), device="cuda")
+    ws = torch.zeros(csa.csa_workspace_size(csa.OP_INDEX_SCORE, wl.R, wl.max_entries, 16), dtype=torch.uint8,
+                     device="cuda")
+    csa.csa_index_score(st.cache, s["rows"], wl.Hi, s["q_idx"], s["w"], scores, ld, ws)
+    n = torch.from_numpy(wl.row_entries()).cuda()
+    want = torch.empty_like(s["topk"])
+    csa.csa_topk_two_level(wl.R, scores, ld, n, wl.max_entries, B, want, ws)
+    assert torch.equal(s["topk"], want)
+    gt = s["topk"].cpu().numpy()
+    sc = scores.cpu().numpy()
+    nn = wl.row_entries()
+    recall = []
+    for r in range(wl.R):
+        assert np.array_equal(gt[r], oracle.topk_two_level(sc[r], int(nn[r]), B)), r
+        flat = set(oracle.topk_row(sc[r], int(nn[r])).tolist()) - {-1}
+        recall.append(len(flat & set(gt[r].tolist())) / max(1, len(flat)))
+    ref = oracle.build_cache(wl)
+    _, _, q = wl.step_queries()
+    o_ref = np.zeros((wl.R, wl.H, 512), np.float32)
+    l_ref = np.zeros((wl.R, wl.H), np.float32)
+    for r in range(wl.R):
+        o_ref[r], l_ref[r] = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], gt[r], q[r], wl.softmax_scale)
+    parity.check_attention(s["out"].float().cpu().numpy(), o_ref, s["lse"].cpu().numpy(), l_ref)
+    print("two-level B=32 recall of the flat top-512 per row:", [round(x, 3) for x in recall])
