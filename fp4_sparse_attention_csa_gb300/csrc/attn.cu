@@ -69,7 +69,8 @@ struct AttnSmem {
   float mu[kTileKeys];
   float red_max[4][kMaxH];             // per key-quarter partial max / sum of a tile
   float red_sum[4][kMaxH];
-  float m_buf[2][kMaxH];               // running max (log2), by tile parity
+  float m_buf[2][kMaxH];               // running max (log2), two buffers flipped when it moves
+  float m_fin[kMaxH];                  // the final running max per head
   float l_run[kMaxH];
   float m_out[kMaxH], l_out[kMaxH];    // a split's final (m, l), read by the cluster's merge
   float inv_l[kMaxH];
@@ -332,6 +333,20 @@ __device__ __forceinline__ void dequant_win(const RawWin& g, AttnSmem& sm, int k
 __device__ __forceinline__ void group_sync(int id) {
   asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
+// The same barrier, also OR-ing a flag over the four warps: every thread of
+// the head group gets the same answer, so all take the same branch after it.
+__device__ __forceinline__ bool group_sync_or(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
 
 template <int N>
 __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]) {
@@ -405,9 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const int m_beg = max(t_beg - hw, 0), m_end = max(t_end - hw, 0);   // main tiles [m_beg, m_end)
 
   // ---- prologue, overlapping the previous kernel's tail when chained after
-  // the top-k of the same call: barriers, TMEM; then wait for it (the
-  // selected indices are ready from there on).  The row inputs read above
-  // and the cache were complete before the call's first kernel started.
+  // the top-k of the same call: barriers and TMEM, then everything that does
+  // not read the selection -- Q, and the whole window tile (gather,
+  // dequantise, S, softmax, PV issue) -- and only then the wait for the
+  // top-k.  The call's inputs were complete before its first kernel started;
+  // the window ring and the cache, which the step's append writes, were
+  // complete before this kernel could start (in a step the score kernel lets
+  // its dependents start only after its own wait, which follows the append).
   pdl_trigger();
   if (tid == 0) {
     mbar_init(&sm.s_bar, 1);
@@ -415,21 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     fence_barrier_init();
   }
   if (warp == 0) tmem_alloc(&sm.tmem_base, 512);
-  pdl_wait();
 
-  // ---- setup.  The window tile's loads go out first (they need no lookup);
-  // the selected entries are looked up (index, then page) while Q is loaded,
-  // and every entry's bytes are prefetched into L2 at once, so the per-tile
-  // gathers below hit L2.
   const int key = 8 * warp + (lane & 7), gq = lane >> 3;      // gather role (see RawMain)
   RawWin wraw;
   RawMain cur, nxt;
   wraw.valid = 0;
   cur.valid = 0;
   if (win_here) gather_win(a, b, pos, key, gq, wraw);
-  const int j = tid;                              // TOPK == kThreads: one selected entry per thread
-  const bool jin = j < nsel && j >= m_beg * kTileKeys && j < m_end * kTileKeys;
-  int e = jin ? __ldg((a.plan_in ? a.plan_in : a.topk) + (size_t)r * TOPK + j) : -1;
   constexpr int kQChunks = H * 64 / kThreads;     // 16-byte chunks of Q per thread
   uint4 qv[kQChunks];
   const uint16_t* qr = a.q + (size_t)r * H * D;
@@ -437,32 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   for (int i = 0; i < kQChunks; ++i) {
     const int c = tid + i * kThreads, h = c >> 6, ch = c & 63;
     qv[i] = __ldg(reinterpret_cast<const uint4*>(qr + (size_t)h * D + ch * 8));
-  }
-  {
-    int pg = -1, slot = 0;
-    if (e >= 0 && a.plan_in) {                    // a resolved entry: page * 64 + slot
-      if ((e >> 6) >= a.num_pages) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
-      else { pg = e >> 6; slot = e & (PAGE - 1); }
-    } else if (e >= 0) {
-      if (e >= n || e / PAGE >= a.max_pages) {
-        raise_flag(a.status, CSA_FLAG_TOPK_OOB);
-      } else {
-        const int p = __ldg(a.page_table + (size_t)b * a.max_pages + e / PAGE);
-        if (p < 0 || p >= a.num_pages) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
-        else { pg = p; slot = e % PAGE; }
-      }
-    }
-    // the plan: every slot of the row written once (its tile's CTA, or split
-    // 0 for the padding past the selection)
-    if (a.plan_out && (jin || (split == 0 && j >= nsel)))
-      a.plan_out[(size_t)r * TOPK + j] = pg >= 0 ? pg * PAGE + slot : -1;
-    if (pg >= 0) {
-      const uint8_t* src = a.kv_pool + (size_t)pg * KV_PAGE;
-      prefetch_l2(src + slot * 256, 256);
-      prefetch_l2(src + KV_SCALE_OFF + slot * 32, 32);
-    }
-    sm.ent_pg[j] = pg;
-    sm.ent_slot[j] = (uint8_t)slot;
   }
   // Q: bf16 -> fp16, K-major 128B swizzle.  With rotary tables the last 64
   // dims of every head are rotated with the row's table row first (fp32, then
@@ -507,8 +492,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     sm.m_buf[1][tid] = -INFINITY;
     sm.l_run[tid] = 0.0f;
   }
-  __syncthreads();                                // entry table visible
-  if (!win_here && m_beg < m_end) gather_main(a, sm, m_beg, key, gq, cur);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -527,6 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const uint64_t dQ = smem_desc(smem_u32(sm.q), 16, 1024, kSwizzle128B);
   const uint64_t dV = smem_desc(smem_u32(sm.k), 16384, 1024, kSwizzle128B);
   const uint64_t dP = smem_desc(smem_u32(sm.p), 8192, 1024, kSwizzle128B);
+
+  // Softmax state: the running max per head in sm.m_buf[mcur] (the same for
+  // the four warps of a head group, which flip mcur together), and this
+  // thread's partial sums of p over its keys for its HH heads.
+  int mcur = 0;
+  float lpart[HH];
+#pragma unroll
+  for (int i = 0; i < HH; ++i) lpart[i] = 0.0f;
 
   // S^T, softmax, P, rescale, PV for the tile now in sm.k.
   auto compute = [&](int it, bool is_win) -> bool {
@@ -561,24 +552,65 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     const float f = scale_log2 * (is_win ? mu_k : 1.0f);
 #pragma unroll
     for (int i = 0; i < HH; ++i) lg[i] = key_ok ? lg[i] * f : -INFINITY;
-    float tmp[HH];
+    // The running max moves only when a logit of the tile exceeds it by more
+    // than 2^8 (p stays <= 2^8, far inside fp16).  The head group agrees on
+    // that with one barrier; usually nothing moves, and then no max or sum is
+    // reduced here at all: each thread adds its own p to its partial sums,
+    // which are reduced once after the last tile.
+    const float* mr = sm.m_buf[mcur] + hsel * HH;
+    bool need = false;
 #pragma unroll
-    for (int i = 0; i < HH; ++i) tmp[i] = lg[i];
-    constexpr int kShift = RedShift<HH>::v;
-    {
-      const float mx = warp_reduce_many<HH, true>(tmp, lane);
-      if ((lane & ((1 << kShift) - 1)) == 0) sm.red_max[q4][hsel * HH + (lane >> kShift)] = mx;
-    }
-    group_sync(1 + hsel);
-    // lane i < HH owns head hsel*HH + i: its new running max and correction
-    float mnew = 0.0f, alpha = 1.0f;
-    {
-      const float tmax = fmaxf(fmaxf(sm.red_max[0][myh], sm.red_max[1][myh]),
-                               fmaxf(sm.red_max[2][myh], sm.red_max[3][myh]));
-      const float mold = sm.m_buf[(it + 1) & 1][myh];
-      mnew = (mold == -INFINITY || tmax > mold + kRescaleLog2) ? tmax : mold;
-      alpha = (mold == -INFINITY) ? 0.0f : (mnew == mold ? 1.0f : exp2f(mold - mnew));
-      if (q4 == 0 && lane < HH) sm.m_buf[it & 1][myh] = mnew;
+    for (int i = 0; i < HH; ++i) need |= lg[i] > mr[i] + kRescaleLog2;
+    need = group_sync_or(1 + hsel, need);
+    float mi[HH];
+    if (need) {
+      float tmp[HH];
+#pragma unroll
+      for (int i = 0; i < HH; ++i) tmp[i] = lg[i];
+      constexpr int kShift = RedShift<HH>::v;
+      {
+        const float mx = warp_reduce_many<HH, true>(tmp, lane);
+        if ((lane & ((1 << kShift) - 1)) == 0) sm.red_max[q4][hsel * HH + (lane >> kShift)] = mx;
+      }
+      group_sync(5 + hsel);
+      // lane i < HH owns head hsel*HH + i: its new running max and correction
+      float mnew, alpha;
+      {
+        const float tmax = fmaxf(fmaxf(sm.red_max[0][myh], sm.red_max[1][myh]),
+                                 fmaxf(sm.red_max[2][myh], sm.red_max[3][myh]));
+        const float mold = sm.m_buf[mcur][myh];
+        mnew = (mold == -INFINITY || tmax > mold + kRescaleLog2) ? tmax : mold;
+        alpha = (mold == -INFINITY) ? 0.0f : (mnew == mold ? 1.0f : exp2f(mold - mnew));
+        if (q4 == 0 && lane < HH) sm.m_buf[mcur ^ 1][myh] = mnew;
+      }
+      bool moved = false;
+#pragma unroll
+      for (int i = 0; i < HH; ++i) {
+        mi[i] = __shfl_sync(0xFFFFFFFFu, mnew, i);
+        const float al = __shfl_sync(0xFFFFFFFFu, alpha, i);
+        lpart[i] *= al;
+        moved |= al != 1.0f;
+      }
+      // rescale this warp's lanes of the O^T columns of its heads whose max moved
+      if (it > 0 && moved) {
+        float al[HH];
+#pragma unroll
+        for (int i = 0; i < HH; ++i) al[i] = __shfl_sync(0xFFFFFFFFu, alpha, i);
+#pragma unroll 1
+        for (int dc = 0; dc < D / 128; ++dc) {
+          float v[HH];
+          const uint32_t ta = tO + lane_off + dc * 64 + hsel * HH;
+          tmem_ld_n<HH>(ta, v);
+#pragma unroll
+          for (int i = 0; i < HH; ++i) v[i] *= al[i];
+          tmem_st_n<HH>(ta, v);
+        }
+        tmem_st_wait();
+      }
+      mcur ^= 1;
+    } else {
+#pragma unroll
+      for (int i = 0; i < HH; ++i) mi[i] = mr[i];
     }
     // p = exp2(l - m); P'^T = p * mu (window) as fp16, heads along the 128-byte row
     {
@@ -586,11 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
       uint32_t packed[HH / 2];
 #pragma unroll
       for (int i = 0; i < HH; i += 2) {
-        const float m0 = __shfl_sync(0xFFFFFFFFu, mnew, i), m1 = __shfl_sync(0xFFFFFFFFu, mnew, i + 1);
-        const float p0 = (lg[i] == -INFINITY) ? 0.0f : exp2f(lg[i] - m0);
-        const float p1 = (lg[i + 1] == -INFINITY) ? 0.0f : exp2f(lg[i + 1] - m1);
-        tmp[i] = p0;
-        tmp[i + 1] = p1;
+        const float p0 = (lg[i] == -INFINITY) ? 0.0f : exp2f(lg[i] - mi[i]);
+        const float p1 = (lg[i + 1] == -INFINITY) ? 0.0f : exp2f(lg[i + 1] - mi[i + 1]);
+        lpart[i] += p0;
+        lpart[i + 1] += p1;
         const __half2 hv = __floats2half2_rn(p0 * fm, p1 * fm);
         packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hv);
       }
@@ -607,32 +638,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
         *reinterpret_cast<uint2*>(prow + swz128(mykey & 7, chunk) + 8 * (hsel & 1)) =
             make_uint2(packed[0], packed[1]);
       }
-    }
-    {
-      const float sum = warp_reduce_many<HH, false>(tmp, lane);
-      if ((lane & ((1 << kShift) - 1)) == 0) sm.red_sum[q4][hsel * HH + (lane >> kShift)] = sum;
-    }
-    // rescale this warp's lanes of the O^T columns of its heads whose max moved
-    const bool resc = __any_sync(0xFFFFFFFFu, it > 0 && lane < HH && alpha != 1.0f);
-    if (resc) {
-      float al[HH];
-#pragma unroll
-      for (int i = 0; i < HH; ++i) al[i] = __shfl_sync(0xFFFFFFFFu, alpha, i);
-#pragma unroll 1
-      for (int dc = 0; dc < D / 128; ++dc) {
-        float v[HH];
-        const uint32_t ta = tO + lane_off + dc * 64 + hsel * HH;
-        tmem_ld_n<HH>(ta, v);
-#pragma unroll
-        for (int i = 0; i < HH; ++i) v[i] *= al[i];
-        tmem_st_n<HH>(ta, v);
-      }
-      tmem_st_wait();
-    }
-    group_sync(5 + hsel);
-    if (q4 == 0 && lane < HH) {
-      const float ts = (sm.red_sum[0][myh] + sm.red_sum[1][myh]) + (sm.red_sum[2][myh] + sm.red_sum[3][myh]);
-      sm.l_run[myh] = alpha * sm.l_run[myh] + ts;
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -658,8 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
 
   int it = 0;
   if (win_here) {
-    if (m_beg < m_end) gather_main(a, sm, m_beg, key, gq, cur);
-    // ---------------- the window tile ----------------
+    // ---------------- the window tile (before the wait) ----------------
     {
       // this thread's window token position; a key past the row's position is
       // empty (zero) and uses the row's own table row.  Whether to rotate is
@@ -672,6 +676,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     ok = compute(0, true);
     it = 1;
   }
+  pdl_wait();                    // the selected indices are ready from here on
+
+  // ---- the selected entries: looked up (index, then page) by all threads at
+  // once and their bytes prefetched into L2, so the per-tile gathers hit L2
+  const int j = tid;                              // TOPK == kThreads: one selected entry per thread
+  const bool jin = j < nsel && j >= m_beg * kTileKeys && j < m_end * kTileKeys;
+  int e = jin ? __ldg((a.plan_in ? a.plan_in : a.topk) + (size_t)r * TOPK + j) : -1;
+  {
+    int pg = -1, slot = 0;
+    if (e >= 0 && a.plan_in) {                    // a resolved entry: page * 64 + slot
+      if ((e >> 6) >= a.num_pages) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
+      else { pg = e >> 6; slot = e & (PAGE - 1); }
+    } else if (e >= 0) {
+      if (e >= n || e / PAGE >= a.max_pages) {
+        raise_flag(a.status, CSA_FLAG_TOPK_OOB);
+      } else {
+        const int p = __ldg(a.page_table + (size_t)b * a.max_pages + e / PAGE);
+        if (p < 0 || p >= a.num_pages) raise_flag(a.status, CSA_FLAG_PAGE_OOB);
+        else { pg = p; slot = e % PAGE; }
+      }
+    }
+    // the plan: every slot of the row written once (its tile's CTA, or split
+    // 0 for the padding past the selection)
+    if (a.plan_out && (jin || (split == 0 && j >= nsel)))
+      a.plan_out[(size_t)r * TOPK + j] = pg >= 0 ? pg * PAGE + slot : -1;
+    if (pg >= 0) {
+      const uint8_t* src = a.kv_pool + (size_t)pg * KV_PAGE;
+      prefetch_l2(src + slot * 256, 256);
+      prefetch_l2(src + KV_SCALE_OFF + slot * 32, 32);
+    }
+    sm.ent_pg[j] = pg;
+    sm.ent_slot[j] = (uint8_t)slot;
+  }
+  __syncthreads();                                // entry table visible
+  if (m_beg < m_end) gather_main(a, sm, m_beg, key, gq, cur);
   for (int m = m_beg; m < m_end && ok; ++m, ++it) {
     nxt.valid = 0;
     if (m + 1 < m_end) gather_main(a, sm, m + 1, key, gq, nxt);
@@ -692,12 +731,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
       ok = false;
     }
   }
+  // ---- the sums of p over all keys per head: the threads' partial sums reduced once
+  {
+    constexpr int kShift = RedShift<HH>::v;
+    float tmp[HH];
+#pragma unroll
+    for (int i = 0; i < HH; ++i) tmp[i] = lpart[i];
+    const float sum = warp_reduce_many<HH, false>(tmp, lane);
+    if ((lane & ((1 << kShift) - 1)) == 0) sm.red_sum[q4][hsel * HH + (lane >> kShift)] = sum;
+    group_sync(1 + hsel);
+    if (q4 == 0 && lane < HH) {
+      sm.l_run[myh] = (sm.red_sum[0][myh] + sm.red_sum[1][myh]) + (sm.red_sum[2][myh] + sm.red_sum[3][myh]);
+      sm.m_fin[myh] = sm.m_buf[mcur][myh];
+    }
+  }
   tc_fence_after();
   __syncthreads();
   // ---------------- epilogue ----------------
   // thread: dims d = 128*hsel + 32*q4 + lane (O^T chunk hsel, TMEM lane quarter q4)
   const bool have = ok && done > 0;
-  const float* m_fin = sm.m_buf[(done + 1) & 1];     // written by the last tile (it = done - 1)
+  const float* m_fin = sm.m_fin;
   const int d = 128 * hsel + 32 * q4 + lane;
   const uint32_t obase = tO + lane_off + hsel * 64;
   if (a.splits == 1) {

@@ -388,7 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
   ScoreWs W = carve_score_ws(ws, a.num_rows, Hi);
   const int warp = warp_id(), lane = lane_id(), tid = threadIdx.x;
   const uint8_t* ipool = static_cast<const uint8_t*>(a.idx_pool);
-  pdl_trigger();
 
   const int cols = mma_n(a.group_rows * Hp);           // TMEM columns of one accumulator
   int G, NB;
@@ -419,6 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   pdl_wait();                    // the segment table, q image and pages are ready from here on
+  // Dependents start only once every score CTA is past its wait, i.e. after
+  // the score prep and whatever it waited for (a step's cache append): the
+  // attention step reads the appended window and pages before its own wait.
+  pdl_trigger();
 
   const int S = W.nseg[0], total = W.nseg[1];
   const int per = (total + gridDim.x - 1) / gridDim.x;
