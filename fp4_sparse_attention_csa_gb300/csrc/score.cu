@@ -76,6 +76,7 @@ constexpr int kQSF = kMaxN * 4;                    // 512
 constexpr int kItemCap = 256;                      // work items per table chunk
 constexpr int kMaxGroupRows = kMaxN / 8;           // rows per segment (8 heads at least)
 static_assert(kStages % kProducers == 0, "a stage belongs to one producer warp");
+static_assert(kGroups < kStages, "an MMA warp's stage index wraps at most once per step");
 static_assert(kMaxN == 128, "one scale-factor atom and one MMA N chunk per segment");
 // TMEM columns: q scale factors (2 parities x 4), then 4 per accumulator for the
 // tile's scale factors, then the accumulators.
@@ -552,6 +553,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
       };
       int i = mg - (it_base % G);
       if (i < 0) i += G;
+      // carried per-tile state (i steps by G): the group's tile u = it / G,
+      // its slot u % NB and phase (u / NB) & 1, the stage it % kStages and
+      // that stage's use it / kStages
+      int m_u, m_ub, m_ph, m_s, m_use;
+      {
+        const int it = it_base + i;
+        m_u = it / G;
+        m_ub = m_u % NB;
+        m_ph = (m_u / NB) & 1;
+        m_s = it % kStages;
+        m_use = it / kStages;
+      }
       for (; i < m; i += G) {
         if (aborted(sm)) { ok = false; break; }
         const Item e = sm.items[i];
@@ -565,10 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
           l_id1 = idesc_mxf4(128, (uint32_t)mma_n(N), 2, 2);
           l_desc_ord = ord;
         }
-        const int it = it_base + i;
-        const int u = it / G;                        // the tile's index within its group
-        const int slot = mg * NB + (u % NB);
-        const int s = it % kStages, use = it / kStages;
+        const int u = m_u;                           // the tile's index within its group
+        const int slot = mg * NB + m_ub;
+        const uint32_t empty_par = (uint32_t)(m_ph ^ 1);   // the slot's previous use, u - NB
+        const int s = m_s, use = m_use;
+        ++m_u;
+        if (++m_ub == NB) { m_ub = 0; m_ph ^= 1; }
+        m_s += G;                                    // G < kStages: wraps at most once
+        if (m_s >= kStages) { m_s -= kStages; ++m_use; }
         if (!warp_wait<true>(&sm.full[s], use & 1, sm, a)) { ok = false; break; }
         // the tile's scale words: entry row r is page r / 64, group (r % 64) / 8, word r % 8
         {
@@ -584,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
         fence_proxy_async_smem();
         __syncwarp();
         // the accumulator's previous tile has been reduced by its four warps
-        if (u >= NB && !warp_wait<true>(&sm.acc_empty[slot], ((u / NB) - 1) & 1, sm, a)) { ok = false; break; }
+        if (u >= NB && !warp_wait<true>(&sm.acc_empty[slot], empty_par, sm, a)) { ok = false; break; }
         if (lane == 0) {
           tc_fence_after();
           const uint32_t sfa = tmem + kTmemSFA + 4 * slot;
@@ -613,6 +630,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
       int32_t* en = sm.rown[cw];                    // and of its rows' visible lengths
       int i = grp - (it_base % G);
       if (i < 0) i += G;
+      // item it = it_base + i is the group's tile u = it / G, in accumulator
+      // slot u % NB with phase (u / NB) & 1; i steps by G, so u steps by one
+      // and both are carried instead of divided out per tile
+      int c_ub, c_ph;
+      {
+        const int u = (it_base + i) / G;
+        c_ub = u % NB;
+        c_ph = (u / NB) & 1;
+      }
       for (; i < m; i += G) {
         if (aborted(sm)) break;
         const Item e = sm.items[i];
@@ -625,10 +651,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
           __syncwarp();
           e_gseg = gseg;
         }
-        const int it = it_base + i;
-        const int u = it / G;
-        const int slot = grp * NB + (u % NB);
-        if (!warp_wait<true>(&sm.acc_full[slot], (u / NB) & 1, sm, a)) break;
+        const int slot = grp * NB + c_ub;
+        const uint32_t full_par = (uint32_t)c_ph;
+        if (++c_ub == NB) { c_ub = 0; c_ph ^= 1; }
+        if (!warp_wait<true>(&sm.acc_full[slot], full_par, sm, a)) break;
         tc_fence_after();
         const int ient = e.tile * kTileEntries + mrow;
         const bool page_ok = (mrow < 64) ? (e.pg0 >= 0) : (e.pg1 >= 0);

@@ -379,29 +379,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int sli
 // CTA k streaming the contiguous slice [k*S, min(n, (k+1)*S)) of the
 // L2-resident row with 16-byte loads (S a multiple of 4).  The cluster
 //   1. reduces the slices' value ranges through distributed shared memory,
-//   2. sums the CTAs' kRowBins-bin value histograms (read remotely) and finds
-//      the bin holding rank 512; every CTA derives the same bin and each
-//      CTA's count of entries in or above it, hence its offset,
-//   3. each CTA compacts its slice's entries in or above that bin, in index
-//      order, straight into CTA 0's candidate list at its offset, so the list
-//      is in row order,
-// and CTA 0 resolves the exact 512th key and the ties' cut on the list.  A
-// list longer than kRowCap (many ties at the cut) or a non-finite range falls
-// back to a whole-row radix select in CTA 0.  A CTA leaves only after a
-// cluster barrier that follows every remote read of its shared memory.
+//   2. sums the CTAs' kRowBins-bin value histograms (read remotely); every CTA
+//      derives the same bin tb holding rank 512, the count above it and the
+//      count inside it,
+//   3. each CTA lists its slice's entries above tb (all selected) and in tb
+//      (the cut's candidates) in its own shared memory, a warp at a time with
+//      one atomic per list per warp, then copies its lists into CTA 0's at
+//      the offsets the CTAs' counts give; the lists are unordered,
+// and CTA 0 picks the cut bin's entries by (score desc, index asc) -- by
+// pairwise rank when there are few, else by radix select -- marks every
+// selected index in a bitmap of the row and writes the bitmap out in index
+// order.  A cut bin with more than kTieCap entries (many ties) or a non-finite
+// range falls back to a whole-row radix select in CTA 0.  A CTA leaves only
+// after a cluster barrier that follows every remote access to its shared memory.
 constexpr int kRowMax = 262144;
 constexpr int kRowBins = 2048;
-constexpr int kRowCap = 4096;
+constexpr int kTieCap = 4096;
+constexpr int kPairwiseMax = 256;   // cut bins up to this size are ranked pairwise
 constexpr int kRowCluster = 8;
 
 struct alignas(16) RowSmem {
   uint32_t hist[kRowBins];         // value histogram; the radix passes reuse it
-  uint32_t cand_key[kRowCap];      // CTA 0: the row's candidates, row order
-  int32_t cand_idx[kRowCap];
+  uint32_t bitmap[kRowMax / 32];   // CTA 0: selected indices of the row
+  uint32_t tie_key[kTieCap];       // CTA 0: the cut bin's entries (unordered)
+  int32_t tie_idx[kTieCap];
+  int32_t gt_idx[TOPK];            // the entries above the cut bin (unordered)
   uint32_t warp_a[kWarps], warp_b[kWarps];
-  uint32_t part[kWarps][kRowCluster];
-  uint32_t cnt[kRowCluster];       // entries in or above the cut bin, per CTA
-  uint32_t sel_bin, sel_need;
+  uint32_t gt_cnt, tie_cnt;        // this CTA's list lengths
+  uint32_t sel_bin, sel_need, sel_tie;
   float fmin, fmax;
 };
 
@@ -452,6 +457,64 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, RowS
   return off + x - v;
 }
 
+// Block-wide radix select (11/11/10 bits) of the need-th largest key among the
+// m keys key_at(i) with valid(i): the key T and how many of the keys equal to T
+// are taken (need minus the keys above T).  Uses hist, warp_a, sel_bin, sel_need.
+template <typename K, typename V>
+__device__ void row_radix(K key_at, V valid, int m, uint32_t need, RowSmem& sm, uint32_t* T_out, uint32_t* take_out) {
+  const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
+  uint32_t prefix = 0, mask = 0, rem = need;
+  const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+  for (int p = 0; p < 3; ++p) {
+    const int sh = shifts[p], nbv = 1 << widths[p];
+    for (int i = tid; i < 2048; i += kThreads) sm.hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < m; i += kThreads) {
+      if (!valid(i)) continue;
+      const uint32_t kk = key_at(i);
+      if ((kk & mask) == prefix) atomicAdd(&sm.hist[(kk >> sh) & (uint32_t)(nbv - 1)], 1u);
+    }
+    __syncthreads();
+    constexpr int per = 2048 / kThreads;
+    uint32_t c[per], mine = 0;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      const int b = per * tid + j;
+      c[j] = b < nbv ? sm.hist[b] : 0u;
+      mine += c[j];
+    }
+    uint32_t incl = mine;                         // suffix sums over higher lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    if (lane == 0) sm.warp_a[warp] = incl;
+    __syncthreads();
+    uint32_t acc = incl - mine;
+    for (int w2 = warp + 1; w2 < kWarps; ++w2) acc += sm.warp_a[w2];
+#pragma unroll
+    for (int j = per - 1; j >= 0; --j) {
+      if (acc < rem && acc + c[j] >= rem) {
+        sm.sel_bin = (uint32_t)(per * tid + j);
+        sm.sel_need = rem - acc;
+      }
+      acc += c[j];
+    }
+    __syncthreads();
+    prefix |= sm.sel_bin << sh;
+    mask |= (uint32_t)(nbv - 1) << sh;
+    rem = sm.sel_need;
+    __syncthreads();
+  }
+  *T_out = prefix;
+  *take_out = rem;
+}
+
+__device__ __forceinline__ void mark(RowSmem& sm, int idx) {
+  atomicOr(&sm.bitmap[idx >> 5], 1u << (idx & 31));
+}
+
 template <int C>                   // CTAs per row: 1, 2, 4 or 8
 __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
   pdl_trigger();
@@ -461,7 +524,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
   const int kq = (int)cluster.block_rank();
   const int r = blockIdx.x / C;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = lane_id();
   const float* row = a.scores + (size_t)r * a.ld;
   int32_t* out = a.out + (size_t)r * TOPK;
 
@@ -505,6 +568,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
     vmax = fmaxf(vmax, v);
   }
   for (int i = tid; i < kRowBins; i += kThreads) sm.hist[i] = 0u;
+  if (kq == 0)                     // CTA 0's bitmap starts empty
+    for (int i = tid; i < (n + 31) >> 5; i += kThreads) sm.bitmap[i] = 0u;
+  if (tid == 0) sm.gt_cnt = sm.tie_cnt = 0u;
   block_minmax(vmin, vmax, sm);
   cluster.sync();                                  // every slice's range is published
   vmin = INFINITY;
@@ -524,7 +590,6 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
     return b < 0 ? 0 : (b >= kRowBins ? kRowBins - 1 : b);
   };
 
-  uint32_t T = 0, take = 0;
   bool done = false;
   if (binning) {
     // ---- pass 2: histogram of the slice ---------------------------------------------
@@ -555,26 +620,20 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
       return;
     }
   } else {
-    // ---- the bin of rank 512 in the summed histogram --------------------------------
-    const int lane = lane_id(), warp = warp_id();
+    // ---- the bin of rank 512 in the summed histogram, the count above it and
+    // the count inside it (the same in every CTA) ---------------------------------------
+    const int warp = warp_id();
     constexpr int per = kRowBins / kThreads;
-    // every CTA's bins of this thread, read once from distributed shared memory
-    uint32_t hv[C][per];
-#pragma unroll
-    for (int q = 0; q < C; ++q) {
-      const uint32_t* h = cluster.map_shared_rank(sm.hist, q);
-#pragma unroll
-      for (int j = 0; j < per; ++j) hv[q][j] = h[per * tid + j];
-    }
     uint32_t c[per], mine = 0;
 #pragma unroll
-    for (int j = 0; j < per; ++j) {
-      uint32_t t = 0;
+    for (int j = 0; j < per; ++j) c[j] = 0u;
 #pragma unroll
-      for (int q = 0; q < C; ++q) t += hv[q][j];
-      c[j] = t;
-      mine += t;
+    for (int q = 0; q < C; ++q) {
+      const uint4 h = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(sm.hist, q) + per * tid);
+      c[0] += h.x; c[1] += h.y; c[2] += h.z; c[3] += h.w;
     }
+#pragma unroll
+    for (int j = 0; j < per; ++j) mine += c[j];
     uint32_t incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -587,136 +646,146 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
     for (int w2 = warp + 1; w2 < kWarps; ++w2) acc += sm.warp_a[w2];
 #pragma unroll
     for (int j = per - 1; j >= 0; --j) {
-      if (acc < (uint32_t)TOPK && acc + c[j] >= (uint32_t)TOPK) sm.sel_bin = (uint32_t)(per * tid + j);
+      if (acc < (uint32_t)TOPK && acc + c[j] >= (uint32_t)TOPK) {
+        sm.sel_bin = (uint32_t)(per * tid + j);
+        sm.sel_need = acc;                          // entries above the bin
+        sm.sel_tie = c[j];                          // entries in the bin
+      }
       acc += c[j];
     }
     __syncthreads();
     const int tb = (int)sm.sel_bin;
-    // each CTA's count of entries in bins >= tb
-#pragma unroll
-    for (int q = 0; q < C; ++q) {
-      uint32_t x = 0;
-#pragma unroll
-      for (int j = 0; j < per; ++j) x += (per * tid + j >= tb) ? hv[q][j] : 0u;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-      if (lane == 0) sm.part[warp][q] = x;
-    }
-    __syncthreads();
-    if (tid < C) {
-      uint32_t t = 0;
-      for (int w2 = 0; w2 < kWarps; ++w2) t += sm.part[w2][tid];
-      sm.cnt[tid] = t;
-    }
-    __syncthreads();
-    uint32_t m_total = 0, pre = 0;
-    for (int q = 0; q < C; ++q) {
-      if (q < kq) pre += sm.cnt[q];
-      m_total += sm.cnt[q];
-    }
-    cluster.sync();                                // every remote histogram read is done
-    if (m_total > (uint32_t)kRowCap) {
+    const uint32_t n_gt = sm.sel_need, n_tie = sm.sel_tie;
+    if (n_tie > (uint32_t)kTieCap) {
+      cluster.sync();                              // every remote histogram read is done
       if (kq != 0) return;         // CTA 0 alone: the whole-row radix below
     } else {
-      // ---- pass 3: compact entries with bin >= tb, in index order, into CTA 0 -------
-      uint32_t* dkey = cluster.map_shared_rank(sm.cand_key, 0);
-      int32_t* didx = cluster.map_shared_rank(sm.cand_idx, 0);
-      uint32_t base = pre;
-      for (int c0 = 0; c0 < len; c0 += 16 * kThreads) {
-        const int i0 = c0 + 16 * tid;
+      // ---- pass 3: list the slice's entries in or above tb --------------------------
+      const float tbf = (float)tb;
+      // a thread's up-to-16 values: count its entries above tb and in tb, one
+      // warp scan each, one atomic per list per warp, then the writes
+      auto collect = [&](const float* v, const int* idx, int cnt) {
+        uint32_t gtm = 0, tiem = 0;
+        for (int j = 0; j < cnt; ++j) {
+          if (idx[j] < 0) continue;
+          const int b = bin_of(v[j]);
+          if (b > tb) gtm |= 1u << j;
+          else if (b == tb) tiem |= 1u << j;
+        }
+        const uint32_t ng = (uint32_t)__popc(gtm), nt = (uint32_t)__popc(tiem);
+        uint32_t ig = ng, it = nt;                  // inclusive warp scans
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t yg = __shfl_up_sync(0xFFFFFFFFu, ig, o), yt = __shfl_up_sync(0xFFFFFFFFu, it, o);
+          if (lane >= o) { ig += yg; it += yt; }
+        }
+        uint32_t bg = 0, bt = 0;
+        if (lane == 31) {
+          if (ig) bg = atomicAdd(&sm.gt_cnt, ig);
+          if (it) bt = atomicAdd(&sm.tie_cnt, it);
+        }
+        bg = __shfl_sync(0xFFFFFFFFu, bg, 31) + ig - ng;
+        bt = __shfl_sync(0xFFFFFFFFu, bt, 31) + it - nt;
+        for (int j = 0; j < cnt; ++j) {
+          if (gtm & (1u << j)) sm.gt_idx[bg++] = lo + idx[j];
+          if (tiem & (1u << j)) {
+            sm.tie_key[bt] = score_key(fold(v[j]));
+            sm.tie_idx[bt] = lo + idx[j];
+            ++bt;
+          }
+        }
+      };
+      const int n4r = (n4 + 4 * kThreads - 1) / (4 * kThreads) * (4 * kThreads);   // warp-uniform trip count
+      for (int base4 = 0; base4 < n4r; base4 += 4 * kThreads) {
         float v[16];
-        if (i0 + 15 < len) {
+        int idx[16];
+        bool any = false;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 x = __ldg(sl4 + (i0 >> 2) + q);
-            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-          }
-        } else {
+        for (int j = 0; j < 4; ++j) {
+          const int i = base4 + tid + j * kThreads;
+          const float4 x = i < n4 ? __ldg(sl4 + i) : make_float4(vmin, vmin, vmin, vmin);
+          v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = i0 + j < len ? __ldg(sl + i0 + j) : vmin;
-        }
-        uint32_t bits = 0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (i0 + j < len && bin_of(v[j]) >= tb) bits |= 1u << j;
-        uint32_t tot;
-        uint32_t off = base + block_scan((uint32_t)__popc(bits), &tot, sm);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (bits & (1u << j)) {
-            dkey[off] = score_key(fold(v[j]));
-            didx[off] = lo + i0 + j;
-            ++off;
+          for (int c = 0; c < 4; ++c) {
+            idx[4 * j + c] = i < n4 ? 4 * i + c : -1;
+            // (v - vmin) * scale >= tb exactly when bin_of(v) >= tb, for tb >= 1
+            any |= (v[4 * j + c] - vmin) * scale >= tbf;
           }
         }
-        base += tot;
+        if (tb == 0) any = true;
+        if (!__any_sync(0xFFFFFFFFu, any)) continue;
+        collect(v, idx, 16);
       }
-      cluster.sync();                              // the row's list is complete in CTA 0
+      if (tid < 32) {                              // the slice's last (len mod 4) entries
+        const int i = 4 * n4 + lane;
+        float v1[1] = {i < len ? __ldg(sl + i) : vmin};
+        int i1[1] = {i < len ? i : -1};
+        collect(v1, i1, 1);
+      }
+      cluster.sync();                              // every CTA's counts are final
+      // ---- CTA q's lists go to CTA 0's at the offsets of CTAs 0..q-1 ---------------
+      if (kq != 0) {
+        uint32_t og = 0, ot = 0;
+        for (int q = 0; q < kq; ++q) {
+          const RowSmem* rs = cluster.map_shared_rank(&sm, q);
+          og += rs->gt_cnt;
+          ot += rs->tie_cnt;
+        }
+        int32_t* r_gt_idx = cluster.map_shared_rank(sm.gt_idx, 0);
+        uint32_t* r_tie_key = cluster.map_shared_rank(sm.tie_key, 0);
+        int32_t* r_tie_idx = cluster.map_shared_rank(sm.tie_idx, 0);
+        for (uint32_t t = tid; t < sm.gt_cnt; t += kThreads) r_gt_idx[og + t] = sm.gt_idx[t];
+        for (uint32_t t = tid; t < sm.tie_cnt; t += kThreads) {
+          r_tie_key[ot + t] = sm.tie_key[t];
+          r_tie_idx[ot + t] = sm.tie_idx[t];
+        }
+      }
+      cluster.sync();                              // the lists are complete in CTA 0
       if (kq != 0) return;
-      // ---- exact 512th key among the candidates ----------------------------------
-      const int m = (int)m_total;
-      {
-        uint32_t prefix = 0, mask = 0, rem = TOPK;
-        const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
-        for (int p = 0; p < 3; ++p) {
-          const int sh = shifts[p], nbv = 1 << widths[p];
-          for (int i = tid; i < 2048; i += kThreads) sm.hist[i] = 0u;
-          __syncthreads();
-          for (int i = tid; i < m; i += kThreads) {
-            const uint32_t kk = sm.cand_key[i];
-            if ((kk & mask) == prefix) atomicAdd(&sm.hist[(kk >> sh) & (uint32_t)(nbv - 1)], 1u);
+      // ---- CTA 0: the cut bin's entries by (score desc, index asc) ----------------
+      const uint32_t need = (uint32_t)TOPK - n_gt;  // 1 <= need <= n_tie
+      for (int t = tid; t < (int)n_gt; t += kThreads) mark(sm, sm.gt_idx[t]);
+      if (n_tie <= (uint32_t)kPairwiseMax) {
+        if (tid < (int)n_tie) {
+          const uint32_t k0 = sm.tie_key[tid];
+          const int i0 = sm.tie_idx[tid];
+          uint32_t rank = 0;
+          for (int j = 0; j < (int)n_tie; ++j) {
+            const uint32_t kj = sm.tie_key[j];
+            rank += (kj > k0 || (kj == k0 && sm.tie_idx[j] < i0)) ? 1u : 0u;
           }
-          __syncthreads();
-          const int lane = lane_id(), warp = warp_id();
-          constexpr int per = 2048 / kThreads;
-          uint32_t c[per], mine = 0;
-#pragma unroll
-          for (int j = 0; j < per; ++j) {
-            const int b = per * tid + j;
-            c[j] = b < nbv ? sm.hist[b] : 0u;
-            mine += c[j];
-          }
-          uint32_t incl = mine;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
-            if (lane + o < 32) incl += y;
-          }
-          if (lane == 0) sm.warp_a[warp] = incl;
-          __syncthreads();
-          uint32_t acc = incl - mine;
-          for (int w2 = warp + 1; w2 < kWarps; ++w2) acc += sm.warp_a[w2];
-#pragma unroll
-          for (int j = per - 1; j >= 0; --j) {
-            if (acc < rem && acc + c[j] >= rem) {
-              sm.sel_bin = (uint32_t)(per * tid + j);
-              sm.sel_need = rem - acc;
-            }
-            acc += c[j];
-          }
-          __syncthreads();
-          prefix |= sm.sel_bin << sh;
-          mask |= (uint32_t)(nbv - 1) << sh;
-          rem = sm.sel_need;
-          __syncthreads();
+          if (rank < need) mark(sm, i0);
         }
-        T = prefix;
-        take = rem;
+      } else {
+        uint32_t T, take;
+        row_radix([&](int i) { return sm.tie_key[i]; }, [](int) { return true; }, (int)n_tie, need, sm, &T, &take);
+        // the keys above T, and the `take` lowest indices among the keys equal to
+        // T: the take-th largest of (kRowMax - index) over those
+        uint32_t U = 0, take_u = 0;
+        row_radix([&](int i) { return (uint32_t)(kRowMax - sm.tie_idx[i]); },
+                  [&](int i) { return sm.tie_key[i] == T; }, (int)n_tie, take, sm, &U, &take_u);
+        for (int t = tid; t < (int)n_tie; t += kThreads) {
+          const uint32_t kk = sm.tie_key[t];
+          if (kk > T || (kk == T && (uint32_t)(kRowMax - sm.tie_idx[t]) >= U)) mark(sm, sm.tie_idx[t]);
+        }
       }
-      // ---- output: candidates are in index order ----------------------------------
-      uint32_t eq_base = 0, sel_base = 0;
-      for (int c0 = 0; c0 < m; c0 += kThreads) {
-        const int i = c0 + tid;
-        const uint32_t kk = i < m ? sm.cand_key[i] : 0u;
-        const uint32_t is_eq = (i < m && kk == T) ? 1u : 0u;
-        uint32_t tot_eq;
-        const uint32_t eq_rank = eq_base + block_scan(is_eq, &tot_eq, sm);
-        const uint32_t sel = (i < m && (kk > T || (is_eq && eq_rank < take))) ? 1u : 0u;
-        uint32_t tot_sel;
-        const uint32_t pos = sel_base + block_scan(sel, &tot_sel, sm);
-        if (sel && pos < (uint32_t)TOPK) out[pos] = sm.cand_idx[i];
-        eq_base += tot_eq;
-        sel_base += tot_sel;
+      __syncthreads();
+      // ---- output: the bitmap in index order ---------------------------------------
+      const int nw = (n + 31) >> 5;
+      const int wper = (nw + kThreads - 1) / kThreads;
+      const int w0 = min(nw, tid * wper), w1 = min(nw, w0 + wper);
+      uint32_t cnt = 0;
+      for (int w = w0; w < w1; ++w) cnt += (uint32_t)__popc(sm.bitmap[w]);
+      uint32_t tot;
+      uint32_t pos = block_scan(cnt, &tot, sm);
+      for (int w = w0; w < w1; ++w) {
+        uint32_t bits = sm.bitmap[w];
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1u;
+          if (pos < (uint32_t)TOPK) out[pos] = 32 * w + b;
+          ++pos;
+        }
       }
       done = true;
     }
@@ -752,8 +821,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
       rem = sm.sel_need;
       __syncthreads();
     }
-    T = prefix;
-    take = rem;
+    const uint32_t T = prefix, take = rem;
     uint32_t eq_base = 0, sel_base = 0;
     for (int c0 = 0; c0 < n; c0 += kThreads) {
       const int i = c0 + tid;
