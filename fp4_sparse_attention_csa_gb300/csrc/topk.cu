@@ -515,15 +515,26 @@ __device__ __forceinline__ void mark(RowSmem& sm, int idx) {
   atomicOr(&sm.bitmap[idx >> 5], 1u << (idx & 31));
 }
 
+// The CTAs that share a row: a thread-block cluster of C (C > 1), or this CTA
+// alone (C == 1), whose barrier is then the CTA's own and whose "remote" shared
+// memory is its own.
+template <int C>
+struct RowGroup {
+  __device__ __forceinline__ void sync() const {
+    if constexpr (C == 1) __syncthreads();
+    else cg::this_cluster().sync();
+  }
+  template <typename T>
+  __device__ __forceinline__ T* at(T* p, int q) const {
+    if constexpr (C == 1) return p;
+    else return cg::this_cluster().map_shared_rank(p, q);
+  }
+};
+
+// Row r's top-512 by its C CTAs; this is CTA kq of them.
 template <int C>                   // CTAs per row: 1, 2, 4 or 8
-__global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
-  pdl_trigger();
-  pdl_wait();                    // the scores come from the previous kernel
-  cg::cluster_group cluster = cg::this_cluster();
-  extern __shared__ __align__(16) uint8_t smem[];
-  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
-  const int kq = (int)cluster.block_rank();
-  const int r = blockIdx.x / C;
+__device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, int kq) {
+  const RowGroup<C> grp;
   const int tid = threadIdx.x, lane = lane_id();
   const float* row = a.scores + (size_t)r * a.ld;
   int32_t* out = a.out + (size_t)r * TOPK;
@@ -572,11 +583,11 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
     for (int i = tid; i < (n + 31) >> 5; i += kThreads) sm.bitmap[i] = 0u;
   if (tid == 0) sm.gt_cnt = sm.tie_cnt = 0u;
   block_minmax(vmin, vmax, sm);
-  cluster.sync();                                  // every slice's range is published
+  grp.sync();                                  // every slice's range is published
   vmin = INFINITY;
   vmax = -INFINITY;
   for (int q = 0; q < C; ++q) {
-    const RowSmem* rs = cluster.map_shared_rank(&sm, q);
+    const RowSmem* rs = grp.at(&sm, q);
     vmin = fminf(vmin, rs->fmin);
     vmax = fmaxf(vmax, rs->fmax);
   }
@@ -612,7 +623,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
     }
     for (int i = 4 * n4 + tid; i < len; i += kThreads) atomicAdd(&sm.hist[bin_of(__ldg(sl + i))], 1u);
   }
-  cluster.sync();                                  // histograms complete; range reads done
+  grp.sync();                                  // histograms complete; range reads done
   if (!binning) {
     if (kq != 0) return;           // CTA 0 alone: all equal, or the whole-row radix below
     if (range == 0.0f) {           // all equal: the lowest 512 indices
@@ -629,7 +640,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
     for (int j = 0; j < per; ++j) c[j] = 0u;
 #pragma unroll
     for (int q = 0; q < C; ++q) {
-      const uint4 h = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(sm.hist, q) + per * tid);
+      const uint4 h = *reinterpret_cast<const uint4*>(grp.at(sm.hist, q) + per * tid);
       c[0] += h.x; c[1] += h.y; c[2] += h.z; c[3] += h.w;
     }
 #pragma unroll
@@ -657,7 +668,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
     const int tb = (int)sm.sel_bin;
     const uint32_t n_gt = sm.sel_need, n_tie = sm.sel_tie;
     if (n_tie > (uint32_t)kTieCap) {
-      cluster.sync();                              // every remote histogram read is done
+      grp.sync();                              // every remote histogram read is done
       if (kq != 0) return;         // CTA 0 alone: the whole-row radix below
     } else {
       // ---- pass 3: list the slice's entries in or above tb --------------------------
@@ -722,25 +733,25 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
         int i1[1] = {i < len ? i : -1};
         collect(v1, i1, 1);
       }
-      cluster.sync();                              // every CTA's counts are final
+      grp.sync();                              // every CTA's counts are final
       // ---- CTA q's lists go to CTA 0's at the offsets of CTAs 0..q-1 ---------------
       if (kq != 0) {
         uint32_t og = 0, ot = 0;
         for (int q = 0; q < kq; ++q) {
-          const RowSmem* rs = cluster.map_shared_rank(&sm, q);
+          const RowSmem* rs = grp.at(&sm, q);
           og += rs->gt_cnt;
           ot += rs->tie_cnt;
         }
-        int32_t* r_gt_idx = cluster.map_shared_rank(sm.gt_idx, 0);
-        uint32_t* r_tie_key = cluster.map_shared_rank(sm.tie_key, 0);
-        int32_t* r_tie_idx = cluster.map_shared_rank(sm.tie_idx, 0);
+        int32_t* r_gt_idx = grp.at(sm.gt_idx, 0);
+        uint32_t* r_tie_key = grp.at(sm.tie_key, 0);
+        int32_t* r_tie_idx = grp.at(sm.tie_idx, 0);
         for (uint32_t t = tid; t < sm.gt_cnt; t += kThreads) r_gt_idx[og + t] = sm.gt_idx[t];
         for (uint32_t t = tid; t < sm.tie_cnt; t += kThreads) {
           r_tie_key[ot + t] = sm.tie_key[t];
           r_tie_idx[ot + t] = sm.tie_idx[t];
         }
       }
-      cluster.sync();                              // the lists are complete in CTA 0
+      grp.sync();                              // the lists are complete in CTA 0
       if (kq != 0) return;
       // ---- CTA 0: the cut bin's entries by (score desc, index asc) ----------------
       const uint32_t need = (uint32_t)TOPK - n_gt;  // 1 <= need <= n_tie
@@ -837,6 +848,63 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
       sel_base += tot_sel;
     }
   }
+}
+
+template <int C>                   // CTAs per row: 1, 2, 4 or 8
+__global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
+  pdl_trigger();
+  pdl_wait();                    // the scores come from the previous kernel
+  extern __shared__ __align__(16) uint8_t smem[];
+  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
+  const int kq = C == 1 ? 0 : (int)cg::this_cluster().block_rank();
+  topk_row<C>(a, sm, (int)blockIdx.x / C, kq);
+}
+
+// Rows of very different lengths (up to kPackC * kPackLong entries): clusters
+// of kPackC CTAs, the rows longer than kPackLong one to a cluster, then the
+// others one to a CTA, four to a cluster, each in row order; so no CTA streams
+// more than kPackLong entries and short rows do not tie up a whole cluster.
+// Every CTA derives the same assignment from the rows' lengths; clusters past
+// the work return at once.
+constexpr int kPackC = 4;
+constexpr int kPackLong = 16384;
+
+__global__ void __launch_bounds__(kThreads) k_topk_packed(TopkArgs a) {
+  pdl_trigger();
+  pdl_wait();                    // the scores come from the previous kernel
+  extern __shared__ __align__(16) uint8_t smem[];
+  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
+  const int tid = threadIdx.x;
+  const int c = (int)blockIdx.x / kPackC, kq = (int)cg::this_cluster().block_rank();
+  auto row_len = [&](int r) {
+    int n = a.n_valid ? __ldg(a.n_valid + r) : (__ldg(a.row_pos + r) + 1) / a.P;
+    return n < 0 ? 0 : (n > a.max_n ? a.max_n : n);
+  };
+  // the long rows come first: how many there are
+  int n_long = 0;
+  for (int base = 0; base < a.num_rows; base += kThreads) {
+    const int r = base + tid;
+    n_long += __syncthreads_count(r < a.num_rows && row_len(r) > kPackLong);
+  }
+  // this cluster's long row, or this CTA's short row: the target-th of its kind
+  const bool want_long = c < n_long;
+  const uint32_t target = want_long ? (uint32_t)c : (uint32_t)(c - n_long) * kPackC + (uint32_t)kq;
+  if (tid == 0) sm.sel_bin = 0xFFFFFFFFu;
+  uint32_t seen = 0;
+  for (int base = 0; base < a.num_rows; base += kThreads) {
+    const int r = base + tid;
+    const uint32_t kind = (r < a.num_rows && (row_len(r) > kPackLong) == want_long) ? 1u : 0u;
+    uint32_t tot;
+    const uint32_t pre = seen + block_scan(kind, &tot, sm);
+    if (kind && pre == target) sm.sel_bin = (uint32_t)r;
+    seen += tot;
+    if (seen > target) break;    // the same for every thread
+  }
+  __syncthreads();
+  const uint32_t row = sm.sel_bin;
+  __syncthreads();               // every thread has the row before sm is reused
+  if (want_long) topk_row<kPackC>(a, sm, (int)row, kq);      // the whole cluster: c < n_long
+  else if (row != 0xFFFFFFFFu) topk_row<1>(a, sm, (int)row, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -1031,7 +1099,27 @@ cudaError_t launch_topk_two_level(const TopkArgs& a, int32_t blocks, Order order
 
 cudaError_t launch_topk(const TopkArgs& a, Order order, cudaStream_t stream) {
   if (a.num_rows <= 0) return cudaSuccess;
-  if (a.max_n <= kRowMax && (a.ld % 4) == 0 && ((uintptr_t)a.scores & 15u) == 0) {
+  const bool row_ok = (a.ld % 4) == 0 && ((uintptr_t)a.scores & 15u) == 0;
+  if (row_ok && a.max_n > kPackLong && a.max_n <= kPackC * kPackLong) {
+    // rows of up to 64K entries: long rows a cluster each, short ones a CTA each
+    const size_t smem = sizeof(RowSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_topk_packed, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_rows * kPackC, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPackC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1 + order_attr(order, attr + 1);
+    return cudaLaunchKernelEx(&cfg, k_topk_packed, a);
+  }
+  if (a.max_n <= kRowMax && row_ok) {
     // CTAs per row: about one per 8K entries, up to 8, at most two CTAs per
     // SM over the grid, rounded down to a power of two (measured on the
     // serving batch, 128 rows of up to 60K entries: 1 per row 34 us, 2 per

@@ -219,6 +219,24 @@ def test_topk_rows_of_different_lengths():
         assert np.array_equal(got[r], oracle.topk_row(sc[r], int(nv[r]))), r
 
 
+def test_topk_long_and_short_rows_in_one_call():
+    """Rows longer than 16384 entries take a whole cluster, shorter ones a CTA
+    each, in one launch: the boundary lengths, a short row whose cut ties
+    overflow the candidate list, and rows of at most 512 entries."""
+    g = np.random.default_rng(11)
+    R, ld = 8, 50000
+    sc = g.standard_normal((R, ld)).astype(np.float32)
+    sc[3, :9000:3] = 2.5                             # a third of a short row ties
+    sc[3, 5] = 7.0
+    sc[5] = np.round(sc[5] * 4) / 4                  # coarse values: many ties at the cut
+    nv = np.array([50000, 16384, 16385, 9000, 700, 30000, 513, 0], np.int32)
+    out = torch.empty((R, 512), dtype=torch.int32, device="cuda")
+    csa.csa_topk(R, torch.from_numpy(sc).cuda(), ld, torch.from_numpy(nv).cuda(), ld, 512, out)
+    got = out.cpu().numpy()
+    for r in range(R):
+        assert np.array_equal(got[r], oracle.topk_row(sc[r], int(nv[r]))), r
+
+
 # --------------------------------------------------------------- attention
 @pytest.mark.parametrize("H,ctx,rows", [(16, [1, 2, 100, 700, 1025, 3000], 1), (64, [300, 2100], 1),
                                         (32, [1500, 2000], 6)])
