@@ -102,6 +102,7 @@ struct ScoreSmem {
   uint64_t qfull[2], qempty[2], qready[2];
   uint64_t drain[kGroups];
   int32_t q_last[2];                           // latest segment whose q was loaded into each buffer
+  int32_t q_next;                              // the segment whose q load goes out next
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -378,6 +379,22 @@ __device__ __forceinline__ bool producer_wait(uint64_t* bar, uint32_t parity, Sc
   return true;
 }
 
+// A producer's bounded wait for its turn to load segment ord's q image.
+__device__ __forceinline__ bool producer_wait_turn(const int32_t* next, int ord, ScoreSmem& sm, const ScoreArgs& a) {
+  const volatile int32_t* v = next;
+  if (*v == ord) return true;
+  const long long t0 = clock64();
+  while (*v != ord) {
+    __nanosleep(64);
+    if (clock64() - t0 > a.wait_budget || *reinterpret_cast<volatile int32_t*>(&sm.abort_flag)) {
+      raise_flag(a.status, CSA_FLAG_TIMEOUT);
+      atomicExch(&sm.abort_flag, 1);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ bool aborted(const ScoreSmem& sm) {
   return *reinterpret_cast<const volatile int32_t*>(&sm.abort_flag) != 0;
 }
@@ -410,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
     }
     for (int g = 0; g < kGroups; ++g) mbar_init(&sm.drain[g], 1);
     sm.q_last[0] = sm.q_last[1] = -1;
+    sm.q_next = 0;
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -498,12 +516,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score(ScoreArgs a, uint8_
           if (first) {
             const Seg sg = sm.segs[e.seg];
             const int par = ord & 1;
+            // The q loads go out in segment order (segment ord - 1's first,
+            // whichever producer has it), so the release of buffer par that this
+            // load waits for is at most one phase ahead of the barrier: a parity
+            // wait cannot tell phase k from phase k - 2.  The producer of ord - 1
+            // never waits on this one: every item before this one is issued.
+            if (!producer_wait_turn(&sm.q_next, ord, sm, a)) break;
             if (ord >= 2 && !producer_wait(&sm.qempty[par], ((ord >> 1) - 1) & 1, sm, a)) break;
             const uint32_t bytes_d = (uint32_t)(sg.nrows * Hp * 64), bytes_s = (uint32_t)(sg.nrows * Hp * 4);
             mbar_expect_tx(&sm.qfull[par], bytes_d + bytes_s);
             bulk_load(sm.qdata[par], W.qimg + (size_t)sg.r0 * Hp * 64, bytes_d, &sm.qfull[par]);
             bulk_load(sm.sfb_raw[par], W.qsf + (size_t)sg.r0 * Hp * 4, bytes_s, &sm.qfull[par]);
             sm.q_last[par] = ord;                    // loads into one buffer are ordered by qempty
+            *reinterpret_cast<volatile int32_t*>(&sm.q_next) = ord + 1;
           }
           const int s = it % kStages, use = it / kStages;
           if (use > 0 && !producer_wait(&sm.empty[s], (use - 1) & 1, sm, a)) break;

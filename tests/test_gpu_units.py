@@ -137,6 +137,23 @@ def test_index_score_matches_oracle(Hi, rows):
     _check_scores(wl, scores.cpu().numpy(), ld, Hi)
 
 
+@pytest.mark.parametrize("rows_per_req", [1, 2])
+def test_index_score_many_short_segments(rows_per_req):
+    """Hundreds of one- and two-tile requests: a CTA's few items span several
+    segments, whose q images go through the two buffers faster than the
+    segments' tiles are scored (the loads must go out in segment order)."""
+    cyc = [1, 2, 3, 100, 260, 700, 1025, 1600, 3000]
+    ctx = [cyc[i % len(cyc)] + rows_per_req for i in range(200)]
+    wl = W.custom("score_short", 61 + rows_per_req, ctx, [rows_per_req] * len(ctx), H=16, Hi=32)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    scores, ld, rc, flags = _score(st, s, wl, 32)
+    assert rc == 0 and flags == 0, flags
+    _check_scores(wl, scores.cpu().numpy(), ld, 32)
+
+
 def test_index_score_rows_without_entries():
     """Rows at position 0 of a pair-pooled cache see no entry: they get no
     segment, write nothing, and the rows around them score as usual (a row
@@ -327,6 +344,30 @@ def test_attention_many_rows_single_split():
     """Enough rows that each row runs in one CTA (no split merge)."""
     ctx = list(np.random.default_rng(7).integers(600, 1400, 160))
     wl = W.custom("attn1", 47, ctx, [1] * 160, H=16, Hi=16)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    st.step_decode(s)
+    rc, flags = csa.csa_check_device_status(s["ws"])
+    assert rc == 0 and flags == 0
+    ref = oracle.build_cache(wl)
+    q_idx, w, q = wl.step_queries()
+    out, lse, topk, scores = oracle.decode(ref, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale, threads=8)
+    gt = s["topk"].cpu().numpy()
+    n = wl.row_entries()
+    for r in range(wl.R):
+        parity.check_topk_row(gt[r], scores[r], int(n[r]))
+    parity.check_attention(s["out"].float().cpu().numpy(), out, s["lse"].cpu().numpy(), lse)
+
+
+def test_decode_more_rows_than_sms_mixed_lengths():
+    """More rows than SMs (the attention runs in two waves) of very different
+    lengths: rows with no entry, with one to four tiles, with partial windows;
+    the index score's CTAs then hold many short segments."""
+    base = [1, 2, 3, 100, 260, 700, 1025, 1600, 3000]
+    ctx = [base[i % len(base)] for i in range(200)]
+    wl = W.custom("attn_sk", 53, ctx, [1] * 200, H=32, Hi=32)
     st = DeviceState(wl)
     st.build_history()
     s = st.step_inputs()
