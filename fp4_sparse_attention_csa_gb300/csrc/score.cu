@@ -353,14 +353,16 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sc
   return false;
 }
 
-// Whole-warp wait: lane 0 waits, the warp then agrees on the outcome, so a
-// time-out never leaves some lanes of a warp inside the loop and others out.
+// Whole-warp wait: every lane probes the barrier and the warp leaves at once
+// when all see the phase complete (the usual case on the per-tile path: one
+// probe and one vote, no hand-off from a polling lane); otherwise every lane
+// waits and the warp agrees on the outcome, so a time-out never leaves some
+// lanes of a warp inside the loop and others out.
 template <bool kPoll>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, ScoreSmem& sm, const ScoreArgs& a) {
-  int ok = 1;
-  if (lane_id() == 0) ok = wait_or_abort<kPoll>(bar, parity, sm, a) ? 1 : 0;
-  __syncwarp();
-  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+  if (__all_sync(0xFFFFFFFFu, mbar_try_wait_poll(bar, parity))) return true;
+  const int ok = wait_or_abort<kPoll>(bar, parity, sm, a) ? 1 : 0;
+  return __all_sync(0xFFFFFFFFu, ok) != 0;
 }
 
 // A producer's wait for a free stage: the pipeline is usually full, so it
