@@ -106,6 +106,16 @@ __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
   const int t = blockIdx.x * kWarps + warp_id();
   if (t >= a.total_tokens) return;
   const int lane = lane_id();
+  // The token's rows, and the previous token's (its pair partner when both are
+  // in this call), go out before anything that waits on the request lookup:
+  // they depend on t alone.
+  float x[16], y[4], xq[16], yq[4];
+  load_bf16x16(a.kv_in + (size_t)t * D + lane * 16, x);
+  load_bf16x4(a.idx_in + (size_t)t * DI + lane * 4, y);
+  if (a.P == 2 && t > 0) {
+    load_bf16x16(a.kv_in + (size_t)(t - 1) * D + lane * 16, xq);
+    load_bf16x4(a.idx_in + (size_t)(t - 1) * DI + lane * 4, yq);
+  }
 
   // request of token t: the largest b with tok_off[b] <= t
   int lo = 0, hi = a.num_requests - 1;
@@ -128,9 +138,6 @@ __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
     if (lane == 0) raise_flag(a.status, CSA_FLAG_APPEND);
     return;
   }
-
-  float x[16];
-  load_bf16x16(a.kv_in + (size_t)t * D + lane * 16, x);
 
   // ---- FP8 window slot of this token: scale = amax / 448, codes = E4M3(x / scale).
   // Only the last win_cap tokens of the request in this call are written: an
@@ -157,23 +164,16 @@ __global__ void __launch_bounds__(kWarps * 32) k_append(AppendArgs a) {
   // ---- cache entry completed by this token
   if (p % a.P == a.P - 1) {
     const int e = p / a.P;
-    float y[4];
-    load_bf16x4(a.idx_in + (size_t)t * DI + lane * 4, y);
     if (a.P == 2) {
-      const uint16_t* pkv = (j == 0) ? a.pending + (size_t)b * (D + DI) : a.kv_in + (size_t)(t - 1) * D;
-      const uint16_t* pix = (j == 0) ? a.pending + (size_t)b * (D + DI) + D : a.idx_in + (size_t)(t - 1) * DI;
-      float xp[16], yp[4];
+      // the pair partner: the request's pending token, or the previous token
       if (j == 0) {
-        load_bf16x16<false>(pkv + lane * 16, xp);
-        load_bf16x4<false>(pix + lane * 4, yp);
-      } else {
-        load_bf16x16(pkv + lane * 16, xp);
-        load_bf16x4(pix + lane * 4, yp);
+        load_bf16x16<false>(a.pending + (size_t)b * (D + DI) + lane * 16, xq);
+        load_bf16x4<false>(a.pending + (size_t)b * (D + DI) + D + lane * 4, yq);
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = (xp[i] + x[i]) * 0.5f;
+      for (int i = 0; i < 16; ++i) x[i] = (xq[i] + x[i]) * 0.5f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) y[i] = (yp[i] + y[i]) * 0.5f;
+      for (int i = 0; i < 4; ++i) y[i] = (yq[i] + y[i]) * 0.5f;
     }
     // ---- compressor steps on the pooled entry (csa_append_compress)
     bool write_entry = true;
