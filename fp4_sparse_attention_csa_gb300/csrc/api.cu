@@ -56,14 +56,18 @@ csa_status_t check_rows(const csa_rows_t* r, const csa_cache_t* c) {
 
 size_t scores_ld(int32_t max_entries) { return align_up((size_t)(max_entries > 0 ? max_entries : 1), 64); }
 
+// Head count the attention workspace is sized for: the call's, or the largest.
+int32_t ws_heads(int32_t n_heads) { return n_heads > 0 && n_heads <= CSA_MAX_HEADS ? n_heads : CSA_MAX_HEADS; }
+
 struct DecodeLayout {
-  size_t scores, topk, end;
+  size_t scores, topk, tail, end;
 };
-DecodeLayout decode_layout(int32_t R, int32_t max_entries) {
+DecodeLayout decode_layout(int32_t R, int32_t max_entries, int32_t n_heads) {
   DecodeLayout L;
   L.scores = align_up(score_ws_bytes(R, CSA_MAX_IDX_HEADS));
   L.topk = align_up(L.scores + sizeof(float) * (size_t)R * scores_ld(max_entries));
-  L.end = align_up(L.topk + sizeof(int32_t) * (size_t)R * CSA_TOPK);
+  L.tail = align_up(L.topk + sizeof(int32_t) * (size_t)R * CSA_TOPK);
+  L.end = align_up(L.tail + attn_tail_ws_bytes(R, ws_heads(n_heads), num_sms()));
   return L;
 }
 
@@ -111,9 +115,12 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
   return from_cuda(launch_index_score(a, num_sms(), prep_order, stream));
 }
 
+// ws_bytes: the workspace's size; the bytes from tail_off on hold the tail
+// split's partials when they fit (otherwise the rows run unsplit).
 csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                       const int32_t* topk, int32_t H, const void* q, float softmax_scale, void* out, float* lse,
-                      const csa_opts_t* opts, void* ws, Order order, cudaStream_t stream) {
+                      const csa_opts_t* opts, void* ws, size_t tail_off, size_t ws_bytes, Order order,
+                      cudaStream_t stream) {
   AttnArgs a;
   a.plan_in = opts ? opts->plan_in : nullptr;
   a.plan_out = opts ? opts->plan_out : nullptr;
@@ -139,8 +146,11 @@ csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, cons
   a.softmax_scale = softmax_scale;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
-  a.splits = attn_choose_splits(rows->num_rows, num_sms());
+  const int sms = num_sms();
+  a.splits = attn_choose_splits(rows->num_rows, sms);
   a.status = static_cast<uint32_t*>(ws);
+  attn_tail_setup(a, ws_bytes > tail_off ? static_cast<uint8_t*>(ws) + tail_off : nullptr,
+                  ws_bytes > tail_off ? ws_bytes - tail_off : 0, sms);
   return from_cuda(launch_sparse_attn(a, order, stream));
 }
 
@@ -204,8 +214,9 @@ csa_status_t check_decode(const csa_cache_t* cache, const csa_window_t* window, 
   if (rows->num_rows == 0) return CSA_OK;
   if (!q_idx || !w || !q || !out || !aligned(q_idx, 16) || !aligned(q, 16) || !aligned(out, 16))
     return CSA_ERR_INVALID_ARGUMENT;
-  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries);
-  if (!ws || ws_bytes < L.end || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  // the attention's tail-split partials (past L.tail) are used when they fit
+  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries, n_heads);
+  if (!ws || ws_bytes < L.tail || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
   return CSA_OK;
 }
 
@@ -214,8 +225,8 @@ csa_status_t check_decode(const csa_cache_t* cache, const csa_window_t* window, 
 csa_status_t run_decode(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                         int32_t n_idx_heads, const void* q_idx, const float* w, int32_t n_heads, const void* q,
                         float softmax_scale, void* out, float* lse, int32_t* topk_out,
-                        const csa_opts_t* opts, void* ws, Order first, cudaStream_t stream) {
-  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries);
+                        const csa_opts_t* opts, void* ws, size_t ws_bytes, Order first, cudaStream_t stream) {
+  const DecodeLayout L = decode_layout(rows->num_rows, rows->max_entries, n_heads);
   uint8_t* base = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(base + L.scores);
   int32_t* topk = topk_out ? topk_out : reinterpret_cast<int32_t*>(base + L.topk);
@@ -236,7 +247,8 @@ csa_status_t run_decode(const csa_cache_t* cache, const csa_window_t* window, co
   if ((s = from_cuda(blocks > 0 ? launch_topk_two_level(t, blocks, Order::kChained, stream)
                                 : launch_topk(t, Order::kChained, stream))) != CSA_OK)
     return s;
-  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, opts, ws, Order::kChained, stream);
+  return run_attn(cache, window, rows, topk, n_heads, q, softmax_scale, out, lse, opts, ws, L.tail, ws_bytes,
+                  Order::kChained, stream);
 }
 
 }  // namespace
@@ -245,7 +257,6 @@ extern "C" {
 
 size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int32_t n_heads) {
   if (num_rows < 0 || max_entries < 0) return 0;
-  (void)n_heads;                     // no size depends on the head count
   switch (op) {
     case CSA_OP_APPEND:
     case CSA_OP_TOPK:
@@ -253,9 +264,9 @@ size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int
     case CSA_OP_INDEX_SCORE:
       return align_up(score_ws_bytes(num_rows, CSA_MAX_IDX_HEADS));
     case CSA_OP_SPARSE_ATTN:
-      return kStatusBytes;
+      return kStatusBytes + attn_tail_ws_bytes(num_rows, ws_heads(n_heads), num_sms());
     case CSA_OP_DECODE:
-      return decode_layout(num_rows, max_entries).end;
+      return decode_layout(num_rows, max_entries, n_heads).end;
     default:
       return 0;
   }
@@ -357,7 +368,8 @@ csa_status_t csa_sparse_attn_ex(const csa_cache_t* cache, const csa_window_t* wi
   const bool planned = opts && opts->plan_in;
   if ((!topk_idx && !planned) || !q || !out || !aligned(q, 16) || !aligned(out, 16)) return CSA_ERR_INVALID_ARGUMENT;
   if (!ws || ws_bytes < kStatusBytes || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
-  return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, opts, ws, Order::kStream,
+  return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, opts, ws, kStatusBytes, ws_bytes,
+                  Order::kStream,
                   stream);
 }
 
@@ -379,7 +391,7 @@ csa_status_t csa_decode_ex(const csa_cache_t* cache, const csa_window_t* window,
   if (opts && opts->candidate_blocks > 0 && rows->max_entries > kTwoLevelMaxEntries) return CSA_ERR_UNSUPPORTED;
   if (rows->num_rows == 0) return s;
   return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, opts,
-                    ws, Order::kStream, stream);
+                    ws, ws_bytes, Order::kStream, stream);
 }
 
 csa_status_t csa_step(const csa_cache_t* cache, const csa_window_t* window, const int32_t* pos0,
@@ -413,7 +425,7 @@ csa_status_t csa_step_ex(const csa_cache_t* cache, const csa_window_t* window, c
   // touch, and it waits for the append before it exits.  Without one it is the
   // call's first kernel.
   return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, opts,
-                    ws, total_tokens > 0 ? Order::kChained : Order::kStream, stream);
+                    ws, ws_bytes, total_tokens > 0 ? Order::kChained : Order::kStream, stream);
 }
 
 csa_status_t csa_check_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out) {

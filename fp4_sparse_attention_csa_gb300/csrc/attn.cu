@@ -53,6 +53,7 @@ constexpr int kTileKeys = 128;
 constexpr int kMainTiles = TOPK / kTileKeys;      // 4
 constexpr int kMaxTiles = kMainTiles + 1;         // 4 global + 1 window
 static_assert(TOPK == kThreads, "one selected entry per thread in the set-up lookup");
+static_assert(D == kThreads, "one output dimension per thread in the merges");
 constexpr int kMaxH = CSA_MAX_HEADS;             // 64
 constexpr float kLog2e = 1.4426950408889634f;
 // The running max used for exp2 moves only when a tile's max exceeds it by
@@ -74,6 +75,7 @@ struct AttnSmem {
   float l_run[kMaxH];
   float m_out[kMaxH], l_out[kMaxH];    // a split's final (m, l), read by the cluster's merge
   float inv_l[kMaxH];
+  uint32_t tail_last;                  // a tail row's CTA: it arrived last and merges the row
   uint64_t s_bar, pv_bar;
   uint32_t tmem_base;
 };
@@ -401,7 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
-  const int r = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
+  // row and split: rows before tail_row0 (all rows without a tail split) take
+  // a.splits CTAs each; a tail row takes tail_splits CTAs that merge through
+  // the workspace
+  const bool tail = a.tail_splits > 1 && (int)blockIdx.x >= a.tail_row0;
+  const int kt = (int)blockIdx.x - a.tail_row0;          // a tail CTA's partial
+  const int splits = tail ? a.tail_splits : a.splits;
+  const int r = tail ? a.tail_row0 + kt / splits : (int)blockIdx.x / splits;
+  const int split = tail ? kt % splits : (int)blockIdx.x % splits;
 
   const int b = __ldg(a.row_req + r);
   const int pos = __ldg(a.row_pos + r);
@@ -414,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const int gtiles = (nsel + kTileKeys - 1) / kTileKeys;
   const int hw = ((a.win_codes != nullptr) && row_ok) ? 1 : 0;   // window tile present
   const int ntiles = gtiles + hw;
-  const int tper = (ntiles + a.splits - 1) / a.splits;
+  const int tper = (ntiles + splits - 1) / splits;
   const int t_beg = min(ntiles, split * tper), t_end = min(ntiles, t_beg + tper);
   const bool win_here = hw && t_beg == 0 && t_end > 0;
   const int m_beg = max(t_beg - hw, 0), m_end = max(t_end - hw, 0);   // main tiles [m_beg, m_end)
@@ -753,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const float* m_fin = sm.m_fin;
   const int d = 128 * hsel + 32 * q4 + lane;
   const uint32_t obase = tO + lane_off + hsel * 64;
-  if (a.splits == 1) {
+  if (splits == 1) {
     // O[h][d] = O^T[d][h] / l[h] as bf16, staged in sm.k (free after the last PV)
     if (tid < H) {
       const float l = sm.l_run[tid];
@@ -783,6 +792,84 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
     if (a.lse && tid < H) {
       const float l = sm.l_run[tid];
       a.lse[(size_t)r * H + tid] = (have && l > 0.0f) ? (m_fin[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+  } else if (tail) {
+    // a tail row's split: its unnormalised O [H][512] and (m, l) go to the
+    // workspace; the row's CTA that arrives last merges the row's partials by
+    // log-sum-exp (the weights of the cluster merge below) and writes the row
+    const int S = splits;
+    const int ntail = (int)gridDim.x - a.tail_row0;
+    float* pm = a.part + (size_t)ntail * H * D;            // [ntail][2][H]: m, then l
+    {
+      float* po = a.part + (size_t)kt * H * D;
+      for (int h0 = 0; h0 < H; h0 += 16) {
+        uint32_t v[16];
+        if (have) {
+          tmem_ld16(obase + h0, v);
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) __stcg(po + (size_t)(h0 + i) * D + d, have ? __uint_as_float(v[i]) : 0.0f);
+      }
+      if (tid < H) {
+        __stcg(pm + (size_t)kt * 2 * H + tid, have ? m_fin[tid] : -INFINITY);
+        __stcg(pm + (size_t)kt * 2 * H + H + tid, have ? sm.l_run[tid] : 0.0f);
+      }
+    }
+    __threadfence();                               // this CTA's partial is visible device-wide
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t prev = atomicAdd(a.row_done + (r - a.tail_row0), 1u);
+      sm.tail_last = prev == (uint32_t)(S - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (sm.tail_last) {
+      __threadfence();
+      const int q0 = kt - split;                   // the row's first partial
+      float* wq = reinterpret_cast<float*>(sm.p);  // [S][H] merge weights (P is free after the last PV)
+      if (tid < H) {
+        float mq[kMaxTiles], lq[kMaxTiles];
+#pragma unroll
+        for (int q = 0; q < kMaxTiles; ++q) {
+          mq[q] = q < S ? __ldcg(pm + (size_t)(q0 + q) * 2 * H + tid) : -INFINITY;
+          lq[q] = q < S ? __ldcg(pm + (size_t)(q0 + q) * 2 * H + H + tid) : 0.0f;
+        }
+        float M = -INFINITY, L = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kMaxTiles; ++q) M = fmaxf(M, mq[q]);
+#pragma unroll
+        for (int q = 0; q < kMaxTiles; ++q) {
+          mq[q] = mq[q] == -INFINITY ? 0.0f : exp2f(mq[q] - M);
+          L += mq[q] * lq[q];
+        }
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll
+        for (int q = 0; q < kMaxTiles; ++q)
+          if (q < S) wq[q * H + tid] = mq[q] * inv;
+        if (a.lse) a.lse[(size_t)r * H + tid] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+      }
+      __syncthreads();
+      // O[h][d] = sum_q w_q[h] O_q[h][d], thread tid: dim tid (D == kThreads)
+      const float* pq = a.part + (size_t)q0 * H * D + tid;
+      constexpr int kHG = 16;                      // heads whose loads go out together
+      for (int h0 = 0; h0 < H; h0 += kHG) {
+        float v[kHG][kMaxTiles];
+#pragma unroll
+        for (int u = 0; u < kHG; ++u)
+#pragma unroll
+          for (int q = 0; q < kMaxTiles; ++q)
+            v[u][q] = q < S ? __ldcg(pq + (size_t)q * H * D + (size_t)(h0 + u) * D) : 0.0f;
+#pragma unroll
+        for (int u = 0; u < kHG; ++u) {
+          float acc = 0.0f;
+#pragma unroll
+          for (int q = 0; q < kMaxTiles; ++q)
+            if (q < S) acc += wq[q * H + h0 + u] * v[u][q];
+          const __nv_bfloat16 o = __float2bfloat16_rn(acc);
+          a.out[((size_t)r * H + h0 + u) * D + tid] = *reinterpret_cast<const uint16_t*>(&o);
+        }
+      }
+      if (tid == 0) a.row_done[r - a.tail_row0] = 0u;   // zero again for the next call
     }
   } else {
     // split partials, merged inside the row's cluster: O [H][512] unnormalised
@@ -913,8 +1000,11 @@ cudaError_t launch_h(const AttnArgs& args, Order order, cudaStream_t stream) {
   // fewer splits where the rows' clusters would not all be resident at once
   AttnArgs a = args;
   while (a.splits > 1 && a.num_rows > clusters_resident<H>(a.splits, smem)) --a.splits;
-  if (a.splits == 1)
-    return launch_kernel(order, k_sparse_attn<H>, dim3(a.num_rows), dim3(kThreads), smem, stream, a);
+  if (a.splits > 1) a.tail_splits = 1;
+  if (a.splits == 1) {
+    const int grid = a.tail_splits > 1 ? a.tail_row0 + (a.num_rows - a.tail_row0) * a.tail_splits : a.num_rows;
+    return launch_kernel(order, k_sparse_attn<H>, dim3(grid), dim3(kThreads), smem, stream, a);
+  }
   // a row's splits form one cluster, which merges their partials
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_rows * a.splits, 1, 1);
@@ -937,6 +1027,49 @@ int32_t attn_choose_splits(int32_t num_rows, int num_sms) {
   if (num_rows <= 0) return 1;
   int s = num_sms / num_rows;
   return s < 1 ? 1 : (s > kMaxTiles ? kMaxTiles : s);
+}
+
+int32_t attn_tail_plan(int32_t num_rows, int num_sms, int32_t* tail_row0) {
+  *tail_row0 = num_rows;
+  if (num_sms <= 0 || num_rows <= num_sms) return 1;
+  const int rem = num_rows % num_sms;
+  if (rem == 0) return 1;
+  int s = num_sms / rem;
+  s = s > kMaxTiles ? kMaxTiles : s;
+  if (s < 2) return 1;
+  *tail_row0 = num_rows - rem;
+  return s;
+}
+
+namespace {
+constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+// The tail partials' bytes: O of every tail CTA, then its (m, l).
+size_t tail_part_bytes(size_t ctas, int32_t H) {
+  return align256(ctas * (size_t)H * D * sizeof(float) + ctas * 2 * (size_t)H * sizeof(float));
+}
+}  // namespace
+
+size_t attn_tail_ws_bytes(int32_t num_rows, int32_t H, int num_sms) {
+  int32_t row0 = 0;
+  const int32_t s = attn_tail_plan(num_rows, num_sms, &row0);
+  if (s < 2) return 0;
+  return tail_part_bytes((size_t)(num_rows - row0) * s, H) + align256((size_t)(num_rows - row0) * sizeof(uint32_t));
+}
+
+void attn_tail_setup(AttnArgs& a, void* base, size_t bytes, int num_sms) {
+  a.tail_row0 = a.num_rows;
+  a.tail_splits = 1;
+  a.part = nullptr;
+  a.row_done = nullptr;
+  if (a.splits != 1 || base == nullptr) return;
+  int32_t row0 = 0;
+  const int32_t s = attn_tail_plan(a.num_rows, num_sms, &row0);
+  if (s < 2 || bytes < attn_tail_ws_bytes(a.num_rows, a.H, num_sms)) return;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  a.tail_row0 = row0;
+  a.tail_splits = s;
+  a.part = reinterpret_cast<float*>(p);
+  a.row_done = reinterpret_cast<uint32_t*>(p + tail_part_bytes((size_t)(a.num_rows - row0) * s, a.H));
 }
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, Order order, cudaStream_t stream) {

@@ -149,9 +149,15 @@ typedef struct {
 } csa_rows_t;
 
 /* Workspace sizing: op = one of the CSA_OP_* values; bytes for num_rows rows
- * of at most max_entries entries each.  n_heads is part of the signature so a
- * caller need not change when a size comes to depend on it; none does now
- * (attention's split partials are merged in shared memory).  0 = bad op. */
+ * of at most max_entries entries each and n_heads attention heads.  For
+ * CSA_OP_SPARSE_ATTN and CSA_OP_DECODE the size also depends on the current
+ * device's SM count: with more rows than SMs, the rows of the last wave of one
+ * CTA per SM are split over several CTAs that merge through the workspace
+ * (see csa_sparse_attn); a workspace without that room (at least the size
+ * computed for a device with num_rows or more SMs) runs every row whole.
+ * A workspace is zero-filled before its first use: its status word and the
+ * attention's arrival counters start at zero, and every call leaves the
+ * counters at zero.  0 = bad op. */
 enum { CSA_OP_APPEND = 0, CSA_OP_INDEX_SCORE = 1, CSA_OP_TOPK = 2,
        CSA_OP_SPARSE_ATTN = 3, CSA_OP_DECODE = 4 };
 CSA_API size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int32_t n_heads);
@@ -203,7 +209,12 @@ CSA_API csa_status_t csa_topk(int32_t num_rows, const float* scores, int32_t ld,
  * the FP8 window positions max(0,t-127)..t ([VLLM] "SWA bounded replay").
  * K = V = the shared 512-d latent (MQA).  With fewer rows than SMs a row is
  * split over key blocks; its CTAs form one thread-block cluster and merge by
- * log-sum-exp in shared memory, so ws holds only the status word.
+ * log-sum-exp in shared memory.  With more rows than SMs, when the last wave
+ * of one CTA per SM holds at most half the SMs' worth of rows, each of those
+ * rows is split over up to five CTAs that leave their partials in ws and the
+ * row's last CTA to finish merges them (same weights).  ws:
+ * csa_workspace_size(CSA_OP_SPARSE_ATTN, R, max_entries, n_heads) bytes,
+ * 256-byte aligned, at least 256.
  *  q bf16 [R, H, 512]; out bf16 [R, H, 512]; lse fp32 [R, H] (nullable). */
 CSA_API csa_status_t csa_sparse_attn(const csa_cache_t* cache, const csa_window_t* window,
                              const csa_rows_t* rows, const int32_t* topk_idx,

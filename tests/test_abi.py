@@ -124,9 +124,9 @@ def test_workspace_sizes_without_device(lib):
     assert csa.csa_workspace_size(csa.OP_TOPK, 10, 1000, 0) == 256
     assert csa.csa_workspace_size(csa.OP_INDEX_SCORE, 192, 3000, 64) >= 192 * 128 * 68
     assert csa.csa_workspace_size(99, 1, 1, 1) == 0
-    # attention keeps split partials in shared memory: the status word only,
-    # whatever the row and head counts
-    for rows, heads in [(1, 64), (4, 64), (30, 16), (128, 64)]:
+    # attention: the status word, plus the tail split's partials only when the
+    # rows exceed the device's SM count (none is known without a device)
+    for rows, heads in [(1, 64), (4, 64), (30, 16), (128, 64), (200, 64)]:
         assert csa.csa_workspace_size(csa.OP_SPARSE_ATTN, rows, 262144, heads) == 256
     # decode = the score step's workspace + the scores [R, ld] + the top-k [R, 512]
     R, n = 128, 65536

@@ -385,6 +385,49 @@ def test_decode_more_rows_than_sms_mixed_lengths():
     parity.check_attention(s["out"].float().cpu().numpy(), out, s["lse"].cpu().numpy(), lse)
 
 
+def test_attention_tail_split():
+    """Rows just past one wave of one CTA per SM: the last wave's rows are
+    split over several CTAs whose partials merge through the workspace.  The
+    output matches the oracle with and without the split (a workspace too
+    small for the partials runs every row whole), the rows before the tail are
+    bit-equal either way, and a second call on the same workspace (arrival
+    counters back at zero) gives the same bits."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    R, H = sms + 7, 64
+    base = [600, 1500, 2600, 4100]
+    ctx = [base[i % len(base)] + i for i in range(R)]
+    wl = W.custom("tail", 71, ctx, [1] * R, H=H, Hi=16, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    ref = oracle.build_cache(wl)
+    q_idx, w, q = wl.step_queries()
+    _, _, topk, _ = oracle.decode(ref, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale, threads=8)
+    tk = torch.from_numpy(topk).cuda()
+    full = csa.csa_workspace_size(csa.OP_SPARSE_ATTN, R, wl.max_entries, H)
+    assert full > 256                                    # partials for 7 rows x 5 splits
+    assert csa.csa_workspace_size(csa.OP_SPARSE_ATTN, sms, wl.max_entries, H) == 256
+    o_ref = np.zeros((R, H, 512), np.float32)
+    l_ref = np.zeros((R, H), np.float32)
+    for r in range(R):
+        o_ref[r], l_ref[r] = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], topk[r], q[r],
+                                                  wl.softmax_scale)
+    outs = []
+    ws_full = torch.zeros(full, dtype=torch.uint8, device="cuda")
+    for ws in (ws_full, torch.zeros(256, dtype=torch.uint8, device="cuda"), ws_full):
+        out = torch.full((R, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((R, H), float("nan"), device="cuda")
+        csa.csa_sparse_attn(st.cache, st.window, s["rows"], tk, H, s["q"], wl.softmax_scale, out, lse, ws)
+        rc, flags = csa.csa_check_device_status(ws)
+        assert rc == 0 and flags == 0, flags
+        parity.check_attention(out.float().cpu().numpy(), o_ref, lse.cpu().numpy(), l_ref)
+        outs.append((out.view(torch.int16).cpu().numpy(), lse.cpu().numpy()))
+    assert np.array_equal(outs[0][0][:sms], outs[1][0][:sms])
+    assert np.array_equal(outs[0][1][:sms], outs[1][1][:sms])
+    assert np.array_equal(outs[0][0], outs[2][0]) and np.array_equal(outs[0][1], outs[2][1])
+
+
 # ------------------------------------------------------------------ decode
 @pytest.mark.parametrize("H,Hi,rows", [(16, 16, 1), (64, 64, 6), (32, 32, 2), (64, 128, 2), (16, 96, 1)])
 def test_decode_end_to_end(H, Hi, rows):
