@@ -385,7 +385,8 @@ def test_decode_more_rows_than_sms_mixed_lengths():
     parity.check_attention(s["out"].float().cpu().numpy(), out, s["lse"].cpu().numpy(), lse)
 
 
-def test_attention_tail_split():
+@pytest.mark.parametrize("H", [64, 16])
+def test_attention_tail_split(H):
     """Rows just past one wave of one CTA per SM: the last wave's rows are
     split over several CTAs whose partials merge through the workspace.  The
     output matches the oracle with and without the split (a workspace too
@@ -393,7 +394,7 @@ def test_attention_tail_split():
     bit-equal either way, and a second call on the same workspace (arrival
     counters back at zero) gives the same bits."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    R, H = sms + 7, 64
+    R = sms + 7
     base = [600, 1500, 2600, 4100]
     ctx = [base[i % len(base)] + i for i in range(R)]
     wl = W.custom("tail", 71, ctx, [1] * R, H=H, Hi=16, shuffle=True)
