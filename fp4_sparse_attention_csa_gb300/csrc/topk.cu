@@ -518,6 +518,11 @@ __device__ __forceinline__ void mark(RowSmem& sm, int idx) {
 // The CTAs that share a row: a thread-block cluster of C (C > 1), or this CTA
 // alone (C == 1), whose barrier is then the CTA's own and whose "remote" shared
 // memory is its own.
+template <int N>
+struct IntConst {
+  static constexpr int value = N;
+};
+
 template <int C>
 struct RowGroup {
   __device__ __forceinline__ void sync() const {
@@ -675,14 +680,23 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
       const float tbf = (float)tb;
       // a thread's up-to-16 values: count its entries above tb and in tb, one
       // warp scan each, one atomic per list per warp, then the writes
-      auto collect = [&](const float* v, const int* idx, int cnt) {
-        uint32_t gtm = 0, tiem = 0;
-        for (int j = 0; j < cnt; ++j) {
-          if (idx[j] < 0) continue;
-          const int b = bin_of(v[j]);
-          if (b > tb) gtm |= 1u << j;
-          else if (b == tb) tiem |= 1u << j;
-        }
+      // a value's class by the same arithmetic as bin_of: its bin above tb
+      // (floor(x) >= tb + 1, and tb not the last bin), or equal to tb; a NaN
+      // value's bin is 0
+      const float tbf1 = (float)(tb + 1);
+      const bool gt_possible = tb < kRowBins - 1;
+      auto classify = [&](float v, bool valid, uint32_t bit, uint32_t& gtm, uint32_t& tiem) {
+        const float x = (fold(v) - vmin) * scale;
+        if (!valid) return;
+        if (gt_possible && x >= tbf1) gtm |= bit;
+        else if (tb == 0 || x >= tbf) tiem |= bit;
+      };
+      // a thread's candidates (bit j: its value j, entry ibase + (j / 4) * 4 *
+      // kThreads + j % 4): one warp scan per list, one atomic per list per warp,
+      // then the writes -- the indices above the cut bin by their set bits, the
+      // cut bin's keys and indices (few) only in warps that hold some
+      auto collect = [&](auto cnt_c, uint32_t gtm, uint32_t tiem, const float* v, int ibase) {
+        constexpr int kCnt = decltype(cnt_c)::value;
         const uint32_t ng = (uint32_t)__popc(gtm), nt = (uint32_t)__popc(tiem);
         uint32_t ig = ng, it = nt;                  // inclusive warp scans
 #pragma unroll
@@ -697,41 +711,43 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
         }
         bg = __shfl_sync(0xFFFFFFFFu, bg, 31) + ig - ng;
         bt = __shfl_sync(0xFFFFFFFFu, bt, 31) + it - nt;
-        for (int j = 0; j < cnt; ++j) {
-          if (gtm & (1u << j)) sm.gt_idx[bg++] = lo + idx[j];
-          if (tiem & (1u << j)) {
-            sm.tie_key[bt] = score_key(fold(v[j]));
-            sm.tie_idx[bt] = lo + idx[j];
-            ++bt;
-          }
+        for (uint32_t m = gtm; m != 0u; m &= m - 1u) {
+          const int j = __ffs(m) - 1;
+          sm.gt_idx[bg++] = lo + ibase + (j >> 2) * (4 * kThreads) + (j & 3);
+        }
+        if (__any_sync(0xFFFFFFFFu, tiem != 0u)) {
+#pragma unroll
+          for (int j = 0; j < kCnt; ++j)
+            if (tiem & (1u << j)) {
+              sm.tie_key[bt] = score_key(fold(v[j]));
+              sm.tie_idx[bt] = lo + ibase + (j >> 2) * (4 * kThreads) + (j & 3);
+              ++bt;
+            }
         }
       };
       const int n4r = (n4 + 4 * kThreads - 1) / (4 * kThreads) * (4 * kThreads);   // warp-uniform trip count
       for (int base4 = 0; base4 < n4r; base4 += 4 * kThreads) {
         float v[16];
-        int idx[16];
-        bool any = false;
+        uint32_t gtm = 0u, tiem = 0u;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int i = base4 + tid + j * kThreads;
-          const float4 x = i < n4 ? __ldg(sl4 + i) : make_float4(vmin, vmin, vmin, vmin);
+          const bool valid = i < n4;
+          const float4 x = valid ? __ldg(sl4 + i) : make_float4(vmin, vmin, vmin, vmin);
           v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            idx[4 * j + c] = i < n4 ? 4 * i + c : -1;
-            // (v - vmin) * scale >= tb exactly when bin_of(v) >= tb, for tb >= 1
-            any |= (v[4 * j + c] - vmin) * scale >= tbf;
-          }
+          for (int c = 0; c < 4; ++c) classify(v[4 * j + c], valid, 1u << (4 * j + c), gtm, tiem);
         }
-        if (tb == 0) any = true;
-        if (!__any_sync(0xFFFFFFFFu, any)) continue;
-        collect(v, idx, 16);
+        if (!__any_sync(0xFFFFFFFFu, (gtm | tiem) != 0u)) continue;
+        collect(IntConst<16>(), gtm, tiem, v, 4 * (base4 + tid));
       }
       if (tid < 32) {                              // the slice's last (len mod 4) entries
         const int i = 4 * n4 + lane;
-        float v1[1] = {i < len ? __ldg(sl + i) : vmin};
-        int i1[1] = {i < len ? i : -1};
-        collect(v1, i1, 1);
+        const bool valid = i < len;
+        float v1[1] = {valid ? __ldg(sl + i) : vmin};
+        uint32_t gtm = 0u, tiem = 0u;
+        classify(v1[0], valid, 1u, gtm, tiem);
+        collect(IntConst<1>(), gtm, tiem, v1, i);
       }
       grp.sync();                              // every CTA's counts are final
       // ---- CTA q's lists go to CTA 0's at the offsets of CTAs 0..q-1 ---------------
@@ -871,7 +887,6 @@ constexpr int kPackLong = 16384;
 
 __global__ void __launch_bounds__(kThreads) k_topk_packed(TopkArgs a) {
   pdl_trigger();
-  pdl_wait();                    // the scores come from the previous kernel
   extern __shared__ __align__(16) uint8_t smem[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
   const int tid = threadIdx.x;
@@ -903,6 +918,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_packed(TopkArgs a) {
   __syncthreads();
   const uint32_t row = sm.sel_bin;
   __syncthreads();               // every thread has the row before sm is reused
+  // the assignment reads only the call's inputs (row lengths); the scores come
+  // from the previous kernel
+  pdl_wait();
   if (want_long) topk_row<kPackC>(a, sm, (int)row, kq);      // the whole cluster: c < n_long
   else if (row != 0xFFFFFFFFu) topk_row<1>(a, sm, (int)row, 0);
 }
