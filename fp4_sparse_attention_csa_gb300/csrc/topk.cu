@@ -536,15 +536,21 @@ struct RowGroup {
   }
 };
 
-// Row r's top-512 by its C CTAs; this is CTA kq of them.
+// The entries row r sees, as given (n_valid) or from its position: a call
+// input, read before the wait for the scores.
+__device__ __forceinline__ int row_n(const TopkArgs& a, int r) {
+  return a.n_valid ? __ldg(a.n_valid + r) : (__ldg(a.row_pos + r) + 1) / a.P;
+}
+
+// Row r's top-512 by its C CTAs; this is CTA kq of them; n_row = row_n(a, r).
 template <int C>                   // CTAs per row: 1, 2, 4 or 8
-__device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, int kq) {
+__device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, int kq, int n_row) {
   const RowGroup<C> grp;
   const int tid = threadIdx.x, lane = lane_id();
   const float* row = a.scores + (size_t)r * a.ld;
   int32_t* out = a.out + (size_t)r * TOPK;
 
-  int n = a.n_valid ? __ldg(a.n_valid + r) : (__ldg(a.row_pos + r) + 1) / a.P;
+  int n = n_row;
   if (n < 0 || n > a.max_n) {
     if (tid == 0 && kq == 0) raise_flag(a.status, CSA_FLAG_ROW_INVALID);
     n = n < 0 ? 0 : a.max_n;
@@ -869,11 +875,13 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
 template <int C>                   // CTAs per row: 1, 2, 4 or 8
 __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
   pdl_trigger();
+  const int r = (int)blockIdx.x / C;
+  const int n_row = row_n(a, r);
   pdl_wait();                    // the scores come from the previous kernel
   extern __shared__ __align__(16) uint8_t smem[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
   const int kq = C == 1 ? 0 : (int)cg::this_cluster().block_rank();
-  topk_row<C>(a, sm, (int)blockIdx.x / C, kq);
+  topk_row<C>(a, sm, r, kq, n_row);
 }
 
 // Rows of very different lengths (up to kPackC * kPackLong entries): clusters
@@ -892,7 +900,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_packed(TopkArgs a) {
   const int tid = threadIdx.x;
   const int c = (int)blockIdx.x / kPackC, kq = (int)cg::this_cluster().block_rank();
   auto row_len = [&](int r) {
-    int n = a.n_valid ? __ldg(a.n_valid + r) : (__ldg(a.row_pos + r) + 1) / a.P;
+    const int n = row_n(a, r);
     return n < 0 ? 0 : (n > a.max_n ? a.max_n : n);
   };
   // the long rows come first: how many there are
@@ -918,11 +926,12 @@ __global__ void __launch_bounds__(kThreads) k_topk_packed(TopkArgs a) {
   __syncthreads();
   const uint32_t row = sm.sel_bin;
   __syncthreads();               // every thread has the row before sm is reused
+  const int n_row = row != 0xFFFFFFFFu ? row_n(a, (int)row) : 0;
   // the assignment reads only the call's inputs (row lengths); the scores come
   // from the previous kernel
   pdl_wait();
-  if (want_long) topk_row<kPackC>(a, sm, (int)row, kq);      // the whole cluster: c < n_long
-  else if (row != 0xFFFFFFFFu) topk_row<1>(a, sm, (int)row, 0);
+  if (want_long) topk_row<kPackC>(a, sm, (int)row, kq, n_row);      // the whole cluster: c < n_long
+  else if (row != 0xFFFFFFFFu) topk_row<1>(a, sm, (int)row, 0, n_row);
 }
 
 // ---------------------------------------------------------------------------
