@@ -398,19 +398,29 @@ constexpr int kTieCap = 4096;
 constexpr int kPairwiseMax = 256;   // cut bins up to this size are ranked pairwise
 constexpr int kRowCluster = 8;
 
-struct alignas(16) RowSmem {
+// Shared memory of a row's CTA for rows of up to kMaxN entries, a cut bin of
+// up to kTies entries, and (kCache > 0) this CTA's slice of the row staged
+// once by a bulk copy and read from there by all three passes.
+template <int kMaxN, int kTies, int kCache>
+struct alignas(16) RowSmemT {
+  static constexpr int kTieCapacity = kTies;
+  static constexpr int kCacheFloats = kCache;
   uint32_t hist[kRowBins];         // value histogram; the radix passes reuse it
-  uint32_t bitmap[kRowMax / 32];   // CTA 0: selected indices of the row
-  uint32_t tie_key[kTieCap];       // CTA 0: the cut bin's entries (unordered)
-  int32_t tie_idx[kTieCap];
+  uint32_t bitmap[kMaxN / 32];     // CTA 0: selected indices of the row
+  uint32_t tie_key[kTies];         // CTA 0: the cut bin's entries (unordered)
+  int32_t tie_idx[kTies];
   int32_t gt_idx[TOPK];            // the entries above the cut bin (unordered)
   uint32_t warp_a[kWarps], warp_b[kWarps];
   uint32_t gt_cnt, tie_cnt;        // this CTA's list lengths
   uint32_t sel_bin, sel_need, sel_tie;
   float fmin, fmax;
+  uint64_t cache_bar;              // the slice's bulk copy
+  alignas(16) float cache[kCache > 0 ? kCache : 4];
 };
+using RowSmem = RowSmemT<kRowMax, kTieCap, 0>;
 
-__device__ __forceinline__ void block_minmax(float& vmin, float& vmax, RowSmem& sm) {
+template <typename SM>
+__device__ __forceinline__ void block_minmax(float& vmin, float& vmax, SM& sm) {
   const int lane = lane_id(), warp = warp_id();
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -436,7 +446,8 @@ __device__ __forceinline__ void block_minmax(float& vmin, float& vmax, RowSmem& 
 
 // Block-wide exclusive scan of one count per thread; returns the thread's
 // offset and the block total (uses warp_a).
-__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, RowSmem& sm) {
+template <typename SM>
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, SM& sm) {
   const int lane = lane_id(), warp = warp_id();
   uint32_t x = v;
 #pragma unroll
@@ -460,8 +471,8 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* total, RowS
 // Block-wide radix select (11/11/10 bits) of the need-th largest key among the
 // m keys key_at(i) with valid(i): the key T and how many of the keys equal to T
 // are taken (need minus the keys above T).  Uses hist, warp_a, sel_bin, sel_need.
-template <typename K, typename V>
-__device__ void row_radix(K key_at, V valid, int m, uint32_t need, RowSmem& sm, uint32_t* T_out, uint32_t* take_out) {
+template <typename K, typename V, typename SM>
+__device__ void row_radix(K key_at, V valid, int m, uint32_t need, SM& sm, uint32_t* T_out, uint32_t* take_out) {
   const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
   uint32_t prefix = 0, mask = 0, rem = need;
   const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
@@ -511,7 +522,8 @@ __device__ void row_radix(K key_at, V valid, int m, uint32_t need, RowSmem& sm, 
   *take_out = rem;
 }
 
-__device__ __forceinline__ void mark(RowSmem& sm, int idx) {
+template <typename SM>
+__device__ __forceinline__ void mark(SM& sm, int idx) {
   atomicOr(&sm.bitmap[idx >> 5], 1u << (idx & 31));
 }
 
@@ -543,8 +555,8 @@ __device__ __forceinline__ int row_n(const TopkArgs& a, int r) {
 }
 
 // Row r's top-512 by its C CTAs; this is CTA kq of them; n_row = row_n(a, r).
-template <int C>                   // CTAs per row: 1, 2, 4 or 8
-__device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, int kq, int n_row) {
+template <int C, typename SM>  // CTAs per row: 1, 2, 4 or 8; the shared memory's layout
+__device__ __forceinline__ void topk_row(const TopkArgs& a, SM& sm, int r, int kq, int n_row) {
   const RowGroup<C> grp;
   const int tid = threadIdx.x, lane = lane_id();
   const float* row = a.scores + (size_t)r * a.ld;
@@ -566,6 +578,37 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
   const float4* sl4 = reinterpret_cast<const float4*>(sl);   // lo is a multiple of 4
   const int n4 = len >> 2;
   auto fold = [](float v) { return v == 0.0f ? 0.0f : v; };   // -0 onto +0
+  // the slice's values: from the staged copy in shared memory, or from global
+  // memory (L2)
+  constexpr bool kCached = SM::kCacheFloats > 0;
+  auto ld4 = [&](int i) -> float4 {
+    if constexpr (kCached) return reinterpret_cast<const float4*>(sm.cache)[i];
+    else return __ldg(sl4 + i);
+  };
+  auto ld1 = [&](int i) -> float {
+    if constexpr (kCached) return sm.cache[i];
+    else return __ldg(sl + i);
+  };
+  if constexpr (kCached) {
+    // one bulk copy of the slice rounded up to 16 bytes (the row's stride is a
+    // multiple of 4 entries, so the copy stays inside the row)
+    const int len4 = (len + 3) & ~3;
+    const uint32_t bytes = len4 <= SM::kCacheFloats ? (uint32_t)len4 * 4u : 0u;
+    if (len4 > SM::kCacheFloats && tid == 0) raise_flag(a.status, CSA_FLAG_ROW_INVALID);
+    if (tid == 0) {
+      mbar_init(&sm.cache_bar, 1);
+      fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0 && bytes > 0u) {
+      mbar_expect_tx(&sm.cache_bar, bytes);
+      bulk_load(sm.cache, sl, bytes, &sm.cache_bar);
+    }
+    if (bytes > 0u && !mbar_wait(&sm.cache_bar, 0)) {
+      raise_flag(a.status, CSA_FLAG_TIMEOUT);
+      (void)mbar_wait(&sm.cache_bar, 0);       // the copy is not left in flight
+    }
+  }
 
   // ---- pass 1: value range of the slice, then of the row ----------------------------
   float vmin = INFINITY, vmax = -INFINITY;
@@ -574,7 +617,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = b0 + j * kThreads;
-      v[j] = i < n4 ? __ldg(sl4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      v[j] = i < n4 ? ld4(i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -585,7 +628,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
     }
   }
   for (int i = 4 * n4 + tid; i < len; i += kThreads) {
-    const float v = __ldg(sl + i);
+    const float v = ld1(i);
     vmin = fminf(vmin, v);
     vmax = fmaxf(vmax, v);
   }
@@ -598,7 +641,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
   vmin = INFINITY;
   vmax = -INFINITY;
   for (int q = 0; q < C; ++q) {
-    const RowSmem* rs = grp.at(&sm, q);
+    const SM* rs = grp.at(&sm, q);
     vmin = fminf(vmin, rs->fmin);
     vmax = fmaxf(vmax, rs->fmax);
   }
@@ -620,7 +663,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int i = b0 + j * kThreads;
-        v[j] = i < n4 ? __ldg(sl4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        v[j] = i < n4 ? ld4(i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -632,7 +675,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
         }
       }
     }
-    for (int i = 4 * n4 + tid; i < len; i += kThreads) atomicAdd(&sm.hist[bin_of(__ldg(sl + i))], 1u);
+    for (int i = 4 * n4 + tid; i < len; i += kThreads) atomicAdd(&sm.hist[bin_of(ld1(i))], 1u);
   }
   grp.sync();                                  // histograms complete; range reads done
   if (!binning) {
@@ -678,7 +721,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
     __syncthreads();
     const int tb = (int)sm.sel_bin;
     const uint32_t n_gt = sm.sel_need, n_tie = sm.sel_tie;
-    if (n_tie > (uint32_t)kTieCap) {
+    if (n_tie > (uint32_t)SM::kTieCapacity) {
       grp.sync();                              // every remote histogram read is done
       if (kq != 0) return;         // CTA 0 alone: the whole-row radix below
     } else {
@@ -691,8 +734,9 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
       // value's bin is 0
       const float tbf1 = (float)(tb + 1);
       const bool gt_possible = tb < kRowBins - 1;
+      // (-0 and +0 class alike here: x differs at most in the sign of a zero)
       auto classify = [&](float v, bool valid, uint32_t bit, uint32_t& gtm, uint32_t& tiem) {
-        const float x = (fold(v) - vmin) * scale;
+        const float x = (v - vmin) * scale;
         if (!valid) return;
         if (gt_possible && x >= tbf1) gtm |= bit;
         else if (tb == 0 || x >= tbf) tiem |= bit;
@@ -721,7 +765,16 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
           const int j = __ffs(m) - 1;
           sm.gt_idx[bg++] = lo + ibase + (j >> 2) * (4 * kThreads) + (j & 3);
         }
-        if (__any_sync(0xFFFFFFFFu, tiem != 0u)) {
+        if constexpr (kCached) {
+          // the staged slice gives a value by its index: one pass over the set bits
+          for (uint32_t m = tiem; m != 0u; m &= m - 1u) {
+            const int j = __ffs(m) - 1;
+            const int e = ibase + (j >> 2) * (4 * kThreads) + (j & 3);
+            sm.tie_key[bt] = score_key(fold(sm.cache[e]));
+            sm.tie_idx[bt] = lo + e;
+            ++bt;
+          }
+        } else if (__any_sync(0xFFFFFFFFu, tiem != 0u)) {
 #pragma unroll
           for (int j = 0; j < kCnt; ++j)
             if (tiem & (1u << j)) {
@@ -739,7 +792,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
         for (int j = 0; j < 4; ++j) {
           const int i = base4 + tid + j * kThreads;
           const bool valid = i < n4;
-          const float4 x = valid ? __ldg(sl4 + i) : make_float4(vmin, vmin, vmin, vmin);
+          const float4 x = valid ? ld4(i) : make_float4(vmin, vmin, vmin, vmin);
           v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
 #pragma unroll
           for (int c = 0; c < 4; ++c) classify(v[4 * j + c], valid, 1u << (4 * j + c), gtm, tiem);
@@ -750,7 +803,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
       if (tid < 32) {                              // the slice's last (len mod 4) entries
         const int i = 4 * n4 + lane;
         const bool valid = i < len;
-        float v1[1] = {valid ? __ldg(sl + i) : vmin};
+        float v1[1] = {valid ? ld1(i) : vmin};
         uint32_t gtm = 0u, tiem = 0u;
         classify(v1[0], valid, 1u, gtm, tiem);
         collect(IntConst<1>(), gtm, tiem, v1, i);
@@ -760,7 +813,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, RowSmem& sm, int r, 
       if (kq != 0) {
         uint32_t og = 0, ot = 0;
         for (int q = 0; q < kq; ++q) {
-          const RowSmem* rs = grp.at(&sm, q);
+          const SM* rs = grp.at(&sm, q);
           og += rs->gt_cnt;
           ot += rs->tie_cnt;
         }
@@ -892,11 +945,15 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(TopkArgs a) {
 // the work return at once.
 constexpr int kPackC = 4;
 constexpr int kPackLong = 16384;
+// Rows of up to kPackC * kPackLong entries, slices of up to kPackLong staged in
+// shared memory; 3072 cut-bin entries keep two CTAs per SM (106 KB each).
+using PackSmem = RowSmemT<kPackC * kPackLong, 3072, kPackLong>;
+static_assert(2 * (sizeof(PackSmem) + 1024) <= 228 * 1024, "two packed CTAs per SM");
 
 __global__ void __launch_bounds__(kThreads) k_topk_packed(TopkArgs a) {
   pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem[];
-  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem);
+  PackSmem& sm = *reinterpret_cast<PackSmem*>(smem);
   const int tid = threadIdx.x;
   const int c = (int)blockIdx.x / kPackC, kq = (int)cg::this_cluster().block_rank();
   auto row_len = [&](int r) {
@@ -1129,7 +1186,7 @@ cudaError_t launch_topk(const TopkArgs& a, Order order, cudaStream_t stream) {
   const bool row_ok = (a.ld % 4) == 0 && ((uintptr_t)a.scores & 15u) == 0;
   if (row_ok && a.max_n > kPackLong && a.max_n <= kPackC * kPackLong) {
     // rows of up to 64K entries: long rows a cluster each, short ones a CTA each
-    const size_t smem = sizeof(RowSmem);
+    const size_t smem = sizeof(PackSmem);
     cudaError_t e = cudaFuncSetAttribute(k_topk_packed, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
