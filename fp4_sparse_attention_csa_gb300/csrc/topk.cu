@@ -377,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int sli
 // ---------------------------------------------------------------------------
 // Rows up to kRowMax entries: a cluster of C CTAs per row (C set at launch),
 // CTA k streaming the contiguous slice [k*S, min(n, (k+1)*S)) of the
-// L2-resident row with 16-byte loads (S a multiple of 4).  The cluster
+// L2-resident row with 16-byte loads (S a multiple of 4), or reading it from
+// shared memory where its layout stages the slice (the packed launch).  The cluster
 //   1. reduces the slices' value ranges through distributed shared memory,
 //   2. sums the CTAs' kRowBins-bin value histograms (read remotely); every CTA
 //      derives the same bin tb holding rank 512, the count above it and the
@@ -389,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(TopkArgs a, int C, int sli
 // and CTA 0 picks the cut bin's entries by (score desc, index asc) -- by
 // pairwise rank when there are few, else by radix select -- marks every
 // selected index in a bitmap of the row and writes the bitmap out in index
-// order.  A cut bin with more than kTieCap entries (many ties) or a non-finite
-// range falls back to a whole-row radix select in CTA 0.  A CTA leaves only
+// order.  A cut bin with more entries than the layout's tie capacity (many
+// ties) or a non-finite range falls back to a whole-row radix select in CTA 0.  A CTA leaves only
 // after a cluster barrier that follows every remote access to its shared memory.
 constexpr int kRowMax = 262144;
 constexpr int kRowBins = 2048;
