@@ -747,7 +747,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, SM& sm, int r, int k
       // then the writes -- the indices above the cut bin by their set bits, the
       // cut bin's keys and indices (few) only in warps that hold some
       auto collect = [&](auto cnt_c, uint32_t gtm, uint32_t tiem, const float* v, int ibase) {
-        constexpr int kCnt = decltype(cnt_c)::value;
+        [[maybe_unused]] constexpr int kCnt = decltype(cnt_c)::value;
         const uint32_t ng = (uint32_t)__popc(gtm), nt = (uint32_t)__popc(tiem);
         uint32_t ig = ng, it = nt;                  // inclusive warp scans
 #pragma unroll
