@@ -132,6 +132,52 @@ def test_attention_skips_bad_entries_and_flags_them():
     parity.check_attention(out[1].float().cpu().numpy(), o_ref, lse[1].cpu().numpy(), l_ref)
 
 
+def test_attention_tail_split_survives_a_flagged_row():
+    """A tail row (rows past one wave of one CTA per SM, split over several
+    CTAs that merge through the workspace) with a selected index outside its
+    visible range: the row is flagged and merged without that entry, the other
+    rows are bit-equal to a clean call, and a clean call on the same workspace
+    afterwards is bit-equal again (every tail CTA counted itself in, so the
+    arrival counters are back at zero)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    R = sms + 3
+    ctx = [700 + 37 * i for i in range(R)]
+    wl, st, s = _state("tlf", 74, ctx, H=16, Hi=16)
+    st.step_decode(s)
+    rc, flags = csa.csa_check_device_status(s["ws"])
+    assert rc == 0 and flags == 0
+    topk = s["topk"].clone()
+    ws = torch.zeros(csa.csa_workspace_size(csa.OP_SPARSE_ATTN, wl.R, wl.max_entries, wl.H), dtype=torch.uint8,
+                     device="cuda")
+    assert ws.numel() > 256                              # the tail split's partials fit
+
+    def run(tk):
+        out = torch.full((wl.R, wl.H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((wl.R, wl.H), float("nan"), device="cuda")
+        csa.csa_sparse_attn(st.cache, st.window, s["rows"], tk, wl.H, s["q"], wl.softmax_scale, out, lse, ws)
+        rc, flags = csa.csa_check_device_status(ws)
+        return out, lse, rc, flags
+
+    out0, lse0, rc, flags = run(topk)
+    assert rc == 0 and flags == 0
+    r = R - 1                                            # a row of the split last wave
+    n = wl.row_entries()
+    bad = topk.clone()
+    bad[r, 7] = int(n[r]) + 5
+    out, lse, rc, flags = run(bad)
+    assert rc == 5 and (flags & csa.FLAG_TOPK_OOB), (rc, flags)
+    assert torch.equal(out[:r], out0[:r]) and torch.equal(lse[:r], lse0[:r])
+    ref = oracle.build_cache(wl)
+    _, _, q = wl.step_queries()
+    sel = topk[r].cpu().numpy().copy()
+    sel[7] = -1
+    o_ref, l_ref = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], sel, q[r], wl.softmax_scale)
+    parity.check_attention(out[r].float().cpu().numpy(), o_ref, lse[r].cpu().numpy(), l_ref)
+    out2, lse2, rc, flags = run(topk)
+    assert rc == 0 and flags == 0
+    assert torch.equal(out2, out0) and torch.equal(lse2, lse0)
+
+
 def test_topk_flags_a_row_longer_than_its_bound():
     g = np.random.default_rng(74)
     R, ld = 3, 4096
