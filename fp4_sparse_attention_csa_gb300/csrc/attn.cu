@@ -763,13 +763,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
   const int d = 128 * hsel + 32 * q4 + lane;
   const uint32_t obase = tO + lane_off + hsel * 64;
   if (splits == 1) {
-    // O[h][d] = O^T[d][h] / l[h] as bf16, staged in sm.k (free after the last PV)
+    // O[h][d] = O^T[d][h] / l[h] as bf16, straight to global memory: a warp
+    // holds 32 consecutive dimensions of a head, 64 contiguous bytes per store
     if (tid < H) {
       const float l = sm.l_run[tid];
       sm.inv_l[tid] = (have && l > 0.0f) ? 1.0f / l : 0.0f;
     }
     __syncthreads();
-    __nv_bfloat16* ostage = reinterpret_cast<__nv_bfloat16*>(sm.k);
+    uint16_t* orow = a.out + (size_t)r * H * D + d;
     for (int h0 = 0; h0 < H; h0 += 16) {
       uint32_t v[16];
       if (have) {
@@ -780,14 +781,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn(AttnArgs a) {
         for (int i = 0; i < 16; ++i) v[i] = 0u;
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        ostage[(h0 + i) * D + d] = __float2bfloat16_rn(__uint_as_float(v[i]) * sm.inv_l[h0 + i]);
-    }
-    __syncthreads();
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(ostage);
-      uint4* dst = reinterpret_cast<uint4*>(a.out + (size_t)r * H * D);
-      for (int i = tid; i < H * D / 8; i += kThreads) dst[i] = src[i];
+      for (int i = 0; i < 16; ++i) {
+        const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[i]) * sm.inv_l[h0 + i]);
+        orow[(size_t)(h0 + i) * D] = *reinterpret_cast<const uint16_t*>(&o);
+      }
     }
     if (a.lse && tid < H) {
       const float l = sm.l_run[tid];
