@@ -115,8 +115,31 @@ csa_status_t run_score(const csa_cache_t* cache, const csa_rows_t* rows, int32_t
   return from_cuda(launch_index_score(a, num_sms(), prep_order, stream));
 }
 
+// The attention's tail split for these rows (tail_splits 1: none): the bytes
+// of ws from tail_off on hold its counters and partials when they fit.
+AttnArgs tail_args(const csa_rows_t* rows, int32_t H, void* ws, size_t tail_off, size_t ws_bytes, int sms) {
+  AttnArgs t{};
+  t.num_rows = rows->num_rows;
+  t.H = H;
+  t.splits = attn_choose_splits(rows->num_rows, sms);
+  attn_tail_setup(t, ws_bytes > tail_off ? static_cast<uint8_t*>(ws) + tail_off : nullptr,
+                  ws_bytes > tail_off ? ws_bytes - tail_off : 0, sms);
+  return t;
+}
+
+// Zeroes the tail split's arrival counters, if the call will split a tail;
+// enqueued before the call's first kernel.  Their place in the workspace
+// depends on the call's shapes, so a workspace reused with other shapes may
+// hold anything there.
+csa_status_t zero_tail_counters(const csa_rows_t* rows, int32_t H, void* ws, size_t tail_off, size_t ws_bytes,
+                                cudaStream_t stream) {
+  const AttnArgs t = tail_args(rows, H, ws, tail_off, ws_bytes, num_sms());
+  if (t.tail_splits < 2) return CSA_OK;
+  return from_cuda(cudaMemsetAsync(t.row_done, 0, sizeof(uint32_t) * (size_t)(t.num_rows - t.tail_row0), stream));
+}
+
 // ws_bytes: the workspace's size; the bytes from tail_off on hold the tail
-// split's partials when they fit (otherwise the rows run unsplit).
+// split's counters and partials when they fit (otherwise the rows run unsplit).
 csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, const csa_rows_t* rows,
                       const int32_t* topk, int32_t H, const void* q, float softmax_scale, void* out, float* lse,
                       const csa_opts_t* opts, void* ws, size_t tail_off, size_t ws_bytes, Order order,
@@ -146,11 +169,13 @@ csa_status_t run_attn(const csa_cache_t* cache, const csa_window_t* window, cons
   a.softmax_scale = softmax_scale;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
-  const int sms = num_sms();
-  a.splits = attn_choose_splits(rows->num_rows, sms);
   a.status = static_cast<uint32_t*>(ws);
-  attn_tail_setup(a, ws_bytes > tail_off ? static_cast<uint8_t*>(ws) + tail_off : nullptr,
-                  ws_bytes > tail_off ? ws_bytes - tail_off : 0, sms);
+  const AttnArgs t = tail_args(rows, H, ws, tail_off, ws_bytes, num_sms());
+  a.splits = t.splits;
+  a.tail_row0 = t.tail_row0;
+  a.tail_splits = t.tail_splits;
+  a.part = t.part;
+  a.row_done = t.row_done;
   return from_cuda(launch_sparse_attn(a, order, stream));
 }
 
@@ -368,6 +393,7 @@ csa_status_t csa_sparse_attn_ex(const csa_cache_t* cache, const csa_window_t* wi
   const bool planned = opts && opts->plan_in;
   if ((!topk_idx && !planned) || !q || !out || !aligned(q, 16) || !aligned(out, 16)) return CSA_ERR_INVALID_ARGUMENT;
   if (!ws || ws_bytes < kStatusBytes || !aligned(ws, 256)) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  if ((s = zero_tail_counters(rows, n_heads, ws, kStatusBytes, ws_bytes, stream)) != CSA_OK) return s;
   return run_attn(cache, window, rows, topk_idx, n_heads, q, softmax_scale, out, lse, opts, ws, kStatusBytes, ws_bytes,
                   Order::kStream,
                   stream);
@@ -390,6 +416,9 @@ csa_status_t csa_decode_ex(const csa_cache_t* cache, const csa_window_t* window,
   if ((s = check_attn_opts(opts, false)) != CSA_OK) return s;
   if (opts && opts->candidate_blocks > 0 && rows->max_entries > kTwoLevelMaxEntries) return CSA_ERR_UNSUPPORTED;
   if (rows->num_rows == 0) return s;
+  if ((s = zero_tail_counters(rows, n_heads, ws, decode_layout(rows->num_rows, rows->max_entries, n_heads).tail,
+                              ws_bytes, stream)) != CSA_OK)
+    return s;
   return run_decode(cache, window, rows, n_idx_heads, q_idx, w, n_heads, q, softmax_scale, out, lse, topk_out, opts,
                     ws, ws_bytes, Order::kStream, stream);
 }
@@ -418,6 +447,10 @@ csa_status_t csa_step_ex(const csa_cache_t* cache, const csa_window_t* window, c
     return s;
   if ((s = check_attn_opts(opts, false)) != CSA_OK) return s;
   if (opts && opts->candidate_blocks > 0 && rows->max_entries > kTwoLevelMaxEntries) return CSA_ERR_UNSUPPORTED;
+  if (rows->num_rows > 0 &&
+      (s = zero_tail_counters(rows, n_heads, ws, decode_layout(rows->num_rows, rows->max_entries, n_heads).tail,
+                              ws_bytes, stream)) != CSA_OK)
+    return s;
   if ((s = from_cuda(launch_append(a, stream))) != CSA_OK) return s;
   if (rows->num_rows == 0) return CSA_OK;
   // With an append kernel in flight, the score prep is chained to it: it reads

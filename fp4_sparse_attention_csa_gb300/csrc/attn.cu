@@ -1050,7 +1050,7 @@ size_t attn_tail_ws_bytes(int32_t num_rows, int32_t H, int num_sms) {
   int32_t row0 = 0;
   const int32_t s = attn_tail_plan(num_rows, num_sms, &row0);
   if (s < 2) return 0;
-  return tail_part_bytes((size_t)(num_rows - row0) * s, H) + align256((size_t)(num_rows - row0) * sizeof(uint32_t));
+  return align256((size_t)(num_rows - row0) * sizeof(uint32_t)) + tail_part_bytes((size_t)(num_rows - row0) * s, H);
 }
 
 void attn_tail_setup(AttnArgs& a, void* base, size_t bytes, int num_sms) {
@@ -1062,11 +1062,12 @@ void attn_tail_setup(AttnArgs& a, void* base, size_t bytes, int num_sms) {
   int32_t row0 = 0;
   const int32_t s = attn_tail_plan(a.num_rows, num_sms, &row0);
   if (s < 2 || bytes < attn_tail_ws_bytes(a.num_rows, a.H, num_sms)) return;
+  // the counters first, then the partials
   uint8_t* p = static_cast<uint8_t*>(base);
   a.tail_row0 = row0;
   a.tail_splits = s;
-  a.part = reinterpret_cast<float*>(p);
-  a.row_done = reinterpret_cast<uint32_t*>(p + tail_part_bytes((size_t)(a.num_rows - row0) * s, a.H));
+  a.row_done = reinterpret_cast<uint32_t*>(p);
+  a.part = reinterpret_cast<float*>(p + align256((size_t)(a.num_rows - row0) * sizeof(uint32_t)));
 }
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, Order order, cudaStream_t stream) {

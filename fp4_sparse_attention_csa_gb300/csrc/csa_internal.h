@@ -134,7 +134,7 @@ struct AttnArgs {
   // each and merge through the workspace; tail_splits == 1: none.
   int32_t tail_row0, tail_splits;
   float* part;              // [tail CTAs][H][512] unnormalised O, then [tail CTAs][2][H] (m, l)
-  uint32_t* row_done;       // [num_rows - tail_row0] CTAs of a tail row that finished; zero between calls
+  uint32_t* row_done;       // [num_rows - tail_row0] CTAs of a tail row that finished; zeroed by the call
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, Order order, cudaStream_t stream);
 int32_t attn_choose_splits(int32_t num_rows, int num_sms);
@@ -144,8 +144,9 @@ int32_t attn_choose_splits(int32_t num_rows, int num_sms);
 int32_t attn_tail_plan(int32_t num_rows, int num_sms, int32_t* tail_row0);
 // Workspace bytes of the tail split's partials and arrival counters (0: none).
 size_t attn_tail_ws_bytes(int32_t num_rows, int32_t H, int num_sms);
-// Sets a's tail split (tail_row0, tail_splits, part, row_done) when the rows
-// have a tail and `bytes` at `base` hold its partials; otherwise no tail split.
+// Sets a's tail split (tail_row0, tail_splits, row_done, part: the counters
+// first) when the rows have a tail and `bytes` at `base` hold it; otherwise no
+// tail split.  The counters are zeroed before the call's first kernel.
 void attn_tail_setup(AttnArgs& a, void* base, size_t bytes, int num_sms);
 
 }  // namespace csa

@@ -155,9 +155,9 @@ typedef struct {
  * CTA per SM are split over several CTAs that merge through the workspace
  * (see csa_sparse_attn); a workspace without that room (at least the size
  * computed for a device with num_rows or more SMs) runs every row whole.
- * A workspace is zero-filled before its first use: its status word and the
- * attention's arrival counters start at zero, and every call leaves the
- * counters at zero.  0 = bad op. */
+ * A workspace is zero-filled before its first use (its status word starts at
+ * zero); the tail split's arrival counters are zeroed by each call that uses
+ * them, so a workspace can serve calls of different shapes.  0 = bad op. */
 enum { CSA_OP_APPEND = 0, CSA_OP_INDEX_SCORE = 1, CSA_OP_TOPK = 2,
        CSA_OP_SPARSE_ATTN = 3, CSA_OP_DECODE = 4 };
 CSA_API size_t csa_workspace_size(int32_t op, int32_t num_rows, int32_t max_entries, int32_t n_heads);

@@ -429,6 +429,52 @@ def test_attention_tail_split(H):
     assert np.array_equal(outs[0][0], outs[2][0]) and np.array_equal(outs[0][1], outs[2][1])
 
 
+def test_decode_tail_split_with_a_workspace_reused_across_shapes():
+    """One workspace serves decodes of different row counts: the tail split's
+    arrival counters sit after the scores and the top-k, so their place moves
+    with the shapes and lands on bytes an earlier call wrote; each call zeroes
+    them first.  All rows, then a prefix of them, then all rows again: every
+    output matches the oracle and the repeated call is bit-equal."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    R, Rp = sms + 40, sms + 7
+    ctx = [600 + 23 * i for i in range(R)]
+    wl = W.custom("tailws", 81, ctx, [1] * R, H=16, Hi=16, shuffle=True)
+    st = DeviceState(wl)
+    st.build_history()
+    s = st.step_inputs()
+    st.step_append(s)
+    ws = torch.zeros(max(csa.csa_workspace_size(csa.OP_DECODE, n, wl.max_entries, wl.H) for n in (R, Rp)),
+                     dtype=torch.uint8, device="cuda")
+    ref = oracle.build_cache(wl)
+    q_idx, w, q = wl.step_queries()
+    _, _, _, scores = oracle.decode(ref, wl.row_req, wl.row_pos, q_idx, w, q, wl.softmax_scale, threads=8)
+    n = wl.row_entries()
+
+    def run(k):
+        rows = csa.make_rows(s["row_req"][:k], s["row_pos"][:k], wl.max_entries, 1)
+        out = torch.full((k, wl.H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((k, wl.H), float("nan"), device="cuda")
+        topk = torch.empty((k, 512), dtype=torch.int32, device="cuda")
+        csa.csa_decode(st.cache, st.window, rows, wl.Hi, s["q_idx"][:k], s["w"][:k], wl.H, s["q"][:k],
+                       wl.softmax_scale, out, lse, topk, ws)
+        rc, flags = csa.csa_check_device_status(ws)
+        assert rc == 0 and flags == 0, flags
+        gt = topk.cpu().numpy()
+        o_ref = np.zeros((k, wl.H, 512), np.float32)
+        l_ref = np.zeros((k, wl.H), np.float32)
+        for r in range(k):
+            parity.check_topk_row(gt[r], scores[r], int(n[r]))
+            o_ref[r], l_ref[r] = oracle.attention_row(ref, wl.row_req[r], wl.row_pos[r], gt[r], q[r],
+                                                      wl.softmax_scale)
+        parity.check_attention(out.float().cpu().numpy(), o_ref, lse.cpu().numpy(), l_ref)
+        return out, lse
+
+    out0, lse0 = run(R)
+    run(Rp)
+    out2, lse2 = run(R)
+    assert torch.equal(out2.view(torch.int16), out0.view(torch.int16)) and torch.equal(lse2, lse0)
+
+
 # ------------------------------------------------------------------ decode
 @pytest.mark.parametrize("H,Hi,rows", [(16, 16, 1), (64, 64, 6), (32, 32, 2), (64, 128, 2), (16, 96, 1)])
 def test_decode_end_to_end(H, Hi, rows):
